@@ -1,0 +1,266 @@
+/*
+ * oracle.c -- plain, slow, fp64 CPU oracle for exact attention and its
+ * backward pass.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path links, loads or
+ * calls this file: it is built into liboracle.so and used by the tests, by
+ * the smoke check and by the benchmark's CPU-baseline leg.  It shares no
+ * code, header, table or helper with the CUDA library.
+ *
+ * What it computes (the plain definition the fused kernel must reproduce):
+ *
+ *   Three-step form of attention ("Reading CMU 11-868 LLM Systems:
+ *   FlashAttention", section "The scenario", slide page 5):
+ *       S = scale * Q K^T,  A = softmax(S) row-wise,  O = A V.
+ *   FlashAttention's output is "identical to standard attention" (same
+ *   post, page 15 summary; quidproquo tag page "flashattention", Hung-yi
+ *   Lee paragraph), so the oracle is that definition written out, with no
+ *   tiling and no online rescaling.
+ *
+ *   Per row i (causal: keys j > i are masked out, top-left alignment):
+ *       S_ij   = scale * sum_k q_ik k_jk
+ *       m_i    = max_j S_ij                 (only to keep exp() finite;
+ *                                            cs2680 Lecture 9, sec. 9.4)
+ *       lse_i  = m_i + ln sum_j exp(S_ij - m_i)
+ *       A_ij   = exp(S_ij - lse_i)
+ *       O_i    = sum_j A_ij v_j
+ *   lse is the per-row normalisation constant the forward pass keeps for
+ *   the backward pass (CMU 11-868 post, "Recomputation", slide page 14;
+ *   cs2680 Lecture 9, sec. 9.6).
+ *
+ *   Backward: the pages give no formulas; this is the textbook gradient of
+ *   O = softmax(scale Q K^T) V with upstream gradient dO:
+ *       dV   = A^T dO
+ *       dA   = dO V^T
+ *       D_i  = sum_j A_ij dA_ij
+ *       dS   = A o (dA - D)      (o = elementwise product, D broadcast per row)
+ *       dQ   = scale * dS K
+ *       dK   = scale * dS^T Q
+ *   lse receives no upstream gradient.
+ *
+ * Layout: every tensor is a dense row-major fp64 array [BH][N][d] (lse and
+ * D are [BH][N]).  Loops are parallelised with OpenMP over independent rows
+ * (forward, dQ) or independent key rows (dK, dV); each output element is
+ * computed by one thread with a plain sequential sum, so results do not
+ * depend on the thread count.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+int oracle_num_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+void oracle_set_num_threads(int n)
+{
+#ifdef _OPENMP
+    if (n > 0) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
+/* Number of keys row i may attend to. */
+static int64_t row_len(int64_t i, int64_t N, int causal)
+{
+    return causal ? (i + 1 < N ? i + 1 : N) : N;
+}
+
+/* Scores of row i of head h into s[0..len), returns len. */
+static int64_t scores_row(const double* q, const double* k, int64_t h, int64_t i,
+                          int64_t N, int64_t d, int causal, double scale, double* s)
+{
+    const double* qi = q + (h * N + i) * d;
+    const double* kh = k + h * N * d;
+    int64_t len = row_len(i, N, causal);
+    for (int64_t j = 0; j < len; ++j) {
+        const double* kj = kh + j * d;
+        double acc = 0.0;
+        for (int64_t c = 0; c < d; ++c) acc += qi[c] * kj[c];
+        s[j] = scale * acc;
+    }
+    return len;
+}
+
+/* lse of a row of scores: m + ln sum exp(s - m). */
+static double logsumexp_row(const double* s, int64_t len)
+{
+    double m = -INFINITY;
+    for (int64_t j = 0; j < len; ++j) if (s[j] > m) m = s[j];
+    double l = 0.0;
+    for (int64_t j = 0; j < len; ++j) l += exp(s[j] - m);
+    return m + log(l);
+}
+
+/* Forward for one (head, row): fills o_row[0..d) and returns lse. */
+static double fwd_row(const double* q, const double* k, const double* v, int64_t h,
+                      int64_t i, int64_t N, int64_t d, int causal, double scale,
+                      double* s, double* o_row)
+{
+    int64_t len = scores_row(q, k, h, i, N, d, causal, scale, s);
+    double lse = logsumexp_row(s, len);
+    const double* vh = v + h * N * d;
+    for (int64_t c = 0; c < d; ++c) o_row[c] = 0.0;
+    for (int64_t j = 0; j < len; ++j) {
+        double a = exp(s[j] - lse);
+        const double* vj = vh + j * d;
+        for (int64_t c = 0; c < d; ++c) o_row[c] += a * vj[c];
+    }
+    return lse;
+}
+
+/* O and lse for all heads and rows. */
+void oracle_attn_fwd(const double* q, const double* k, const double* v, int64_t BH,
+                     int64_t N, int64_t d, int causal, double scale, double* o,
+                     double* lse)
+{
+#pragma omp parallel
+    {
+        double* s = (double*)malloc(sizeof(double) * (size_t)(N > 0 ? N : 1));
+#pragma omp for schedule(dynamic, 16)
+        for (int64_t r = 0; r < BH * N; ++r) {
+            int64_t h = r / N, i = r % N;
+            lse[r] = fwd_row(q, k, v, h, i, N, d, causal, scale, s, o + r * d);
+        }
+        free(s);
+    }
+}
+
+/* O and lse for a selection of (head, row) pairs only: the sampled check of
+ * large workloads.  o_sel is [nsel][d], lse_sel is [nsel]. */
+void oracle_attn_fwd_rows(const double* q, const double* k, const double* v,
+                          int64_t BH, int64_t N, int64_t d, int causal, double scale,
+                          const int64_t* heads, const int64_t* rows, int64_t nsel,
+                          double* o_sel, double* lse_sel)
+{
+    (void)BH;
+#pragma omp parallel
+    {
+        double* s = (double*)malloc(sizeof(double) * (size_t)(N > 0 ? N : 1));
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t t = 0; t < nsel; ++t)
+            lse_sel[t] = fwd_row(q, k, v, heads[t], rows[t], N, d, causal, scale, s,
+                                 o_sel + t * d);
+        free(s);
+    }
+}
+
+/* The full attention matrix A = softmax(S) of every head, [BH][N][N]; masked
+ * entries are exactly 0.  For small cases only. */
+void oracle_attn_probs(const double* q, const double* k, int64_t BH, int64_t N,
+                       int64_t d, int causal, double scale, double* A)
+{
+#pragma omp parallel
+    {
+        double* s = (double*)malloc(sizeof(double) * (size_t)(N > 0 ? N : 1));
+#pragma omp for schedule(dynamic, 16)
+        for (int64_t r = 0; r < BH * N; ++r) {
+            int64_t h = r / N, i = r % N;
+            int64_t len = scores_row(q, k, h, i, N, d, causal, scale, s);
+            double lse = logsumexp_row(s, len);
+            double* Ar = A + r * N;
+            for (int64_t j = 0; j < N; ++j) Ar[j] = j < len ? exp(s[j] - lse) : 0.0;
+        }
+        free(s);
+    }
+}
+
+/*
+ * Backward.  Pass 1 (one thread per row i): scores, lse_i, A_i, dA_i,
+ * D_i = sum_j A_ij dA_ij and dQ_i = scale sum_j dS_ij k_j.  Pass 2 (one
+ * thread per key row j): A_ij and dS_ij from the same definitions, using
+ * lse_i and D_i from pass 1, then dV_j = sum_i A_ij dO_i and
+ * dK_j = scale sum_i dS_ij q_i.  Only O(N) per-row values cross between the
+ * passes; no N x N matrix is stored.
+ */
+void oracle_attn_bwd(const double* q, const double* k, const double* v,
+                     const double* dout, int64_t BH, int64_t N, int64_t d, int causal,
+                     double scale, double* dq, double* dk, double* dv)
+{
+    double* lse = (double*)malloc(sizeof(double) * (size_t)(BH * N > 0 ? BH * N : 1));
+    double* D = (double*)malloc(sizeof(double) * (size_t)(BH * N > 0 ? BH * N : 1));
+
+#pragma omp parallel
+    {
+        double* s = (double*)malloc(sizeof(double) * (size_t)(N > 0 ? N : 1));
+        double* da = (double*)malloc(sizeof(double) * (size_t)(N > 0 ? N : 1));
+#pragma omp for schedule(dynamic, 16)
+        for (int64_t r = 0; r < BH * N; ++r) {
+            int64_t h = r / N, i = r % N;
+            const double* vh = v + h * N * d;
+            const double* kh = k + h * N * d;
+            const double* doi = dout + r * d;
+            int64_t len = scores_row(q, k, h, i, N, d, causal, scale, s);
+            double l = logsumexp_row(s, len);
+            lse[r] = l;
+            double Di = 0.0;
+            for (int64_t j = 0; j < len; ++j) {
+                const double* vj = vh + j * d;
+                double acc = 0.0;
+                for (int64_t c = 0; c < d; ++c) acc += doi[c] * vj[c];
+                da[j] = acc;
+                Di += exp(s[j] - l) * acc;
+            }
+            D[r] = Di;
+            double* dqi = dq + r * d;
+            for (int64_t c = 0; c < d; ++c) dqi[c] = 0.0;
+            for (int64_t j = 0; j < len; ++j) {
+                double ds = exp(s[j] - l) * (da[j] - Di);
+                const double* kj = kh + j * d;
+                for (int64_t c = 0; c < d; ++c) dqi[c] += ds * kj[c];
+            }
+            for (int64_t c = 0; c < d; ++c) dqi[c] *= scale;
+        }
+        free(s);
+        free(da);
+    }
+
+#pragma omp parallel for schedule(dynamic, 16)
+    for (int64_t r = 0; r < BH * N; ++r) {
+        int64_t h = r / N, j = r % N;
+        const double* qh = q + h * N * d;
+        const double* kj = k + r * d;
+        const double* vj = v + r * d;
+        const double* doh = dout + h * N * d;
+        double* dkj = dk + r * d;
+        double* dvj = dv + r * d;
+        for (int64_t c = 0; c < d; ++c) { dkj[c] = 0.0; dvj[c] = 0.0; }
+        int64_t i0 = causal ? j : 0;
+        for (int64_t i = i0; i < N; ++i) {
+            const double* qi = qh + i * d;
+            const double* doi = doh + i * d;
+            double sdot = 0.0, ddot = 0.0;
+            for (int64_t c = 0; c < d; ++c) { sdot += qi[c] * kj[c]; ddot += doi[c] * vj[c]; }
+            double a = exp(scale * sdot - lse[h * N + i]);
+            double ds = a * (ddot - D[h * N + i]);
+            for (int64_t c = 0; c < d; ++c) { dvj[c] += a * doi[c]; dkj[c] += ds * qi[c]; }
+        }
+        for (int64_t c = 0; c < d; ++c) dkj[c] *= scale;
+    }
+    free(lse);
+    free(D);
+}
+
+/* Floating-point operation counts of the method, as the pages count them:
+ * the forward pass is two S x S x d matmuls, 4 S^2 d per head (cs2680
+ * Lecture 9, sec. 9.2), half of that when causal; the recomputation of the
+ * scores in the backward pass is one extra Q K^T, 2 S^2 d (sec. 9.6). */
+double oracle_fwd_flops(int64_t BH, int64_t N, int64_t d, int causal)
+{
+    double f = 4.0 * (double)BH * (double)N * (double)N * (double)d;
+    return causal ? 0.5 * f : f;
+}
+
+double oracle_recompute_flops(int64_t N, int64_t d)
+{
+    return 2.0 * (double)N * (double)N * (double)d;
+}

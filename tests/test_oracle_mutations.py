@@ -1,0 +1,107 @@
+"""Plant plausible mistakes in a copy of the oracle and check that the pins
+catch every one of them.
+
+Each mutation edits one expression of ``oracle/oracle.c`` (a dropped term, a
+wrong sign or index, a transposed operand), builds the copy into a temporary
+library and runs a battery of the pin checks against it: at least one check
+must fail.  The unmodified source must pass the same battery.  CPU only.
+"""
+import math
+import os
+import subprocess
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.c")
+
+MUTATIONS = {
+    "scores_drop_scale": ("s[j] = scale * acc;", "s[j] = acc;"),
+    "lse_drop_max": ("return m + log(l);", "return log(l);"),
+    "causal_off_by_one": ("return causal ? (i + 1 < N ? i + 1 : N) : N;",
+                          "return causal ? (i < N ? i : N) : N;"),
+    "out_uses_wrong_row": ("const double* vj = vh + j * d;\n        for (int64_t c = 0; c < d; ++c) o_row[c] += a * vj[c];",
+                           "const double* vj = vh + (len - 1 - j) * d;\n        for (int64_t c = 0; c < d; ++c) o_row[c] += a * vj[c];"),
+    "dS_wrong_sign": ("double ds = exp(s[j] - l) * (da[j] - Di);",
+                      "double ds = exp(s[j] - l) * (da[j] + Di);"),
+    "dQ_drop_scale": ("for (int64_t c = 0; c < d; ++c) dqi[c] *= scale;", ""),
+    "dK_drop_scale": ("for (int64_t c = 0; c < d; ++c) dkj[c] *= scale;", ""),
+    "dK_transposed_operand": ("dkj[c] += ds * qi[c];", "dkj[c] += ds * doi[c];"),
+    "dV_uses_dS": ("dvj[c] += a * doi[c];", "dvj[c] += ds * doi[c];"),
+    "D_drops_probability": ("Di += exp(s[j] - l) * acc;", "Di += acc;"),
+    "bwd_causal_start": ("int64_t i0 = causal ? j : 0;", "int64_t i0 = causal ? j + 1 : 0;"),
+}
+
+
+def rnd(shape, seed):
+    return np.random.default_rng(seed).standard_normal(shape)
+
+
+def battery(lib):
+    """Names of the pin checks that fail for the oracle library ``lib``."""
+    failed = []
+    B, H, N, d = 1, 2, 9, 3
+    q, k, v, do = (rnd((B, H, N, d), s) for s in (1, 2, 3, 4))
+    scale = 0.8
+    for causal in (False, True):
+        tq, tk, tv = (torch.tensor(x, requires_grad=True) for x in (q, k, v))
+        to = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, is_causal=causal, scale=scale)
+        to.backward(torch.tensor(do))
+        o, lse = oracle.attn_fwd(q, k, v, causal, scale, lib=lib)
+        if np.abs(o - to.detach().numpy()).max() > 1e-12:
+            failed.append("sdpa_O_%d" % causal)
+        s = scale * np.einsum("bhid,bhjd->bhij", q, k)
+        if causal:
+            s = np.where(np.tril(np.ones((N, N), bool)), s, -np.inf)
+        if np.abs(np.exp(lse) - np.exp(s).sum(-1)).max() > 1e-9:
+            failed.append("lse_%d" % causal)
+        dq, dk, dv = oracle.attn_bwd(q, k, v, do, causal, scale, lib=lib)
+        for name, mine, ref in (("dq", dq, tq.grad), ("dk", dk, tk.grad), ("dv", dv, tv.grad)):
+            if np.abs(mine - ref.numpy()).max() > 1e-11:
+                failed.append("sdpa_%s_%d" % (name, causal))
+        # central differences of L = sum(dO * O) along one random direction
+        dirs = [rnd(q.shape, 10 + t) for t in range(3)]
+        h = 1e-6
+        for t, g in enumerate((dq, dk, dv)):
+            args_p = [q.copy(), k.copy(), v.copy()]
+            args_m = [q.copy(), k.copy(), v.copy()]
+            args_p[t] += h * dirs[t]
+            args_m[t] -= h * dirs[t]
+            lp = (oracle.attn_fwd(*args_p, causal, scale, lib=lib)[0] * do).sum()
+            lm = (oracle.attn_fwd(*args_m, causal, scale, lib=lib)[0] * do).sum()
+            num = (lp - lm) / (2 * h)
+            ana = (g * dirs[t]).sum()
+            if abs(num - ana) > 1e-6 * max(1.0, abs(ana)):
+                failed.append("fd_%d_%d" % (t, causal))
+    o, lse = oracle.attn_fwd(q, k, v, True, scale, lib=lib)
+    if np.abs(o[:, :, 0] - v[:, :, 0]).max() > 1e-15:
+        failed.append("causal_row0")
+    o, lse = oracle.attn_fwd(q, k, v, False, 0.0, lib=lib)
+    if np.abs(o - v.mean(2, keepdims=True)).max() > 1e-12 or np.abs(lse - math.log(N)).max() > 1e-12:
+        failed.append("scale0")
+    return failed
+
+
+def _build(src_text, tmp_path, name):
+    c = tmp_path / (name + ".c")
+    c.write_text(src_text)
+    so = tmp_path / (name + ".so")
+    subprocess.run(["gcc", "-O1", "-std=c11", "-fPIC", "-shared", "-fopenmp", str(c), "-o", str(so), "-lm"],
+                   check=True)
+    return oracle.bind(str(so))
+
+
+def test_unmodified_oracle_passes_battery():
+    assert battery(oracle._load()) == []
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_planted_mistake_is_caught(name, tmp_path):
+    before, after = MUTATIONS[name]
+    text = open(SRC).read()
+    assert text.count(before) == 1, name
+    lib = _build(text.replace(before, after), tmp_path, name)
+    assert battery(lib), "mutation %s passed every pin" % name
