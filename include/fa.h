@@ -1,0 +1,130 @@
+/*
+ * fa.h -- C ABI of libfa.so: exact, IO-aware fused attention on GB300
+ * (sm_103a), forward and backward.
+ *
+ * The operation (the three-step form of "Reading CMU 11-868 LLM Systems:
+ * FlashAttention", slide page 5, with a softmax scale and an optional causal
+ * mask):
+ *
+ *     S = scale * Q K^T            (causal: S_ij = -inf for j > i)
+ *     A = softmax(S) row by row
+ *     O = A V
+ *     lse_i = ln sum_j exp(S_ij)   (natural log, of the scaled scores)
+ *
+ * The forward kernel tiles Q by rows and streams K/V blocks through shared
+ * memory with the online-softmax rescaling of cs2680 Lecture 9, sec. 9.4 and
+ * the CMU post's slide page 12; only O and lse reach HBM.  The backward
+ * kernels recompute S and P on chip from Q, K, V and lse (cs2680 Lecture 9,
+ * sec. 9.6; CMU post, slide page 14) and never store an N x N matrix.
+ *
+ * Layout (all entry points): Q, K, V, O, dO, dQ, dK, dV are dense,
+ * contiguous [B][H][N][d] arrays of bf16 (d innermost); lse and the
+ * workspace's per-row terms are [B][H][N] fp32.  Causal masking is square
+ * and top-left (row i attends to keys j <= i).
+ *
+ * Pointers: every tensor pointer is a DEVICE pointer of the current CUDA
+ * device, 16-byte aligned, owned by the caller; the library neither frees
+ * nor retains them past the call's stream work.  Calls are asynchronous on
+ * `stream` (a cudaStream_t, NULL = legacy default stream) and never
+ * synchronise, except fa_device_status().
+ *
+ * Errors: every entry point returns FA_OK (0) or a negative FA_ERR_* code.
+ * On an argument error nothing is launched and no output is touched.  A
+ * kernel whose internal pipeline wait exceeds its time limit stops early and
+ * records FA_ERR_TIMEOUT in a per-device status word; fa_device_status()
+ * reports it.
+ */
+#ifndef FA_H_
+#define FA_H_
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define FA_OK 0
+#define FA_ERR_ARG (-1)            /* null pointer, B/H/N < 1, non-finite scale, size overflow */
+#define FA_ERR_UNSUPPORTED_D (-2)  /* head dimension d not in {64, 128} */
+#define FA_ERR_ALIGN (-3)          /* a tensor pointer is not 16-byte aligned */
+#define FA_ERR_WORKSPACE (-4)      /* workspace missing, misaligned or too small */
+#define FA_ERR_DEVICE (-5)         /* current device is not sm_103 / no tcgen05, or no device */
+#define FA_ERR_LAUNCH (-6)         /* a CUDA error was raised by a launch */
+#define FA_ERR_TIMEOUT (-7)        /* a kernel's pipeline wait timed out (reported by fa_device_status) */
+
+/*
+ * Forward pass.
+ *   q, k, v : [B][H][N][d] bf16, read only.
+ *   o       : [B][H][N][d] bf16, written: O = softmax(scale Q K^T [+mask]) V,
+ *             rounded to nearest-even from fp32.
+ *   lse     : [B][H][N] fp32, written: ln sum_j exp(S_ij); the only
+ *             per-row statistic kept for the backward pass.
+ *   B, H, N : >= 1; d in {64, 128}; causal 0 or 1; scale finite (may be 0
+ *             or negative).
+ * Passes: cs2680 Lecture 9 sec. 9.4 (online softmax, running max m and
+ * denominator l, correction by exp(m - m_new)); CMU post slide page 12.
+ */
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+           int N, int d, int causal, float scale, void* stream);
+
+/*
+ * Bytes of device workspace fa_bwd needs for these sizes: an fp32 dQ
+ * accumulator of B*H*ceil(N/128)*128*d floats plus a per-row fp32 term
+ * D_i = sum_k dO_ik O_ik of B*H*ceil(N/128)*128 floats.  Returns 0 when the
+ * sizes are invalid.
+ */
+size_t fa_bwd_workspace_size(int B, int H, int N, int d);
+
+/*
+ * Backward pass of fa_fwd, by recomputation.
+ *   q, k, v, o, dout : [B][H][N][d] bf16, read only (o is fa_fwd's output).
+ *   lse              : [B][H][N] fp32 from fa_fwd, read only.
+ *   dq, dk, dv       : [B][H][N][d] bf16, written: the gradients of
+ *                      L = sum(dout * O) with respect to q, k, v.
+ *   workspace        : device buffer of at least
+ *                      fa_bwd_workspace_size(B, H, N, d) bytes, 256-byte
+ *                      aligned, owned by the caller; its contents on entry
+ *                      do not matter and on return are unspecified.  Two
+ *                      calls in flight at once need two workspaces.
+ * dQ is accumulated in fp32 with atomic adds, so its last bits may differ
+ * from run to run; dK and dV are deterministic.
+ * Passes: cs2680 Lecture 9 sec. 9.6 (recompute the scores instead of
+ * storing them); CMU post slide page 14 (the forward pass keeps only the
+ * per-row normalisation constants).
+ */
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+           const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+           int causal, float scale, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Synchronises `stream`, then returns and clears the status word of the
+ * current device: FA_OK, FA_ERR_TIMEOUT if a kernel gave up on a pipeline
+ * wait since the last call, or FA_ERR_LAUNCH if the stream holds a CUDA
+ * error.  If `site` is not NULL it receives the identifier of the first wait
+ * that timed out (0 if none).
+ */
+int fa_device_status(void* stream, int* site);
+
+/* A static, human-readable description of a status code. */
+const char* fa_status_string(int status);
+
+/*
+ * The order in which the forward kernel's persistent CTAs take work items.
+ * A work item is one (b*H + h, q-tile pair) unit: 256 query rows of one
+ * head.  Writes up to max_items entries of item_bh, item_pair and
+ * item_cost (the item's number of 128-key tiles summed over its two query
+ * tiles) and returns the number of items, or a negative FA_ERR_* code.
+ * Causal work is ordered longest first (the LPT rule of the CMU post's
+ * slide pages 27-46); host-only, needs no device.
+ */
+int fa_fwd_schedule(int B, int H, int N, int causal, int* item_bh, int* item_pair,
+                    int* item_cost, int max_items);
+
+/* Library version, for the loader's sanity check. */
+int fa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_H_ */

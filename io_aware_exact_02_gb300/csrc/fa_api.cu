@@ -1,0 +1,257 @@
+// fa_api.cu -- the C-ABI front end of libfa.so: argument checks, TMA tensor
+// maps, the per-device status word and the exported entry points declared in
+// include/fa.h.  No entry point allocates device memory; fa_bwd uses the
+// caller's workspace.
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstddef>
+#include <cstdint>
+#include <mutex>
+
+#include "fa_internal.h"
+
+namespace fa {
+
+// The status word: [0] = first error code a kernel recorded, [1] = the wait
+// site that raised it.  One per device, part of the module's static data.
+__device__ int g_status[2];
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+  bool checked = false;
+  bool supported = false;
+  int* status = nullptr;  // device address of g_status
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+// Per-device setup: architecture check and the status word's address.
+int device_state(DeviceState** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return FA_ERR_DEVICE;
+  }
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceState& s = g_dev[dev];
+  if (!s.checked) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return FA_ERR_DEVICE;
+    }
+    s.supported = (major == 10 && minor == 3);
+    if (s.supported) {
+      void* addr = nullptr;
+      if (cudaGetSymbolAddress(&addr, g_status) != cudaSuccess) {
+        cudaGetLastError();
+        return FA_ERR_DEVICE;
+      }
+      s.status = static_cast<int*>(addr);
+    }
+    s.checked = true;
+  }
+  if (!s.supported) return FA_ERR_DEVICE;
+  *out = &s;
+  return FA_OK;
+}
+
+int get_encode(PFN_cuTensorMapEncodeTiled_v12000* fn) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_encode) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || f == nullptr) {
+      cudaGetLastError();
+      return FA_ERR_DEVICE;
+    }
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  }
+  *fn = g_encode;
+  return FA_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Shared checks of the shape arguments.
+int check_shape(int B, int H, int N, int d, float scale) {
+  if (B < 1 || H < 1 || N < 1) return FA_ERR_ARG;
+  if (!std::isfinite(scale)) return FA_ERR_ARG;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED_D;
+  // Element counts of a [B][H][Npad][d] array must fit in int64 and the
+  // tensor map's 32-bit coordinates must reach every row.
+  const long long bh = (long long)B * H;
+  if (bh > (1LL << 30)) return FA_ERR_ARG;
+  const long long npad = (long long)ceil_div(N, kTile) * kTile;
+  if ((double)bh * (double)npad * (double)d > 9.0e18) return FA_ERR_ARG;
+  if ((unsigned long long)bh * (unsigned long long)ceil_div(N, kPairRows) > 0x7fffffffULL)
+    return FA_ERR_ARG;
+  return FA_OK;
+}
+
+}  // namespace
+
+int make_tmap_bhnd(const void* base, int BH, int N, int d, CUtensorMap* out) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc;
+  int rc = get_encode(&enc);
+  if (rc != FA_OK) return rc;
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
+  cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)N * d * 2};
+  cuuint32_t box[3] = {64, kTile, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = enc(out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+                   strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FA_OK : FA_ERR_ARG;
+}
+
+}  // namespace fa
+
+using namespace fa;
+
+extern "C" {
+
+int fa_version(void) { return 1; }
+
+const char* fa_status_string(int status) {
+  switch (status) {
+    case FA_OK: return "ok";
+    case FA_ERR_ARG: return "invalid argument (null pointer, size < 1, non-finite scale or overflow)";
+    case FA_ERR_UNSUPPORTED_D: return "unsupported head dimension (d must be 64 or 128)";
+    case FA_ERR_ALIGN: return "tensor pointer not 16-byte aligned";
+    case FA_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case FA_ERR_DEVICE: return "no usable device (needs sm_103 with tcgen05)";
+    case FA_ERR_LAUNCH: return "CUDA launch error";
+    case FA_ERR_TIMEOUT: return "a kernel pipeline wait timed out";
+    default: return "unknown status";
+  }
+}
+
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
+           int d, int causal, float scale, void* stream) {
+  if (!q || !k || !v || !o || !lse) return FA_ERR_ARG;
+  if (causal != 0 && causal != 1) return FA_ERR_ARG;
+  int rc = check_shape(B, H, N, d, scale);
+  if (rc != FA_OK) return rc;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+    return FA_ERR_ALIGN;
+  DeviceState* ds;
+  if ((rc = device_state(&ds)) != FA_OK) return rc;
+  const int BH = B * H;
+  CUtensorMap tq, tk, tv;
+  if ((rc = make_tmap_bhnd(q, BH, N, d, &tq)) != FA_OK) return rc;
+  if ((rc = make_tmap_bhnd(k, BH, N, d, &tk)) != FA_OK) return rc;
+  if ((rc = make_tmap_bhnd(v, BH, N, d, &tv)) != FA_OK) return rc;
+  FwdParams p;
+  p.o = o;
+  p.lse = lse;
+  p.status = ds->status;
+  p.BH = BH;
+  p.N = N;
+  p.n_kv = ceil_div(N, kTile);
+  p.n_pairs = ceil_div(N, kPairRows);
+  p.causal = causal;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  return launch_fwd(tq, tk, tv, p, d, static_cast<cudaStream_t>(stream));
+}
+
+size_t fa_bwd_workspace_size(int B, int H, int N, int d) {
+  if (check_shape(B, H, N, d, 1.0f) != FA_OK) return 0;
+  const size_t rows = (size_t)B * H * (size_t)ceil_div(N, kTile) * kTile;
+  size_t acc = rows * (size_t)d * sizeof(float);
+  acc = (acc + 255) & ~(size_t)255;
+  return acc + rows * sizeof(float);
+}
+
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+           const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d, int causal,
+           float scale, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv) return FA_ERR_ARG;
+  if (causal != 0 && causal != 1) return FA_ERR_ARG;
+  int rc = check_shape(B, H, N, d, scale);
+  if (rc != FA_OK) return rc;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dout) ||
+      !aligned16(lse) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+    return FA_ERR_ALIGN;
+  const size_t need = fa_bwd_workspace_size(B, H, N, d);
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || workspace_bytes < need)
+    return FA_ERR_WORKSPACE;
+  DeviceState* ds;
+  if ((rc = device_state(&ds)) != FA_OK) return rc;
+  const int BH = B * H;
+  CUtensorMap tq, tk, tv, tdo;
+  if ((rc = make_tmap_bhnd(q, BH, N, d, &tq)) != FA_OK) return rc;
+  if ((rc = make_tmap_bhnd(k, BH, N, d, &tk)) != FA_OK) return rc;
+  if ((rc = make_tmap_bhnd(v, BH, N, d, &tv)) != FA_OK) return rc;
+  if ((rc = make_tmap_bhnd(dout, BH, N, d, &tdo)) != FA_OK) return rc;
+  const size_t rows = (size_t)BH * (size_t)ceil_div(N, kTile) * kTile;
+  size_t acc = (rows * (size_t)d * sizeof(float) + 255) & ~(size_t)255;
+  BwdParams p;
+  p.o = o;
+  p.dout = dout;
+  p.lse = lse;
+  p.dq = dq;
+  p.dk = dk;
+  p.dv = dv;
+  p.dq_acc = static_cast<float*>(workspace);
+  p.delta = reinterpret_cast<float*>(static_cast<char*>(workspace) + acc);
+  p.status = ds->status;
+  p.BH = BH;
+  p.N = N;
+  p.n_kv = ceil_div(N, kTile);
+  p.causal = causal;
+  p.scale = scale;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  return launch_bwd(tq, tk, tv, tdo, p, d, static_cast<cudaStream_t>(stream));
+}
+
+int fa_device_status(void* stream, int* site) {
+  if (site) *site = 0;
+  DeviceState* ds;
+  int rc = device_state(&ds);
+  if (rc != FA_OK) return rc;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    cudaGetLastError();
+    return FA_ERR_LAUNCH;
+  }
+  int h[2] = {0, 0};
+  const int zero[2] = {0, 0};
+  if (cudaMemcpyFromSymbol(h, g_status, sizeof(h)) != cudaSuccess ||
+      cudaMemcpyToSymbol(g_status, zero, sizeof(zero)) != cudaSuccess) {
+    cudaGetLastError();
+    return FA_ERR_LAUNCH;
+  }
+  if (site) *site = h[1];
+  return h[0];
+}
+
+int fa_fwd_schedule(int B, int H, int N, int causal, int* item_bh, int* item_pair,
+                    int* item_cost, int max_items) {
+  if (causal != 0 && causal != 1) return FA_ERR_ARG;
+  int rc = check_shape(B, H, N, 64, 1.0f);
+  if (rc != FA_OK) return rc;
+  const int BH = B * H;
+  const int n_pairs = ceil_div(N, kPairRows);
+  const int n_kv = ceil_div(N, kTile);
+  const long long total = (long long)BH * n_pairs;
+  for (long long t = 0; t < total && t < max_items; ++t) {
+    int bh, pair;
+    fwd_item((int)t, BH, n_pairs, &bh, &pair);
+    if (item_bh) item_bh[t] = bh;
+    if (item_pair) item_pair[t] = pair;
+    if (item_cost)
+      item_cost[t] = fwd_kv_tiles(2 * pair, n_kv, causal) + fwd_kv_tiles(2 * pair + 1, n_kv, causal);
+  }
+  return (int)total;
+}
+
+}  // extern "C"

@@ -1,0 +1,412 @@
+// fa_fwd.cu -- forward pass of exact attention on sm_103a.
+//
+// One CTA computes 256 query rows (two 128-row Q tiles) of one head.  It
+// keeps both Q tiles in shared memory, streams the head's K and V tiles
+// through a ring of shared-memory slots filled by TMA, and never writes a
+// score to HBM: S lives in tensor memory, P replaces it there as bf16, and
+// only O and the per-row logsumexp are stored (cs2680 Lecture 9, sec. 9.2 and
+// 9.4; "Reading CMU 11-868 LLM Systems: FlashAttention", slide pages 9-12).
+//
+// Warp roles (320 threads):
+//   warps 0-3  softmax for Q tile 0 (thread r owns row r of the tile)
+//   warps 4-7  softmax for Q tile 1
+//   warp 8     TMA producer: Q tiles once, then K_0, V_0, K_1, V_1, ...
+//   warp 9     MMA issuer (one thread) and TMEM owner
+// The two softmax warpgroups ping-pong: while one exponentiates its tile
+// the tensor core computes the other tile's S and PV products (the overlap
+// the CMU post motivates on slide pages 20-22 and 51-52).
+//
+// Tensor memory (512 columns x 128 lanes of 32 bit):
+//   [0,128)  S for tile 0, overwritten in place by P (bf16 pairs, 64 cols)
+//   [128,256) S / P for tile 1
+//   [256,256+d) O accumulator of tile 0, [256+d, 256+2d) O of tile 1
+//
+// Online softmax per row (cs2680 Lecture 9 sec. 9.4, CMU post slide page 12):
+// scores are used in log2 units t = scale*log2(e)*s.  The reference maximum
+// m only moves when a tile's maximum exceeds it by more than kRescaleSlack,
+// in which case the running denominator l and the O accumulator are
+// multiplied by 2^(m_old - m_new); otherwise the stale m is kept and the
+// exponentials stay below 2^kRescaleSlack.  O and l always share the same
+// reference, so O / l and lse = (m + log2 l) * ln 2 are exact.
+#include "fa_internal.h"
+#include "sm100_ptx.cuh"
+
+namespace fa {
+namespace {
+
+constexpr float kRescaleSlack = 8.0f;  // log2 units
+constexpr float kLn2 = 0.69314718055994530942f;
+
+template <int D>
+struct FwdCfg {
+  static constexpr int kTileBytes = kTile * D * 2;        // one 128 x d bf16 tile
+  static constexpr int kStages = (D == 128) ? 5 : 8;     // K/V ring slots
+  static constexpr int kThreads = 320;
+  static constexpr uint32_t kTmemCols = 512;
+  // TMEM column of S/P and of O for Q tile t.
+  static __device__ __forceinline__ uint32_t col_s(int t) { return (uint32_t)t * 128u; }
+  static __device__ __forceinline__ uint32_t col_o(int t) { return 256u + (uint32_t)t * D; }
+  static constexpr int kKSteps = D / 16;                 // MMA K-steps of S = Q K^T
+};
+
+template <int D>
+struct alignas(1024) FwdSmem {
+  uint8_t q[2][FwdCfg<D>::kTileBytes];
+  uint8_t kv[FwdCfg<D>::kStages][FwdCfg<D>::kTileBytes];
+  uint64_t q_full;
+  uint64_t kv_full[FwdCfg<D>::kStages];
+  uint64_t kv_empty[FwdCfg<D>::kStages];
+  uint64_t s_full[2];
+  uint64_t p_full[2];
+  uint64_t o_full[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+// Wait sites reported through the status word.
+enum : int {
+  kSiteQFull = 101, kSiteKvEmpty, kSiteKvFull, kSitePFull, kSiteSFull, kSiteOFull, kSiteDrain
+};
+
+// Descriptor of the K-major, 128B-swizzled tile at `base` for MMA K-step kk:
+// 64-column blocks are 16 KB apart; a 16-element step is 32 bytes.
+__device__ __forceinline__ uint64_t kmajor_desc(uint32_t base, int kk) {
+  return sdesc_sw128(base + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
+}
+
+// Descriptor of a row-major [keys][d] tile used as the MN-major B operand of
+// O += P V for K-step kk (16 keys = two 8-row groups = 2048 bytes).
+__device__ __forceinline__ uint64_t mnmajor_desc(uint32_t base, int kk) {
+  return sdesc_sw128(base + kk * 2048, 16384, 1024);
+}
+
+// Wait without the abort shortcut: used while winding down after an abort.
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
+  const uint32_t a = smem_u32(bar);
+  const unsigned long long t0 = globaltimer_ns();
+  while (!mbar_try_wait(a, parity)) {
+    if (globaltimer_ns() - t0 > 100000000ull) return;  // 100 ms
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
+    fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                  const __grid_constant__ CUtensorMap tv, const FwdParams p) {
+  using Cfg = FwdCfg<D>;
+  constexpr int S = Cfg::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  FwdSmem<D>& sm = *reinterpret_cast<FwdSmem<D>*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  volatile int* abortf = &sm.abort_flag;
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+
+  if (tid == 0) {
+    mbar_init(&sm.q_full, 1);
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&sm.kv_full[s], 1);
+      mbar_init(&sm.kv_empty[s], 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&sm.s_full[t], 1);
+      mbar_init(&sm.p_full[t], 128);
+      mbar_init(&sm.o_full[t], 1);
+    }
+    mbar_init(&sm.drain, 1);
+    sm.abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(&sm.tmem_base, Cfg::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem_base;
+
+  int bh, pair;
+  fwd_item(blockIdx.x, p.BH, p.n_pairs, &bh, &pair);
+  const int row0 = pair * kPairRows;
+  const int n_t0 = fwd_kv_tiles(2 * pair, p.n_kv, p.causal);
+  const int n_t1 = fwd_kv_tiles(2 * pair + 1, p.n_kv, p.causal);  // n_t0 <= n_t1 <= n_t0 + 1
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ producer
+    if (lane_id() == 0) {
+      prefetch_tmap(&tq);
+      prefetch_tmap(&tk);
+      prefetch_tmap(&tv);
+      mbar_arrive_expect_tx(&sm.q_full, 2 * Cfg::kTileBytes);
+      for (int t = 0; t < 2; ++t)
+        for (int h = 0; h < D / 64; ++h)
+          tma_load_3d(sm.q[t] + h * 16384, &tq, &sm.q_full, h * 64, row0 + t * kTile, bh);
+      int c = 0;
+      bool ok = true;
+      for (int j = 0; j < n_t1 && ok; ++j) {
+        for (int w = 0; w < 2 && ok; ++w, ++c) {
+          const int slot = c % S, use = c / S;
+          if (use > 0 &&
+              !mbar_wait(&sm.kv_empty[slot], (use - 1) & 1, p.status, abortf, kSiteKvEmpty)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&sm.kv_full[slot], Cfg::kTileBytes);
+          for (int h = 0; h < D / 64; ++h)
+            tma_load_3d(sm.kv[slot] + h * 16384, w == 0 ? &tk : &tv, &sm.kv_full[slot], h * 64,
+                        j * kTile, bh);
+        }
+      }
+      if (!ok) {
+        // Let the copies already issued land before the CTA exits.
+        drain_wait(&sm.q_full, 0);
+        for (int cc = c - 1; cc >= 0 && cc >= c - S; --cc) drain_wait(&sm.kv_full[cc % S], (cc / S) & 1);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 9) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane_id() == 0) {
+      const uint32_t id_s = idesc_bf16(128, 128, false, false);
+      const uint32_t id_pv = idesc_bf16(128, D, false, true);
+      const uint32_t q_addr[2] = {smem_u32(sm.q[0]), smem_u32(sm.q[1])};
+      uint32_t p_par[2] = {0, 0};
+      bool ok = mbar_wait(&sm.q_full, 0, p.status, abortf, kSiteQFull);
+
+      auto issue_s = [&](int t, int kslot) {
+        const uint32_t kb = smem_u32(sm.kv[kslot]);
+#pragma unroll
+        for (int kk = 0; kk < Cfg::kKSteps; ++kk)
+          mma_ss(tmem + Cfg::col_s(t), kmajor_desc(q_addr[t], kk), kmajor_desc(kb, kk), id_s,
+                 kk > 0);
+        tc_commit(&sm.s_full[t]);
+      };
+      auto issue_pv = [&](int t, int vslot, bool accumulate) {
+        const uint32_t vb = smem_u32(sm.kv[vslot]);
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk)
+          mma_ts(tmem + Cfg::col_o(t), tmem + Cfg::col_s(t) + kk * 8, mnmajor_desc(vb, kk), id_pv,
+                 (accumulate || kk > 0) ? 1u : 0u);
+      };
+      auto wait_full = [&](int cnt) -> bool {
+        return mbar_wait(&sm.kv_full[cnt % S], (cnt / S) & 1, p.status, abortf, kSiteKvFull);
+      };
+      auto wait_p = [&](int t) -> bool {
+        const bool r = mbar_wait(&sm.p_full[t], p_par[t], p.status, abortf, kSitePFull);
+        p_par[t] ^= 1;
+        return r;
+      };
+
+      if (ok) ok = wait_full(0);
+      if (ok) {
+        tc_fence_after();
+        issue_s(0, 0);
+        issue_s(1, 0);
+        tc_commit(&sm.kv_empty[0]);
+      }
+      for (int j = 1; j < n_t1 && ok; ++j) {
+        const int kc = 2 * j, vc = 2 * j - 1;
+        ok = wait_full(kc) && wait_full(vc);
+        if (!ok) break;
+        ok = wait_p(0);
+        if (!ok) break;
+        tc_fence_after();
+        issue_pv(0, vc % S, j - 1 > 0);
+        if (j < n_t0) {
+          issue_s(0, kc % S);
+        } else {
+          tc_commit(&sm.o_full[0]);  // tile 0 has no more keys (causal)
+        }
+        ok = wait_p(1);
+        if (!ok) break;
+        tc_fence_after();
+        issue_pv(1, vc % S, j - 1 > 0);
+        tc_commit(&sm.kv_empty[vc % S]);
+        issue_s(1, kc % S);
+        tc_commit(&sm.kv_empty[kc % S]);
+      }
+      if (ok) {
+        const int vc = 2 * n_t1 - 1;
+        ok = wait_full(vc);
+        if (ok && n_t0 == n_t1) {
+          ok = wait_p(0);
+          if (ok) {
+            tc_fence_after();
+            issue_pv(0, vc % S, n_t1 - 1 > 0);
+            tc_commit(&sm.o_full[0]);
+          }
+        }
+        if (ok) ok = wait_p(1);
+        if (ok) {
+          tc_fence_after();
+          issue_pv(1, vc % S, n_t1 - 1 > 0);
+          tc_commit(&sm.o_full[1]);
+          tc_commit(&sm.kv_empty[vc % S]);
+        }
+      }
+      // Every MMA issued so far must finish before TMEM is released.
+      tc_commit(&sm.drain);
+      drain_wait(&sm.drain, 0);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int t = warp >> 2;             // which Q tile
+    const int r = tid & 127;             // row within the tile
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    const int n_t = t == 0 ? n_t0 : n_t1;
+    const int R = row0 + t * kTile + r;  // global query row
+    const float c2 = p.scale_log2;
+    const bool neg = c2 < 0.f;
+    const float neutral = neg ? __int_as_float(0x7f800000) : __int_as_float(0xff800000);
+    const uint32_t colS = tmem + lane_base + Cfg::col_s(t);
+    const uint32_t colO = tmem + lane_base + Cfg::col_o(t);
+    const int diag_tile = p.causal ? (row0 + t * kTile) / kTile : -1;
+
+    float m_ref = __int_as_float(0xff800000);  // -inf
+    float l = 0.f;
+    uint32_t s_par = 0;
+    bool ok = true;
+    for (int j = 0; j < n_t; ++j) {
+      ok = mbar_wait(&sm.s_full[t], s_par, p.status, abortf, kSiteSFull);
+      ok = __all_sync(0xffffffffu, ok);  // keep the warp's collective TMEM ops converged
+      s_par ^= 1;
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t sr[4][32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld32(colS + c * 32, sr[c]);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_wait_ld(sr[c]);
+
+      const bool need_mask = (j + 1) * kTile > p.N || j == diag_tile;
+      if (need_mask) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const int col = j * kTile + c * 32 + i;
+            if (col >= p.N || (p.causal && col > R)) sr[c][i] = __float_as_uint(neutral);
+          }
+      }
+      // Tile extreme of the raw scores (max for scale >= 0, min otherwise).
+      float mx = __uint_as_float(sr[0][0]);
+      if (!neg) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int i = 0; i < 32; ++i) mx = fmaxf(mx, __uint_as_float(sr[c][i]));
+      } else {
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int i = 0; i < 32; ++i) mx = fminf(mx, __uint_as_float(sr[c][i]));
+      }
+      const float m_tile = mx * c2;
+      float alpha = 1.f;
+      if (m_tile > m_ref + kRescaleSlack) {
+        alpha = ex2_approx(m_ref - m_tile);  // 0 on the first tile (m_ref = -inf)
+        m_ref = m_tile;
+      }
+      l *= alpha;
+      const float neg_m = -m_ref;
+      float lsum = 0.f;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int c2i = 0; c2i < 2; ++c2i) {
+          const int c = 2 * h + c2i;
+#pragma unroll
+          for (int i = 0; i < 32; i += 2) {
+            float p0 = ex2_approx(fmaf(__uint_as_float(sr[c][i]), c2, neg_m));
+            float p1 = ex2_approx(fmaf(__uint_as_float(sr[c][i + 1]), c2, neg_m));
+            if (need_mask) {
+              const int col = j * kTile + c * 32 + i;
+              if (col >= p.N || (p.causal && col > R)) p0 = 0.f;
+              if (col + 1 >= p.N || (p.causal && col + 1 > R)) p1 = 0.f;
+            }
+            lsum += p0 + p1;
+            pk[c2i * 16 + i / 2] = pack_bf16x2(p0, p1);
+          }
+        }
+        tmem_st32(colS + h * 32, pk);
+      }
+      l += lsum;
+      tmem_wait_st();
+      // Correct the O accumulator if this row's reference moved (warp-wide
+      // decision: TMEM loads/stores are warp-collective).
+      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t orow[32];
+          tmem_ld32(colO + c * 32, orow);
+          tmem_wait_ld(orow);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) orow[i] = __float_as_uint(__uint_as_float(orow[i]) * alpha);
+          tmem_st32(colO + c * 32, orow);
+        }
+        tmem_wait_st();
+      }
+      tc_fence_before();
+      mbar_arrive(&sm.p_full[t]);
+    }
+    if (ok) ok = mbar_wait(&sm.o_full[t], 0, p.status, abortf, kSiteOFull);
+    ok = __all_sync(0xffffffffu, ok);
+    if (ok) {
+      tc_fence_after();
+      const float inv_l = 1.f / l;
+      __nv_bfloat16* orow_g = reinterpret_cast<__nv_bfloat16*>(p.o) + ((size_t)bh * p.N + R) * D;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t orow[32];
+        tmem_ld32(colO + c * 32, orow);
+        tmem_wait_ld(orow);
+        if (R < p.N) {
+          uint4 v[4];
+          uint32_t* w = reinterpret_cast<uint32_t*>(v);
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            w[i] = pack_bf16x2(__uint_as_float(orow[2 * i]) * inv_l,
+                               __uint_as_float(orow[2 * i + 1]) * inv_l);
+          uint4* dst = reinterpret_cast<uint4*>(orow_g + c * 32);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) dst[i] = v[i];
+        }
+      }
+      if (R < p.N) p.lse[(size_t)bh * p.N + R] = (m_ref + __log2f(l)) * kLn2;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after();
+    tmem_dealloc(tmem, Cfg::kTmemCols);
+  }
+}
+
+template <int D>
+int launch_fwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                 const FwdParams& p, cudaStream_t stream) {
+  const size_t smem = sizeof(FwdSmem<D>) + 1024;
+  if (cudaFuncSetAttribute(fa_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)smem) != cudaSuccess)
+    return FA_ERR_LAUNCH;
+  const unsigned grid = (unsigned)p.BH * (unsigned)p.n_pairs;
+  fa_fwd_kernel<D><<<grid, FwdCfg<D>::kThreads, smem, stream>>>(tq, tk, tv, p);
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+}
+
+}  // namespace
+
+int launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+               const FwdParams& p, int d, cudaStream_t stream) {
+  if (d == 128) return launch_fwd_d<128>(tq, tk, tv, p, stream);
+  if (d == 64) return launch_fwd_d<64>(tq, tk, tv, p, stream);
+  return FA_ERR_UNSUPPORTED_D;
+}
+
+}  // namespace fa

@@ -1,0 +1,79 @@
+// fa_internal.h -- declarations shared by the C-ABI front end (fa_api.cu)
+// and the kernels (fa_fwd.cu, fa_bwd.cu).  Not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/fa.h"
+
+namespace fa {
+
+constexpr int kTile = 128;        // rows of a Q tile and of a K/V tile
+constexpr int kPairRows = 2 * kTile;  // query rows of one forward work item
+constexpr int kHeadGroup = 8;     // heads whose work items are kept together
+
+__host__ __device__ inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+// Number of 128-key tiles query tile `qt` (rows 128*qt .. 128*qt+127) visits.
+__host__ __device__ inline int fwd_kv_tiles(int qt, int n_kv, int causal) {
+  if (!causal) return n_kv;
+  const int last = qt + 1;  // keys j <= row: tiles 0 .. qt
+  return last < n_kv ? last : n_kv;
+}
+
+// The forward kernel's work order.  Items are (head, pair of query tiles).
+// Heads are taken in groups of kHeadGroup so that the CTAs running at the
+// same time share few heads' K/V in L2; inside a group the pairs go from
+// the last (most keys under a causal mask) to the first, so under a causal
+// mask the longest items start first and the short ones fill the tail.
+__host__ __device__ inline void fwd_item(int t, int BH, int n_pairs, int* bh, int* pair) {
+  const int per_group = kHeadGroup * n_pairs;
+  const int g = t / per_group;
+  const int gsize = (BH - g * kHeadGroup) < kHeadGroup ? (BH - g * kHeadGroup) : kHeadGroup;
+  const int idx = t - g * per_group;
+  *pair = n_pairs - 1 - idx / gsize;
+  *bh = g * kHeadGroup + idx % gsize;
+}
+
+struct FwdParams {
+  void* o;          // [BH][N][d] bf16
+  float* lse;       // [BH][N] fp32
+  int* status;      // device status word (2 ints: code, site)
+  int BH, N;
+  int n_kv;         // ceil(N / 128)
+  int n_pairs;      // ceil(N / 256)
+  int causal;
+  float scale_log2;  // scale * log2(e)
+};
+
+struct BwdParams {
+  const void* o;     // [BH][N][d] bf16 (forward output)
+  const void* dout;  // [BH][N][d] bf16
+  const float* lse;  // [BH][N] fp32
+  void* dq;          // [BH][N][d] bf16
+  void* dk;
+  void* dv;
+  float* dq_acc;     // workspace: [BH][n_kv*128][d] fp32, tile-blocked
+  float* delta;      // workspace: [BH][n_kv*128] fp32 (D_i)
+  int* status;
+  int BH, N;
+  int n_kv;
+  int causal;
+  float scale;
+  float scale_log2;
+};
+
+// Build a rank-3 tensor map over a [BH][N][d] bf16 array: dims (d, N, BH),
+// box (64, 128, 1), 128-byte swizzle, zero fill outside.  Returns 0 or an
+// FA_ERR_* code.
+int make_tmap_bhnd(const void* base, int BH, int N, int d, CUtensorMap* out);
+
+int launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+               const FwdParams& p, int d, cudaStream_t stream);
+
+int launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+               const CUtensorMap& tdo, const BwdParams& p, int d, cudaStream_t stream);
+
+}  // namespace fa

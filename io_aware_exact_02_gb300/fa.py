@@ -1,0 +1,177 @@
+"""ctypes binding of libfa.so (argument marshalling only).
+
+Every function here passes raw device pointers, sizes and the current CUDA
+stream to the C ABI declared in include/fa.h; all the arithmetic runs in the
+library's CUDA kernels.  There is no fallback: if libfa.so is missing or
+cannot be loaded, or a call returns an error code, a ``FaError`` is raised.
+
+Tensors are torch tensors used as device buffers: q, k, v, o, dout, dq, dk,
+dv are contiguous bf16 (B, H, N, d) on a CUDA device, lse is contiguous fp32
+(B, H, N).
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libfa.so")
+
+FA_OK = 0
+FA_ERR_ARG = -1
+FA_ERR_UNSUPPORTED_D = -2
+FA_ERR_ALIGN = -3
+FA_ERR_WORKSPACE = -4
+FA_ERR_DEVICE = -5
+FA_ERR_LAUNCH = -6
+FA_ERR_TIMEOUT = -7
+
+# Every symbol include/fa.h declares, with (restype, argtypes).
+_vp, _i, _f, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+_ip = ctypes.POINTER(ctypes.c_int)
+SIGNATURES = {
+    "fa_fwd": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp]),
+    "fa_bwd_workspace_size": (_sz, [_i, _i, _i, _i]),
+    "fa_bwd": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f,
+                    _vp, _sz, _vp]),
+    "fa_device_status": (_i, [_vp, _ip]),
+    "fa_status_string": (ctypes.c_char_p, [_i]),
+    "fa_fwd_schedule": (_i, [_i, _i, _i, _i, _ip, _ip, _ip, _i]),
+    "fa_version": (_i, []),
+}
+
+
+class FaError(RuntimeError):
+    def __init__(self, fn: str, code: int, msg: str):
+        super().__init__("%s failed: %s (%d)" % (fn, msg, code))
+        self.code = code
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load(path: str | None = None):
+    """Load libfa.so (once) and declare its signatures.  Raises if missing."""
+    global _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            raise FaError("load", FA_ERR_DEVICE,
+                          "%s is missing; build it with python -m io_aware_exact_02_gb300.build" % p)
+        lib = ctypes.CDLL(p)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        if path is None:
+            _lib = lib
+        return lib
+
+
+def status_string(code: int) -> str:
+    return load().fa_status_string(int(code)).decode()
+
+
+def _check(fn: str, code: int):
+    if code != FA_OK:
+        raise FaError(fn, code, status_string(code))
+
+
+def _stream_of(t: torch.Tensor):
+    return ctypes.c_void_p(torch.cuda.current_stream(t.device).cuda_stream)
+
+
+def _check_qkv(name, t, shape, dtype=torch.bfloat16):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if t.dtype != dtype:
+        raise ValueError("%s must be %s" % (name, dtype))
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError("%s has shape %s, expected %s" % (name, tuple(t.shape), tuple(shape)))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+
+
+def default_scale(d: int) -> float:
+    return 1.0 / math.sqrt(d)
+
+
+def fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None):
+    """O, lse = attention(q, k, v).  Returns (o, lse) (allocated if not given)."""
+    B, H, N, d = q.shape
+    scale = default_scale(d) if scale is None else float(scale)
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _check_qkv(name, t, (B, H, N, d))
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    _check_qkv("out", out, (B, H, N, d))
+    _check_qkv("lse", lse, (B, H, N), torch.float32)
+    rc = load().fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                       B, H, N, d, int(bool(causal)), ctypes.c_float(scale), _stream_of(q))
+    _check("fa_fwd", rc)
+    return out, lse
+
+
+def bwd_workspace_size(B: int, H: int, N: int, d: int) -> int:
+    return int(load().fa_bwd_workspace_size(B, H, N, d))
+
+
+def bwd(q, k, v, o, dout, lse, causal: bool = False, scale: float | None = None,
+        dq=None, dk=None, dv=None, workspace=None):
+    """dq, dk, dv of L = sum(dout * O).  Returns (dq, dk, dv)."""
+    B, H, N, d = q.shape
+    scale = default_scale(d) if scale is None else float(scale)
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("dout", dout)):
+        _check_qkv(name, t, (B, H, N, d))
+    _check_qkv("lse", lse, (B, H, N), torch.float32)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(q) if dk is None else dk
+    dv = torch.empty_like(q) if dv is None else dv
+    for name, t in (("dq", dq), ("dk", dk), ("dv", dv)):
+        _check_qkv(name, t, (B, H, N, d))
+    need = bwd_workspace_size(B, H, N, d)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    nbytes = workspace.numel() * workspace.element_size()
+    rc = load().fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(),
+                       lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, N, d,
+                       int(bool(causal)), ctypes.c_float(scale), workspace.data_ptr(), nbytes,
+                       _stream_of(q))
+    _check("fa_bwd", rc)
+    return dq, dk, dv
+
+
+def device_status(stream=None):
+    """Synchronise the stream; return (code, site) and clear the status word."""
+    s = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream if stream is None else stream)
+    site = ctypes.c_int(0)
+    code = load().fa_device_status(s, ctypes.byref(site))
+    return int(code), int(site.value)
+
+
+def check_device_status(stream=None):
+    code, site = device_status(stream)
+    if code != FA_OK:
+        raise FaError("kernel", code, status_string(code) + " (site %d)" % site)
+
+
+def fwd_schedule(B: int, H: int, N: int, causal: bool):
+    """The forward kernel's work order: list of (bh, pair, cost)."""
+    lib = load()
+    n = lib.fa_fwd_schedule(B, H, N, int(bool(causal)), None, None, None, 0)
+    if n < 0:
+        _check("fa_fwd_schedule", n)
+    bh = (ctypes.c_int * n)()
+    pr = (ctypes.c_int * n)()
+    cost = (ctypes.c_int * n)()
+    lib.fa_fwd_schedule(B, H, N, int(bool(causal)), bh, pr, cost, n)
+    return list(zip(bh, pr, cost))

@@ -1,0 +1,151 @@
+"""The C-ABI library without a GPU: it loads, exports every symbol
+include/fa.h declares, rejects bad arguments with its error codes before
+touching a device, and its host-side scheduler follows the LPT rule."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from io_aware_exact_02_gb300 import build, fa
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fa.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return fa.load()
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fa_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_bound_symbols():
+    assert declared_symbols() == sorted(fa.SIGNATURES)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+    assert lib.fa_version() == 1
+
+
+def test_status_strings(lib):
+    for code in (fa.FA_OK, fa.FA_ERR_ARG, fa.FA_ERR_UNSUPPORTED_D, fa.FA_ERR_ALIGN,
+                 fa.FA_ERR_WORKSPACE, fa.FA_ERR_DEVICE, fa.FA_ERR_LAUNCH, fa.FA_ERR_TIMEOUT):
+        s = lib.fa_status_string(code)
+        assert s and s != b"unknown status"
+    assert lib.fa_status_string(12345) == b"unknown status"
+
+
+FAKE = 1 << 20  # a 16-byte aligned non-null address; never dereferenced
+
+
+def call_fwd(lib, q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=FAKE, B=1, H=1, N=128, d=64, causal=0,
+             scale=0.125):
+    return lib.fa_fwd(q, k, v, o, lse, B, H, N, d, causal, ctypes.c_float(scale), None)
+
+
+def test_fwd_argument_errors_launch_nothing(lib):
+    assert call_fwd(lib, q=None) == fa.FA_ERR_ARG
+    assert call_fwd(lib, lse=None) == fa.FA_ERR_ARG
+    assert call_fwd(lib, B=0) == fa.FA_ERR_ARG
+    assert call_fwd(lib, H=-1) == fa.FA_ERR_ARG
+    assert call_fwd(lib, N=0) == fa.FA_ERR_ARG
+    assert call_fwd(lib, causal=2) == fa.FA_ERR_ARG
+    assert call_fwd(lib, scale=float("nan")) == fa.FA_ERR_ARG
+    assert call_fwd(lib, scale=float("inf")) == fa.FA_ERR_ARG
+    assert call_fwd(lib, d=96) == fa.FA_ERR_UNSUPPORTED_D
+    assert call_fwd(lib, d=256) == fa.FA_ERR_UNSUPPORTED_D
+    assert call_fwd(lib, k=FAKE + 8) == fa.FA_ERR_ALIGN
+    assert call_fwd(lib, lse=FAKE + 4) == fa.FA_ERR_ALIGN
+    assert call_fwd(lib, B=1 << 16, H=1 << 16) == fa.FA_ERR_ARG
+
+
+def test_bwd_argument_errors_launch_nothing(lib):
+    ws = lib.fa_bwd_workspace_size(1, 1, 128, 64)
+
+    def call(**kw):
+        a = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, do=FAKE, lse=FAKE, dq=FAKE, dk=FAKE, dv=FAKE,
+                 B=1, H=1, N=128, d=64, causal=0, scale=0.125, ws=FAKE, wsb=ws)
+        a.update(kw)
+        return lib.fa_bwd(a["q"], a["k"], a["v"], a["o"], a["do"], a["lse"], a["dq"], a["dk"],
+                          a["dv"], a["B"], a["H"], a["N"], a["d"], a["causal"],
+                          ctypes.c_float(a["scale"]), a["ws"], a["wsb"], None)
+
+    assert call(dv=None) == fa.FA_ERR_ARG
+    assert call(N=0) == fa.FA_ERR_ARG
+    assert call(d=80) == fa.FA_ERR_UNSUPPORTED_D
+    assert call(do=FAKE + 2) == fa.FA_ERR_ALIGN
+    assert call(ws=None) == fa.FA_ERR_WORKSPACE
+    assert call(wsb=ws - 1) == fa.FA_ERR_WORKSPACE
+    assert call(ws=FAKE + 16) == fa.FA_ERR_WORKSPACE
+
+
+def test_workspace_size(lib):
+    # fp32 dQ accumulator over 128-row-padded rows plus one fp32 per row.
+    assert lib.fa_bwd_workspace_size(2, 3, 300, 64) == 2 * 3 * 384 * 64 * 4 + 2 * 3 * 384 * 4
+    assert lib.fa_bwd_workspace_size(1, 1, 128, 128) == 128 * 128 * 4 + 128 * 4
+    assert lib.fa_bwd_workspace_size(1, 1, 0, 64) == 0
+    assert lib.fa_bwd_workspace_size(1, 1, 128, 72) == 0
+
+
+# ------------------------------------------------------------- scheduling
+
+def greedy(costs, workers):
+    """List scheduling: each item goes to the least-loaded worker, in order."""
+    loads = [0] * workers
+    for c in costs:
+        w = loads.index(min(loads))
+        loads[w] += c
+    return loads
+
+
+def golden_lpt():
+    path = os.path.join(ROOT, "tests", "golden", "pages_numbers.txt")
+    vals = {}
+    for line in open(path):
+        line = line.split("#", 1)[0].strip()
+        if line:
+            key, val = line.split(None, 1)
+            vals[key] = [int(x) for x in val.split(",")] if "," in val else val
+    return vals["lpt_in_order"], vals["lpt_longest_first"]
+
+
+def test_lpt_example_of_the_pages():
+    # Two batches of four causal query tiles costing 1, 2, 3, 4 key tiles,
+    # three SMs: in order the SMs end with [9, 5, 6]; longest first gives
+    # [7, 7, 6] (CMU 11-868 post, LPT paragraph).
+    in_order, lpt = golden_lpt()
+    costs = [1, 2, 3, 4, 1, 2, 3, 4]
+    assert greedy(costs, 3) == in_order
+    assert greedy(sorted(costs, reverse=True), 3) == lpt
+
+
+@pytest.mark.parametrize("B,H,N,causal", [(1, 2, 1024, 1), (2, 5, 3000, 1), (3, 4, 700, 0),
+                                          (1, 17, 4096, 1), (1, 1, 1, 0)])
+def test_schedule_covers_every_item_once_longest_first(lib, B, H, N, causal):
+    items = fa.fwd_schedule(B, H, N, causal)
+    n_pairs = -(-N // 256)
+    assert sorted((bh, p) for bh, p, _ in items) == [(bh, p) for bh in range(B * H)
+                                                    for p in range(n_pairs)]
+    n_kv = -(-N // 128)
+    for bh, p, c in items:
+        expect = (min(2 * p + 1, n_kv) + min(2 * p + 2, n_kv)) if causal else 2 * n_kv
+        assert c == expect
+    # Within each group of heads the costs never increase (LPT order), and the
+    # order equals a stable longest-first sort of the group's items.
+    group = 8 * n_pairs
+    for g0 in range(0, len(items), group):
+        chunk = items[g0:g0 + group]
+        costs = [c for _, _, c in chunk]
+        assert costs == sorted(costs, reverse=True)
+    if causal and B * H >= 1:
+        loads_lpt = greedy([c for _, _, c in items], 3)
+        loads_fwd = greedy(sorted([c for _, _, c in items]), 3)
+        assert max(loads_lpt) <= max(loads_fwd)

@@ -1,0 +1,163 @@
+"""Forward pass on the GPU (through the C ABI) against the fp64 oracle.
+
+Tolerances (bf16 inputs, fp32 accumulation, bf16 output):
+  O:   max |dO| <= 2e-2 and mean |dO| <= 2e-3 over every element,
+  lse: max |dlse| <= 1e-3 absolute.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from io_aware_exact_02_gb300 import build, fa, synth
+
+pytestmark = pytest.mark.gpu
+
+O_MAX, O_MEAN, LSE_MAX = 2e-2, 2e-3, 1e-3
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    build.build()
+    return fa.load()
+
+
+def run_fwd(q, k, v, causal, scale):
+    dev = torch.device("cuda")
+    o, lse = fa.fwd(q.to(dev), k.to(dev), v.to(dev), causal=causal, scale=scale)
+    fa.check_device_status()
+    return o.float().cpu().numpy(), lse.cpu().numpy()
+
+
+def compare(o, lse, o_ref, lse_ref, what=""):
+    do = np.abs(o.astype(np.float64) - o_ref)
+    dl = np.abs(lse.astype(np.float64) - lse_ref)
+    assert np.isfinite(o).all() and np.isfinite(lse).all(), what
+    assert do.max() <= O_MAX, (what, do.max())
+    assert do.mean() <= O_MEAN, (what, do.mean())
+    assert dl.max() <= LSE_MAX, (what, dl.max())
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("N", [1, 17, 127, 128, 129, 255, 256, 257, 300, 1000])
+def test_fwd_matches_oracle_small(N, causal, d):
+    B, H = 2, 3
+    q, k, v, _ = synth.draw(B, H, N, d, seed=N + 7 * d + causal, with_dout=False)
+    scale = 1.0 / math.sqrt(d)
+    o, lse = run_fwd(q, k, v, causal, scale)
+    o_ref, lse_ref = oracle.attn_fwd(q, k, v, causal, scale)
+    compare(o, lse, o_ref, lse_ref, "N=%d causal=%d d=%d" % (N, causal, d))
+
+
+def test_tiny_workload():
+    w = synth.TINY
+    q, k, v, _ = synth.draw_workload(w, with_dout=False)
+    o, lse = run_fwd(q, k, v, w.causal, w.softmax_scale)
+    o_ref, lse_ref = oracle.attn_fwd(q, k, v, w.causal, w.softmax_scale)
+    compare(o, lse, o_ref, lse_ref, "tiny")
+
+
+@pytest.mark.parametrize("scale", [0.0, -0.2, 0.9, 2.0])
+@pytest.mark.parametrize("causal", [False, True])
+def test_fwd_scales(scale, causal):
+    q, k, v, _ = synth.draw(1, 2, 333, 64, seed=11, with_dout=False)
+    o, lse = run_fwd(q, k, v, causal, scale)
+    o_ref, lse_ref = oracle.attn_fwd(q, k, v, causal, scale)
+    compare(o, lse, o_ref, lse_ref, "scale=%g" % scale)
+
+
+def test_fwd_heavy_rows_force_rescaling():
+    # 1% of K rows x8 (the long-context recipe) at a size the oracle runs in
+    # full: the running maximum of many rows grows after the first tile.
+    q, k, v, _ = synth.draw(1, 4, 2048, 128, seed=3, heavy_frac=0.01, with_dout=False)
+    for causal in (False, True):
+        o, lse = run_fwd(q, k, v, causal, 1 / math.sqrt(128))
+        o_ref, lse_ref = oracle.attn_fwd(q, k, v, causal, 1 / math.sqrt(128))
+        compare(o, lse, o_ref, lse_ref, "heavy causal=%d" % causal)
+
+
+def test_fwd_deterministic_bitwise():
+    q, k, v, _ = synth.draw(2, 2, 1111, 128, seed=5, with_dout=False)
+    dev = torch.device("cuda")
+    q, k, v = q.to(dev), k.to(dev), v.to(dev)
+    o1, l1 = fa.fwd(q, k, v, causal=True)
+    o2, l2 = fa.fwd(q, k, v, causal=True)
+    fa.check_device_status()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_fwd_invariants_on_gpu():
+    # No oracle: scale 0 gives the (prefix) mean of V and lse = ln(count);
+    # a joint permutation of K and V rows leaves non-causal O unchanged.
+    B, H, N, d = 1, 2, 700, 64
+    q, k, v, _ = synth.draw(B, H, N, d, seed=9, with_dout=False)
+    o, lse = run_fwd(q, k, v, False, 0.0)
+    vm = v.double().mean(2, keepdim=True).numpy()
+    assert np.abs(o - vm).max() < 1e-2
+    assert np.abs(lse - math.log(N)).max() < 1e-4
+    o, lse = run_fwd(q, k, v, True, 0.0)
+    pref = (v.double().cumsum(2) / torch.arange(1, N + 1).double()[None, None, :, None]).numpy()
+    assert np.abs(o - pref).max() < 2e-2
+    assert np.abs(lse - np.log(np.arange(1, N + 1))[None, None]).max() < 1e-4
+    o1, l1 = run_fwd(q, k, v, False, 0.125)
+    perm = torch.randperm(N, generator=torch.Generator().manual_seed(1))
+    o2, l2 = run_fwd(q, k[:, :, perm].contiguous(), v[:, :, perm].contiguous(), False, 0.125)
+    assert np.abs(o1 - o2).max() < 1e-2
+    assert np.abs(l1 - l2).max() < 1e-4
+
+
+def test_fwd_causal_row_zero_is_v0():
+    q, k, v, _ = synth.draw(1, 3, 513, 128, seed=21, with_dout=False)
+    o, lse = run_fwd(q, k, v, True, 0.3)
+    assert np.abs(o[:, :, 0] - v[:, :, 0].float().numpy()).max() < 1e-6
+    ref = 0.3 * (q[:, :, 0].double() * k[:, :, 0].double()).sum(-1).numpy()
+    assert np.abs(lse[:, :, 0] - ref).max() < 1e-4
+
+
+def test_fwd_bad_arguments_raise():
+    q, k, v, _ = synth.draw(1, 1, 64, 64, seed=1, with_dout=False)
+    dev = torch.device("cuda")
+    q, k, v = q.to(dev), k.to(dev), v.to(dev)
+    with pytest.raises(fa.FaError) as e:
+        fa.fwd(q, k, v, scale=float("nan"))
+    assert e.value.code == fa.FA_ERR_ARG
+    big = torch.empty(1, 1, 64, 96, dtype=torch.bfloat16, device=dev)
+    with pytest.raises(fa.FaError) as e:
+        fa.fwd(big, big, big)
+    assert e.value.code == fa.FA_ERR_UNSUPPORTED_D
+
+
+# ------------------------------------------- full-size workloads, sampled rows
+
+FULL = [w.name for w in synth.ALL if w.name != "tiny"]
+
+
+def sampled_check(w, o_dev, lse_dev, q, k, v, n_heads=3, n_rows=48, seed=0):
+    rng = np.random.default_rng(seed)
+    BH = w.B * w.H
+    heads = sorted(set(rng.choice(BH, size=min(n_heads, BH), replace=False).tolist()) | {BH - 1})
+    rows = np.unique(np.concatenate([rng.choice(w.N, size=n_rows, replace=False),
+                                     [0, w.N - 1, min(w.N - 1, 128), min(w.N - 1, 255)]]))
+    qf = q.reshape(BH, w.N, w.d)[heads].unsqueeze(0)
+    kf = k.reshape(BH, w.N, w.d)[heads].unsqueeze(0)
+    vf = v.reshape(BH, w.N, w.d)[heads].unsqueeze(0)
+    hh = np.repeat(np.arange(len(heads)), rows.size)
+    rr = np.tile(rows, len(heads))
+    o_ref, lse_ref = oracle.attn_fwd_rows(qf, kf, vf, w.causal, w.softmax_scale, hh, rr)
+    o = o_dev.reshape(BH, w.N, w.d)[heads][:, rows].float().cpu().numpy().reshape(-1, w.d)
+    lse = lse_dev.reshape(BH, w.N)[heads][:, rows].cpu().numpy().reshape(-1)
+    compare(o, lse, o_ref, lse_ref, w.name)
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_fwd_full_size_sampled(name):
+    w = synth.by_name(name)
+    q, k, v, _ = synth.draw_workload(w, with_dout=False)
+    dev = torch.device("cuda")
+    o, lse = fa.fwd(q.to(dev), k.to(dev), v.to(dev), causal=w.causal, scale=w.softmax_scale)
+    fa.check_device_status()
+    assert torch.isfinite(lse).all()
+    sampled_check(w, o, lse, q, k, v)
