@@ -69,8 +69,9 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
 
 /*
  * Bytes of device workspace fa_bwd needs for these sizes: an fp32 dQ
- * accumulator of B*H*ceil(N/128)*128*d floats plus a per-row fp32 term
- * D_i = sum_k dO_ik O_ik of B*H*ceil(N/128)*128 floats.  Returns 0 when the
+ * accumulator of B*H*ceil(N/128)*128*d floats, then two per-row fp32
+ * terms of B*H*ceil(N/128)*128 floats each (D_i = sum_k dO_ik O_ik and
+ * lse_i * log2 e), each part rounded up to 256 bytes.  Returns 0 when the
  * sizes are invalid.
  */
 size_t fa_bwd_workspace_size(int B, int H, int N, int d);

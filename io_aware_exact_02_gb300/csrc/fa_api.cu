@@ -166,10 +166,7 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
 
 size_t fa_bwd_workspace_size(int B, int H, int N, int d) {
   if (check_shape(B, H, N, d, 1.0f) != FA_OK) return 0;
-  const size_t rows = (size_t)B * H * (size_t)ceil_div(N, kTile) * kTile;
-  size_t acc = rows * (size_t)d * sizeof(float);
-  acc = (acc + 255) & ~(size_t)255;
-  return acc + rows * sizeof(float);
+  return bwd_workspace_layout((long long)B * H, N, d).total;
 }
 
 int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
@@ -193,8 +190,7 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
   if ((rc = make_tmap_bhnd(k, BH, N, d, &tk)) != FA_OK) return rc;
   if ((rc = make_tmap_bhnd(v, BH, N, d, &tv)) != FA_OK) return rc;
   if ((rc = make_tmap_bhnd(dout, BH, N, d, &tdo)) != FA_OK) return rc;
-  const size_t rows = (size_t)BH * (size_t)ceil_div(N, kTile) * kTile;
-  size_t acc = (rows * (size_t)d * sizeof(float) + 255) & ~(size_t)255;
+  const BwdWorkspace ws = bwd_workspace_layout(BH, N, d);
   BwdParams p;
   p.o = o;
   p.dout = dout;
@@ -202,8 +198,9 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
   p.dq = dq;
   p.dk = dk;
   p.dv = dv;
-  p.dq_acc = static_cast<float*>(workspace);
-  p.delta = reinterpret_cast<float*>(static_cast<char*>(workspace) + acc);
+  p.dq_acc = reinterpret_cast<float*>(static_cast<char*>(workspace) + ws.dq_acc);
+  p.delta = reinterpret_cast<float*>(static_cast<char*>(workspace) + ws.delta);
+  p.lse2 = reinterpret_cast<float*>(static_cast<char*>(workspace) + ws.lse2);
   p.status = ds->status;
   p.BH = BH;
   p.N = N;

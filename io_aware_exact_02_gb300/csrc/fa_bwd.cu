@@ -1,9 +1,525 @@
-// fa_bwd.cu -- backward pass (placeholder until the kernels land).
+// fa_bwd.cu -- backward pass of exact attention on sm_103a, by recomputation.
+//
+// The forward pass kept only O and the per-row logsumexp; this pass
+// recomputes the scores and probabilities tile by tile on chip from Q, K, V
+// and lse instead of reading a stored N x N matrix (cs2680 Lecture 9,
+// sec. 9.6; "Reading CMU 11-868 LLM Systems: FlashAttention", slide page 14).
+// The gradient formulas are the softmax Jacobian (the pages print none):
+//     P = exp(scale Q K^T - lse),  dV = P^T dO,  dP = dO V^T,
+//     D_i = sum_k dO_ik O_ik,  dS = P o (dP - D),
+//     dQ = scale dS K,  dK = scale dS^T Q.
+//
+// Three kernels:
+//   1. prep: per row D_i, lse_i * log2(e) into the workspace (padded rows get
+//      D = 0, lse = +inf so that their probabilities are exactly 0), and the
+//      fp32 dQ accumulator zeroed.  HBM-bound.
+//   2. main: one CTA per (head, 128-key tile j).  K_j, V_j stay in shared
+//      memory; dK_j, dV_j accumulate in tensor memory while the CTA walks the
+//      query tiles i (all of them, or i >= j under a causal mask).  Per step:
+//        S^T  = K_j Q_i^T           (tcgen05, both operands in smem)
+//        dP^T = V_j dO_i^T
+//        P^T  = exp2(S^T c - lse_i log2 e)  -> bf16 in TMEM over S^T
+//        dV  += P^T dO_i                    (A operand from TMEM)
+//        dS^T = P^T o (dP^T - D_i)          -> bf16 in smem (128B swizzle)
+//        dK  += dS^T Q_i
+//        dQ_i = dS K_j  -> TMEM (over dP^T) -> fp32 vector atomics into the
+//                          workspace, by a dedicated warpgroup
+//   3. convert: dQ = bf16(scale * accumulator).
+//
+// Warp roles of the main kernel (384 threads):
+//   warps 0-3  compute (thread r owns key row r of the tile): P, dS, epilogue
+//   warps 4-7  dQ drain: TMEM -> registers -> atomic adds
+//   warp 8     TMA producer;  warp 9 MMA issuer and TMEM owner
+// Tensor memory: [0,128) S^T / P^T, [128,256) dP^T / dQ, [256,256+d) dV,
+// [256+d, 256+2d) dK.
 #include "fa_internal.h"
+#include "sm100_ptx.cuh"
 
 namespace fa {
-int launch_bwd(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
-               const BwdParams&, int, cudaStream_t) {
-  return FA_ERR_LAUNCH;
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+template <int D>
+struct BwdCfg {
+  static constexpr int kTileBytes = kTile * D * 2;  // one 128 x d bf16 tile
+  static constexpr int kStages = 2;                  // Q/dO ring
+  static constexpr int kThreads = 384;
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D;
+};
+
+template <int D>
+struct BwdSmem {
+  uint8_t k[BwdCfg<D>::kTileBytes];
+  uint8_t v[BwdCfg<D>::kTileBytes];
+  uint8_t q[BwdCfg<D>::kStages][BwdCfg<D>::kTileBytes];
+  uint8_t dO[BwdCfg<D>::kStages][BwdCfg<D>::kTileBytes];
+  uint8_t ds[kTile * kTile * 2];  // dS^T [key][query] bf16, 128B swizzle
+  float lse2[BwdCfg<D>::kStages][kTile];
+  float delta[BwdCfg<D>::kStages][kTile];
+  uint64_t kv_full;
+  uint64_t q_full[BwdCfg<D>::kStages];
+  uint64_t q_empty[BwdCfg<D>::kStages];
+  uint64_t s_full, dp_full, p_ready, ds_ready, dq_full, dq_empty, acc_full, drain;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+enum : int {
+  kSiteKvFull = 201, kSiteQFull, kSiteQEmpty, kSiteSFull, kSiteDpFull, kSitePReady,
+  kSiteDsReady, kSiteDqFull, kSiteDqEmpty, kSiteAccFull, kSiteAlign
+};
+
+__device__ __forceinline__ uint64_t kmajor_desc(uint32_t base, int kk) {
+  return sdesc_sw128(base + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
 }
+__device__ __forceinline__ uint64_t mnmajor_desc(uint32_t base, int kk) {
+  return sdesc_sw128(base + kk * 2048, 16384, 1024);
+}
+
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
+  const uint32_t a = smem_u32(bar);
+  const unsigned long long t0 = globaltimer_ns();
+  while (!mbar_try_wait(a, parity)) {
+    if (globaltimer_ns() - t0 > 100000000ull) return;
+  }
+}
+
+// Non-tensor bulk copy global -> shared, completing `bar`'s transaction count.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
+                                          uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Work order of the main kernel: heads in groups of kHeadGroup; inside a
+// group the key tiles go first to last (under a causal mask key tile j
+// visits n_kv - j query tiles, so the longest work items start first).
+__device__ __forceinline__ void bwd_item(int t, int BH, int n_kv, int* bh, int* j) {
+  const int per_group = kHeadGroup * n_kv;
+  const int g = t / per_group;
+  const int gsize = (BH - g * kHeadGroup) < kHeadGroup ? (BH - g * kHeadGroup) : kHeadGroup;
+  const int idx = t - g * per_group;
+  *j = idx / gsize;
+  *bh = g * kHeadGroup + idx % gsize;
+}
+
+// Address (in floats) of element (row, 4*c4 .. 4*c4+3) of the dQ accumulator.
+// The accumulator is blocked per 128-row tile as [tile][d/4][128][4] so that
+// the 32 rows of a warp add to 512 contiguous bytes.
+template <int D>
+__device__ __forceinline__ size_t dqacc_index(int bh, int n_kv, int row, int c4) {
+  const int tile = row >> 7, r = row & 127;
+  return ((((size_t)bh * n_kv + tile) * (D / 4) + c4) * kTile + r) * 4;
+}
+
+// ------------------------------------------------------------------ prep
+
+template <int D>
+__global__ void __launch_bounds__(256) fa_bwd_prep_kernel(const BwdParams p) {
+  constexpr int kLanesPerRow = D / 8;  // 16-byte loads of 8 bf16
+  constexpr int kRowsPerWarp = 32 / kLanesPerRow;
+  const int lane = threadIdx.x & 31;
+  const int warp_global = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int npad = p.n_kv * kTile;
+  const long long total_rows = (long long)p.BH * npad;
+  const long long row_g = (long long)warp_global * kRowsPerWarp + lane / kLanesPerRow;
+  const int sub = lane % kLanesPerRow;
+  float acc = 0.f;
+  int bh = 0, row = 0;
+  const bool in_range = row_g < total_rows;
+  if (in_range) {
+    bh = (int)(row_g / npad);
+    row = (int)(row_g % npad);
+    if (row < p.N) {
+      const size_t off = ((size_t)bh * p.N + row) * D + sub * 8;
+      const uint4 a = *reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(p.o) + off);
+      const uint4 b = *reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(p.dout) + off);
+      const __nv_bfloat162* ha = reinterpret_cast<const __nv_bfloat162*>(&a);
+      const __nv_bfloat162* hb = reinterpret_cast<const __nv_bfloat162*>(&b);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 fa2 = __bfloat1622float2(ha[i]);
+        const float2 fb2 = __bfloat1622float2(hb[i]);
+        acc = fmaf(fa2.x, fb2.x, acc);
+        acc = fmaf(fa2.y, fb2.y, acc);
+      }
+    }
+  }
+#pragma unroll
+  for (int o = kLanesPerRow / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  if (in_range) {
+    if (sub == 0) {
+      const size_t ri = (size_t)bh * npad + row;
+      p.delta[ri] = acc;
+      p.lse2[ri] = row < p.N ? p.lse[(size_t)bh * p.N + row] * kLog2e : __int_as_float(0x7f800000);
+    }
+    // Zero this row of the dQ accumulator: D floats, 4 per lane-slot.
+    for (int c4 = sub; c4 < D / 4; c4 += kLanesPerRow)
+      *reinterpret_cast<float4*>(p.dq_acc + dqacc_index<D>(bh, p.n_kv, row, c4)) =
+          make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+}
+
+// ------------------------------------------------------------------ convert
+
+template <int D>
+__global__ void __launch_bounds__(256) fa_bwd_convert_kernel(const BwdParams p) {
+  // One thread per 8 output elements (one 16-byte store).
+  const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  const long long total = (long long)p.BH * p.N * (D / 8);
+  if (idx >= total) return;
+  const int c8 = (int)(idx % (D / 8));
+  const long long rg = idx / (D / 8);
+  const int bh = (int)(rg / p.N), row = (int)(rg % p.N);
+  const float4 a = *reinterpret_cast<const float4*>(p.dq_acc + dqacc_index<D>(bh, p.n_kv, row, 2 * c8));
+  const float4 b = *reinterpret_cast<const float4*>(p.dq_acc + dqacc_index<D>(bh, p.n_kv, row, 2 * c8 + 1));
+  uint4 out;
+  out.x = pack_bf16x2(a.x * p.scale, a.y * p.scale);
+  out.y = pack_bf16x2(a.z * p.scale, a.w * p.scale);
+  out.z = pack_bf16x2(b.x * p.scale, b.y * p.scale);
+  out.w = pack_bf16x2(b.z * p.scale, b.w * p.scale);
+  *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.dq) + ((size_t)bh * p.N + row) * D +
+                            c8 * 8) = out;
+}
+
+// ------------------------------------------------------------------ main
+
+template <int D>
+__global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
+    fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                       const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
+                       const BwdParams p) {
+  using Cfg = BwdCfg<D>;
+  constexpr int NS = Cfg::kStages;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // The swizzled tiles need 1024-byte alignment; the dynamic window starts
+  // there on this architecture, and the size leaves no slack to realign.
+  if ((smem_u32(smem_raw) & 1023u) != 0) {
+    if (threadIdx.x == 0) {
+      atomicCAS(p.status, 0, FA_ERR_LAUNCH);
+      atomicCAS(p.status + 1, 0, kSiteAlign);
+    }
+    return;
+  }
+  BwdSmem<D>& sm = *reinterpret_cast<BwdSmem<D>*>(smem_raw);
+  volatile int* abortf = &sm.abort_flag;
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+
+  if (tid == 0) {
+    mbar_init(&sm.kv_full, 1);
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&sm.q_full[s], 1);
+      mbar_init(&sm.q_empty[s], 1);
+    }
+    mbar_init(&sm.s_full, 1);
+    mbar_init(&sm.dp_full, 1);
+    mbar_init(&sm.p_ready, 128);
+    mbar_init(&sm.ds_ready, 128);
+    mbar_init(&sm.dq_full, 1);
+    mbar_init(&sm.dq_empty, 128);
+    mbar_init(&sm.acc_full, 1);
+    mbar_init(&sm.drain, 1);
+    sm.abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(&sm.tmem_base, Cfg::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem_base;
+
+  int bh, j;
+  bwd_item(blockIdx.x, p.BH, p.n_kv, &bh, &j);
+  const int i0 = p.causal ? j : 0;
+  const int n_iter = p.n_kv - i0;
+  const int npad = p.n_kv * kTile;
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ producer
+    if (lane_id() == 0) {
+      prefetch_tmap(&tq);
+      prefetch_tmap(&tk);
+      prefetch_tmap(&tv);
+      prefetch_tmap(&tdo);
+      mbar_arrive_expect_tx(&sm.kv_full, 2 * Cfg::kTileBytes);
+      for (int h = 0; h < D / 64; ++h) {
+        tma_load_3d(sm.k + h * 16384, &tk, &sm.kv_full, h * 64, j * kTile, bh);
+        tma_load_3d(sm.v + h * 16384, &tv, &sm.kv_full, h * 64, j * kTile, bh);
+      }
+      int it = 0;
+      for (; it < n_iter; ++it) {
+        const int s = it % NS, use = it / NS;
+        if (use > 0 && !mbar_wait(&sm.q_empty[s], (use - 1) & 1, p.status, abortf, kSiteQEmpty))
+          break;
+        const int i = i0 + it;
+        mbar_arrive_expect_tx(&sm.q_full[s], 2 * Cfg::kTileBytes + 2 * kTile * 4);
+        for (int h = 0; h < D / 64; ++h) {
+          tma_load_3d(sm.q[s] + h * 16384, &tq, &sm.q_full[s], h * 64, i * kTile, bh);
+          tma_load_3d(sm.dO[s] + h * 16384, &tdo, &sm.q_full[s], h * 64, i * kTile, bh);
+        }
+        bulk_load(sm.lse2[s], p.lse2 + (size_t)bh * npad + i * kTile, kTile * 4, &sm.q_full[s]);
+        bulk_load(sm.delta[s], p.delta + (size_t)bh * npad + i * kTile, kTile * 4, &sm.q_full[s]);
+      }
+      if (it < n_iter) {
+        drain_wait(&sm.kv_full, 0);
+        for (int c = it - 1; c >= 0 && c >= it - NS; --c) drain_wait(&sm.q_full[c % NS], (c / NS) & 1);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 9) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane_id() == 0) {
+      const uint32_t id_s = idesc_bf16(128, 128, false, false);   // S^T, dP^T
+      const uint32_t id_acc = idesc_bf16(128, D, false, true);    // dV, dK
+      const uint32_t id_dq = idesc_bf16(128, D, true, true);      // dQ
+      const uint32_t kb = smem_u32(sm.k), vb = smem_u32(sm.v), dsb = smem_u32(sm.ds);
+      bool ok = mbar_wait(&sm.kv_full, 0, p.status, abortf, kSiteKvFull);
+      for (int it = 0; it < n_iter && ok; ++it) {
+        const int s = it % NS;
+        const uint32_t par = it & 1;
+        const uint32_t qb = smem_u32(sm.q[s]), dob = smem_u32(sm.dO[s]);
+        ok = mbar_wait(&sm.q_full[s], (it / NS) & 1, p.status, abortf, kSiteQFull);
+        if (!ok) break;
+        tc_fence_after();
+        // S^T = K_j Q_i^T
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_ss(tmem + Cfg::kColS, kmajor_desc(kb, kk), kmajor_desc(qb, kk), id_s, kk > 0);
+        tc_commit(&sm.s_full);
+        // dP^T = V_j dO_i^T, into the columns dQ_{i-1} occupied
+        if (it > 0) {
+          ok = mbar_wait(&sm.dq_empty, (it - 1) & 1, p.status, abortf, kSiteDqEmpty);
+          if (!ok) break;
+          tc_fence_after();
+        }
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_ss(tmem + Cfg::kColDP, kmajor_desc(vb, kk), kmajor_desc(dob, kk), id_s, kk > 0);
+        tc_commit(&sm.dp_full);
+        // dV += P^T dO_i
+        ok = mbar_wait(&sm.p_ready, par, p.status, abortf, kSitePReady);
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk)
+          mma_ts(tmem + Cfg::kColDV, tmem + Cfg::kColS + kk * 8, mnmajor_desc(dob, kk), id_acc,
+                 (it > 0 || kk > 0) ? 1u : 0u);
+        // dK += dS^T Q_i ; dQ_i = dS K_j
+        ok = mbar_wait(&sm.ds_ready, par, p.status, abortf, kSiteDsReady);
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk)
+          mma_ss(tmem + Cfg::kColDK, kmajor_desc(dsb, kk), mnmajor_desc(qb, kk), id_acc,
+                 (it > 0 || kk > 0) ? 1u : 0u);
+        tc_commit(&sm.q_empty[s]);
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk)
+          mma_ss(tmem + Cfg::kColDP, mnmajor_desc(dsb, kk), mnmajor_desc(kb, kk), id_dq, kk > 0);
+        tc_commit(&sm.dq_full);
+      }
+      if (ok) tc_commit(&sm.acc_full);
+      tc_commit(&sm.drain);
+      drain_wait(&sm.drain, 0);
+    }
+    __syncwarp();
+  } else if (warp < 4) {
+    // ------------------------------------------------------------ compute
+    const int r = tid;  // key row within the tile
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t colS = tmem + lane_base + Cfg::kColS;
+    const uint32_t colDP = tmem + lane_base + Cfg::kColDP;
+    const float c2 = p.scale_log2;
+    const int kv_row = j * kTile + r;
+    bool ok = true;
+    for (int it = 0; it < n_iter; ++it) {
+      const int s = it % NS;
+      const uint32_t par = it & 1;
+      const int i = i0 + it;
+      const bool diag = p.causal && i == j;
+      ok = mbar_wait(&sm.q_full[s], (it / NS) & 1, p.status, abortf, kSiteQFull);
+      if (ok) ok = mbar_wait(&sm.s_full, par, p.status, abortf, kSiteSFull);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      const float* lse2 = sm.lse2[s];
+      uint32_t pk[64];  // P^T row, bf16 pairs
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t sr[2][32];
+        tmem_ld32(colS + h * 64, sr[0]);
+        tmem_ld32(colS + h * 64 + 32, sr[1]);
+        tmem_wait_ld(sr[0]);
+        tmem_wait_ld(sr[1]);
+#pragma unroll
+        for (int c = 0; c < 2; ++c)
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            const int col = h * 64 + c * 32 + e;  // query column within the tile
+            float p0 = ex2_approx(fmaf(__uint_as_float(sr[c][e]), c2, -lse2[col]));
+            float p1 = ex2_approx(fmaf(__uint_as_float(sr[c][e + 1]), c2, -lse2[col + 1]));
+            if (diag) {
+              if (r > col) p0 = 0.f;
+              if (r > col + 1) p1 = 0.f;
+            }
+            pk[h * 32 + c * 16 + e / 2] = pack_bf16x2(p0, p1);
+          }
+        uint32_t st[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) st[e] = pk[h * 32 + e];
+        tmem_st32(colS + h * 32, st);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&sm.p_ready);
+
+      ok = mbar_wait(&sm.dp_full, par, p.status, abortf, kSiteDpFull);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      const float* dl = sm.delta[s];
+      uint8_t* ds_row = sm.ds + r * 128;  // row r of both 64-column blocks
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t dp[32];
+        tmem_ld32(colDP + c * 32, dp);
+        tmem_wait_ld(dp);
+        uint32_t w[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const int col = c * 32 + 2 * e;
+          const float2 pf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pk[col / 2]));
+          const float d0 = pf.x * (__uint_as_float(dp[2 * e]) - dl[col]);
+          const float d1 = pf.y * (__uint_as_float(dp[2 * e + 1]) - dl[col + 1]);
+          w[e] = pack_bf16x2(d0, d1);
+        }
+        // 32 bf16 = four 16-byte chunks of the 128B-swizzled row.
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const int chunk = c * 4 + q4;       // 0..15 over the 128 columns
+          const int blk = chunk >> 3, ch = chunk & 7;
+          *reinterpret_cast<uint4*>(ds_row + blk * 16384 + ((ch ^ (r & 7)) << 4)) =
+              make_uint4(w[4 * q4], w[4 * q4 + 1], w[4 * q4 + 2], w[4 * q4 + 3]);
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(&sm.ds_ready);
+    }
+    // Epilogue: dV and scale * dK of this key row.
+    if (ok) ok = mbar_wait(&sm.acc_full, 0, p.status, abortf, kSiteAccFull);
+    ok = __all_sync(0xffffffffu, ok);
+    if (ok) {
+      tc_fence_after();
+#pragma unroll
+      for (int which = 0; which < 2; ++which) {
+        const uint32_t col = tmem + lane_base + (which == 0 ? Cfg::kColDV : Cfg::kColDK);
+        const float mul = which == 0 ? 1.f : p.scale;
+        __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(which == 0 ? p.dv : p.dk) +
+                             ((size_t)bh * p.N + kv_row) * D;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t a[32];
+          tmem_ld32(col + c * 32, a);
+          tmem_wait_ld(a);
+          if (kv_row < p.N) {
+            uint4 v[4];
+            uint32_t* w = reinterpret_cast<uint32_t*>(v);
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+              w[e] = pack_bf16x2(__uint_as_float(a[2 * e]) * mul, __uint_as_float(a[2 * e + 1]) * mul);
+            uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) d4[e] = v[e];
+          }
+        }
+      }
+    }
+  } else if (warp < 8) {
+    // ------------------------------------------------------------ dQ drain
+    const int r = tid - 128;  // query row within the tile
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t colDQ = tmem + lane_base + Cfg::kColDP;
+    for (int it = 0; it < n_iter; ++it) {
+      bool ok = mbar_wait(&sm.dq_full, it & 1, p.status, abortf, kSiteDqFull);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t a[D / 32][32];
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) tmem_ld32(colDQ + c * 32, a[c]);
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) tmem_wait_ld(a[c]);
+      tc_fence_before();
+      mbar_arrive(&sm.dq_empty);
+      const int row = (i0 + it) * kTile + r;
+      float* base = p.dq_acc + dqacc_index<D>(bh, p.n_kv, row, 0);
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float4 val = make_float4(__uint_as_float(a[c][4 * e]), __uint_as_float(a[c][4 * e + 1]),
+                                         __uint_as_float(a[c][4 * e + 2]), __uint_as_float(a[c][4 * e + 3]));
+          atomicAdd(reinterpret_cast<float4*>(base + (size_t)(c * 8 + e) * kTile * 4), val);
+        }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after();
+    tmem_dealloc(tmem, Cfg::kTmemCols);
+  }
+}
+
+template <int D>
+int launch_bwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                 const CUtensorMap& tdo, const BwdParams& p, cudaStream_t stream) {
+  const long long npad = (long long)p.n_kv * kTile;
+  // 1. prep: one warp per (32 / (D/8)) rows.
+  {
+    const long long rows = (long long)p.BH * npad;
+    const long long warps = (rows + (32 / (D / 8)) - 1) / (32 / (D / 8));
+    const long long blocks = (warps * 32 + 255) / 256;
+    fa_bwd_prep_kernel<D><<<(unsigned)blocks, 256, 0, stream>>>(p);
+    if (cudaGetLastError() != cudaSuccess) return FA_ERR_LAUNCH;
+  }
+  // 2. main
+  {
+    const size_t smem = sizeof(BwdSmem<D>);
+    if (cudaFuncSetAttribute(fa_bwd_main_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem) != cudaSuccess)
+      return FA_ERR_LAUNCH;
+    const unsigned grid = (unsigned)p.BH * (unsigned)p.n_kv;
+    fa_bwd_main_kernel<D><<<grid, BwdCfg<D>::kThreads, smem, stream>>>(tq, tk, tv, tdo, p);
+    if (cudaGetLastError() != cudaSuccess) return FA_ERR_LAUNCH;
+  }
+  // 3. convert
+  {
+    const long long total = (long long)p.BH * p.N * (D / 8);
+    fa_bwd_convert_kernel<D><<<(unsigned)((total + 255) / 256), 256, 0, stream>>>(p);
+    if (cudaGetLastError() != cudaSuccess) return FA_ERR_LAUNCH;
+  }
+  return FA_OK;
+}
+
+}  // namespace
+
+int launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+               const CUtensorMap& tdo, const BwdParams& p, int d, cudaStream_t stream) {
+  if (d == 128) return launch_bwd_d<128>(tq, tk, tv, tdo, p, stream);
+  if (d == 64) return launch_bwd_d<64>(tq, tk, tv, tdo, p, stream);
+  return FA_ERR_UNSUPPORTED_D;
+}
+
 }  // namespace fa

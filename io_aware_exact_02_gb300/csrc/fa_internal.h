@@ -57,6 +57,7 @@ struct BwdParams {
   void* dv;
   float* dq_acc;     // workspace: [BH][n_kv*128][d] fp32, tile-blocked
   float* delta;      // workspace: [BH][n_kv*128] fp32 (D_i)
+  float* lse2;       // workspace: [BH][n_kv*128] fp32 (lse_i * log2 e, +inf past N)
   int* status;
   int BH, N;
   int n_kv;
@@ -72,6 +73,22 @@ int make_tmap_bhnd(const void* base, int BH, int N, int d, CUtensorMap* out);
 
 int launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                const FwdParams& p, int d, cudaStream_t stream);
+
+// Byte offsets of the backward workspace's parts for these sizes:
+// the fp32 dQ accumulator, then D, then lse * log2(e), each 256-byte aligned.
+struct BwdWorkspace {
+  size_t dq_acc, delta, lse2, total;
+};
+inline BwdWorkspace bwd_workspace_layout(long long BH, int N, int d) {
+  const size_t rows = (size_t)BH * (size_t)ceil_div(N, kTile) * kTile;
+  auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
+  BwdWorkspace w;
+  w.dq_acc = 0;
+  w.delta = up(rows * (size_t)d * sizeof(float));
+  w.lse2 = w.delta + up(rows * sizeof(float));
+  w.total = w.lse2 + up(rows * sizeof(float));
+  return w;
+}
 
 int launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                const CUtensorMap& tdo, const BwdParams& p, int d, cudaStream_t stream);

@@ -82,7 +82,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // Per-CTA abort protocol: the first waiter that times out stores the code
 // in the device status word (first error wins) and sets the CTA's abort
 // flag; every other waiter polls that flag and gives up too.
-__device__ __noinline__ void report_timeout(int* status, volatile int* abort_flag, int site) {
+static __device__ __noinline__ void report_timeout(int* status, volatile int* abort_flag, int site) {
   atomicCAS(status, 0, kStatusTimeout);
   atomicCAS(status + 1, 0, site);
   *abort_flag = 1;

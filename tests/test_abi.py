@@ -88,9 +88,13 @@ def test_bwd_argument_errors_launch_nothing(lib):
 
 
 def test_workspace_size(lib):
-    # fp32 dQ accumulator over 128-row-padded rows plus one fp32 per row.
-    assert lib.fa_bwd_workspace_size(2, 3, 300, 64) == 2 * 3 * 384 * 64 * 4 + 2 * 3 * 384 * 4
-    assert lib.fa_bwd_workspace_size(1, 1, 128, 128) == 128 * 128 * 4 + 128 * 4
+    # fp32 dQ accumulator over 128-row-padded rows plus two fp32 per row.
+    def up(x):
+        return (x + 255) // 256 * 256
+    rows = 2 * 3 * 384
+    assert lib.fa_bwd_workspace_size(2, 3, 300, 64) == up(rows * 64 * 4) + 2 * up(rows * 4)
+    assert lib.fa_bwd_workspace_size(1, 1, 128, 128) == 128 * 128 * 4 + 2 * 128 * 4
+    assert lib.fa_bwd_workspace_size(1, 1, 1, 64) == 128 * 64 * 4 + 2 * 512
     assert lib.fa_bwd_workspace_size(1, 1, 0, 64) == 0
     assert lib.fa_bwd_workspace_size(1, 1, 128, 72) == 0
 

@@ -1,0 +1,130 @@
+"""Backward pass on the GPU (through the C ABI) against the fp64 oracle.
+
+The forward outputs O and lse the backward pass consumes come from the GPU
+forward pass (the path a user runs); the oracle recomputes everything from
+q, k, v, dO alone.  Tolerance (bf16 in/out, fp32 accumulation, bf16 P and
+dS as tensor-core operands): for each of dQ, dK, dV,
+    max |G_gpu - G_oracle| / max |G_oracle| <= 3e-2.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from io_aware_exact_02_gb300 import build, fa, synth
+
+pytestmark = pytest.mark.gpu
+
+G_REL = 3e-2
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    build.build()
+    return fa.load()
+
+
+def run(q, k, v, do, causal, scale):
+    dev = torch.device("cuda")
+    q, k, v, do = (t.to(dev) for t in (q, k, v, do))
+    o, lse = fa.fwd(q, k, v, causal=causal, scale=scale)
+    dq, dk, dv = fa.bwd(q, k, v, o, do, lse, causal=causal, scale=scale)
+    fa.check_device_status()
+    return dq, dk, dv
+
+
+def rel_err(g, ref):
+    g = g.float().cpu().numpy().astype(np.float64)
+    assert np.isfinite(g).all()
+    den = np.abs(ref).max()
+    return np.abs(g - ref).max() / (den if den > 0 else 1.0)
+
+
+def check(gpu, ref, what):
+    for name, g, r in zip(("dq", "dk", "dv"), gpu, ref):
+        e = rel_err(g, r)
+        assert e <= G_REL, (what, name, e)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("N", [1, 17, 127, 128, 129, 256, 300, 1000])
+def test_bwd_matches_oracle_small(N, causal, d):
+    B, H = 2, 2
+    q, k, v, do = synth.draw(B, H, N, d, seed=1000 + N + d + causal)
+    scale = 1.0 / math.sqrt(d)
+    gpu = run(q, k, v, do, causal, scale)
+    ref = oracle.attn_bwd(q, k, v, do, causal, scale)
+    check(gpu, ref, "N=%d causal=%d d=%d" % (N, causal, d))
+
+
+@pytest.mark.parametrize("scale", [-0.3, 0.7])
+def test_bwd_other_scales(scale):
+    q, k, v, do = synth.draw(1, 2, 200, 64, seed=77)
+    for causal in (False, True):
+        gpu = run(q, k, v, do, causal, scale)
+        ref = oracle.attn_bwd(q, k, v, do, causal, scale)
+        check(gpu, ref, "scale=%g causal=%d" % (scale, causal))
+
+
+def test_bwd_scale_zero_closed_form():
+    # scale = 0: every probability is 1/N (non-causal), so dV_j = mean_i dO_i
+    # and dQ = dK = 0 exactly (both carry the factor scale).
+    B, H, N, d = 1, 2, 384, 64
+    q, k, v, do = synth.draw(B, H, N, d, seed=5)
+    dq, dk, dv = run(q, k, v, do, False, 0.0)
+    assert torch.count_nonzero(dq) == 0 and torch.count_nonzero(dk) == 0
+    mean = do.double().mean(2, keepdim=True).expand(B, H, N, d).numpy()
+    assert np.abs(dv.double().cpu().numpy() - mean).max() < 2e-3
+
+
+def test_bwd_heavy_rows():
+    q, k, v, do = synth.draw(1, 2, 1024, 128, seed=8, heavy_frac=0.01)
+    for causal in (False, True):
+        gpu = run(q, k, v, do, causal, 1 / math.sqrt(128))
+        ref = oracle.attn_bwd(q, k, v, do, causal, 1 / math.sqrt(128))
+        check(gpu, ref, "heavy causal=%d" % causal)
+
+
+def test_bwd_dk_dv_deterministic():
+    q, k, v, do = synth.draw(2, 2, 700, 128, seed=4)
+    a = run(q, k, v, do, True, 0.1)
+    b = run(q, k, v, do, True, 0.1)
+    assert torch.equal(a[1], b[1]) and torch.equal(a[2], b[2])
+    # dQ is summed with atomics: equal up to the order of fp32 additions.
+    assert (a[0].float() - b[0].float()).abs().max().item() < 1e-2
+
+
+def test_bwd_rejects_small_workspace():
+    q, k, v, do = synth.draw(1, 1, 128, 64, seed=2)
+    dev = torch.device("cuda")
+    q, k, v, do = (t.to(dev) for t in (q, k, v, do))
+    o, lse = fa.fwd(q, k, v)
+    ws = torch.empty(fa.bwd_workspace_size(1, 1, 128, 64) - 256, dtype=torch.uint8, device=dev)
+    with pytest.raises(fa.FaError) as e:
+        fa.bwd(q, k, v, o, do, lse, workspace=ws)
+    assert e.value.code == fa.FA_ERR_WORKSPACE
+
+
+# --------------------------------------- full-size workloads, sampled heads
+
+FULL_BWD = {"causal_lm": 2, "long": 1, "small_batch": 2, "sweep_N8192_d128": 1, "tiny": 1}
+
+
+@pytest.mark.parametrize("name", sorted(FULL_BWD))
+def test_bwd_full_size_sampled_heads(name):
+    w = synth.by_name(name)
+    q, k, v, do = synth.draw_workload(w)
+    dq, dk, dv = run(q, k, v, do, w.causal, w.softmax_scale)
+    BH = w.BH
+    rng = np.random.default_rng(1)
+    heads = sorted(set([BH - 1] + rng.choice(BH, size=FULL_BWD[name], replace=False).tolist()))[
+        : FULL_BWD[name]]
+
+    def sel(t):
+        return t.reshape(BH, w.N, w.d)[heads].unsqueeze(0)
+
+    ref = oracle.attn_bwd(sel(q), sel(k), sel(v), sel(do), w.causal, w.softmax_scale)
+    check((sel(dq.cpu()), sel(dk.cpu()), sel(dv.cpu())), ref, name)
