@@ -1,0 +1,439 @@
+"""Benchmark of the attention hot path: one step = fa_fwd + fa_bwd over one
+batch of synthetic input, at the slides' largest forward-sweep size with
+d = 128 (B=8, H=16, N=8192, non-causal, scale 1/sqrt(d)).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Prints one JSON line (rank 0).  FLOPs follow the pages' count: forward
+4*B*H*N^2*d (two S x S x d matmuls per head, cs2680 Lecture 9 sec. 9.2),
+halved when causal; backward 2.5x the forward.  ``value`` is whole-job
+TFLOPS with the inputs resident in HBM; ``e2e`` is the same metric with the
+step's inputs copied from pinned host memory and its outputs copied back
+inside the timed region.  Every rank (one per GPU, launched by torchrun)
+runs its own independent batch (weak scaling, no data-path collective);
+timing is the max over ranks, exchanged over gloo.
+
+``--impl reference`` times the fp64 CPU oracle (the reference arm of this
+build) on a bounded sample of the same workload on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "attention fwd/bwd TFLOPS (bf16, d=128, N=1K-16K) and % of GB300 bf16 tensor peak"
+UNIT = "TFLOPS"
+WORKLOAD = dict(name="sweep_N8192_d128", B=8, H=16, N=8192, d=128, causal=False)
+PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_BYTES = 129 * 1024 * 1024
+
+
+# ----------------------------------------------------------------- host logic
+
+def fwd_flops(B, H, N, d, causal):
+    f = 4.0 * B * H * N * N * d
+    return f * 0.5 if causal else f
+
+
+def step_flops(w):
+    f = fwd_flops(w["B"], w["H"], w["N"], w["d"], w["causal"])
+    return f, 2.5 * f
+
+
+def rank_seed(base: int, rank: int) -> int:
+    """Each rank draws its own batch: a disjoint stream of the same recipe."""
+    return base + 1000003 * rank
+
+
+def aggregate(per_rank_flops: float, world: int, max_seconds: float) -> float:
+    """Whole-job TFLOPS: all ranks' FLOPs over the slowest rank's time."""
+    return per_rank_flops * world / max_seconds / 1e12
+
+
+def reduce_max(value: float, group=None) -> float:
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return value
+    t = torch.tensor([value], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX, group=group)
+    return float(t.item())
+
+
+def barrier(group=None):
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier(group=group)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return dict(PEAKS_FALLBACK), "fallback"
+
+
+def source_hash(path: str) -> str:
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def profiled_traffic(kernel_key: str):
+    """DRAM bytes per launch of a kernel from the committed ncu summary, if it
+    was captured on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            t = json.load(f)
+        ent = t[kernel_key]
+        src = os.path.join(ROOT, ent["source"])
+        if source_hash(src) != ent["source_sha256_16"]:
+            return None
+        return float(ent["dram_bytes_per_launch"])
+    except (OSError, ValueError, KeyError):
+        return None
+
+
+def gpu_selector(local_rank: int) -> str:
+    """nvidia-smi -i argument for this rank's GPU (its UUID when torch knows it)."""
+    import torch
+    try:
+        u = str(torch.cuda.get_device_properties(local_rank).uuid)
+        if u and u != "None":
+            return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        pass
+    return str(local_rank)
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason sampler running during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: str):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=5)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) != 6:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[2:]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def workload_dict(name: str):
+    from io_aware_exact_02_gb300 import synth
+    if name == WORKLOAD["name"]:
+        return dict(WORKLOAD)
+    wl = synth.by_name(name)
+    return dict(name=wl.name, B=wl.B, H=wl.H, N=wl.N, d=wl.d, causal=wl.causal)
+
+
+# ------------------------------------------------------------ reference arm
+
+def cpu_sample(w, heads: int, seed: int = 0):
+    """Time the fp64 oracle on `heads` whole heads of the workload (fwd + bwd).
+
+    Returns (TFLOPS by the workload's FLOP count for that sample, seconds,
+    threads)."""
+    import oracle
+    from io_aware_exact_02_gb300 import synth
+    q, k, v, do = synth.draw(1, heads, w["N"], w["d"], seed=seed)
+    scale = 1.0 / math.sqrt(w["d"])
+    t0 = time.perf_counter()
+    oracle.attn_fwd(q, k, v, w["causal"], scale)
+    oracle.attn_bwd(q, k, v, do, w["causal"], scale)
+    dt = time.perf_counter() - t0
+    ff, bf = step_flops(dict(w, B=1, H=heads))
+    return (ff + bf) / dt / 1e12, dt, oracle.num_threads()
+
+
+def run_reference(args, w, rank, world):
+    if rank != 0:
+        return 0
+    heads = args.ref_heads
+    for _ in range(args.warmup):
+        cpu_sample(w, heads)
+    times = []
+    threads = 1
+    for _ in range(args.steps):
+        _, dt, threads = cpu_sample(w, heads)
+        times.append(dt)
+    ff, bf = step_flops(dict(w, B=1, H=heads))
+    sec = statistics.mean(times)
+    value = (ff + bf) / sec / 1e12
+    sample = ("fwd+bwd of %d of %d heads (N=%d, d=%d, %s) per step, fp64 oracle on host cores"
+              % (heads, w["B"] * w["H"], w["N"], w["d"], "causal" if w["causal"] else "non-causal"))
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": w["name"], "B": w["B"], "H": w["H"], "N": w["N"], "d": w["d"],
+                   "causal": w["causal"], "sample_heads": heads},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------ GPU arm
+
+def run_gpu(args, w, rank, world, local_rank):
+    import torch
+    from io_aware_exact_02_gb300 import fa, synth
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    fa.load()
+    B, H, N, d, causal = w["B"], w["H"], w["N"], w["d"], w["causal"]
+    scale = 1.0 / math.sqrt(d)
+    seed = rank_seed(args.seed, rank)
+    q, k, v, do = synth.draw(B, H, N, d, seed=seed, device=dev)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+    ws = torch.empty(fa.bwd_workspace_size(B, H, N, d), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    in_bytes = q.numel() * q.element_size()
+    l2_note = ("inputs larger than L2 (each of Q, K, V, dO is %d MiB > 129 MB)" % (in_bytes >> 20)
+               if in_bytes > L2_BYTES else "inputs smaller than L2")
+
+    def step(events=None):
+        if events is not None:
+            events[0].record(stream)
+        fa.fwd(q, k, v, causal=causal, scale=scale, out=o, lse=lse)
+        if events is not None:
+            events[1].record(stream)
+        fa.bwd(q, k, v, o, do, lse, causal=causal, scale=scale, dq=dq, dk=dk, dv=dv,
+               workspace=ws, phases=1)
+        if events is not None:
+            events[2].record(stream)
+        fa.bwd(q, k, v, o, do, lse, causal=causal, scale=scale, dq=dq, dk=dk, dv=dv,
+               workspace=ws, phases=2)
+        if events is not None:
+            events[3].record(stream)
+        fa.bwd(q, k, v, o, do, lse, causal=causal, scale=scale, dq=dq, dk=dk, dv=dv,
+               workspace=ws, phases=4)
+        if events is not None:
+            events[4].record(stream)
+
+    launches_per_step = 4  # fwd, bwd prep, bwd main, dQ convert
+    for _ in range(args.warmup):
+        step()
+    fa.check_device_status()
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    sampler = ClockSampler(gpu_selector(local_rank))
+    sampler.start()
+    time.sleep(0.3)
+    barrier()
+    torch.cuda.synchronize(dev)
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for s in range(args.steps):
+        step(evs[s])
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    clocks = sampler.stop()
+    fa.check_device_status()
+    elapsed = t_start.elapsed_time(t_end) / 1e3
+    per_kernel = {"fwd": 0.0, "bwd_prep": 0.0, "bwd_main": 0.0, "bwd_convert": 0.0}
+    names = list(per_kernel)
+    for s in range(args.steps):
+        for i, nm in enumerate(names):
+            per_kernel[nm] += evs[s][i].elapsed_time(evs[s][i + 1]) / 1e3
+    max_elapsed = reduce_max(elapsed)
+    ff, bf = step_flops(w)
+    value = aggregate((ff + bf) * args.steps, world, max_elapsed)
+
+    # ---------------------------------------------------------- end to end
+    e2e = None
+    if not args.no_e2e:
+        e2e_steps = max(1, min(args.steps, args.e2e_steps))
+        hq, hk, hv, hdo = (t.to("cpu").pin_memory() for t in (q, k, v, do))
+        ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+        hlse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+        hdq, hdk, hdv = (torch.empty(q.shape, dtype=q.dtype).pin_memory() for _ in range(3))
+
+        def e2e_step():
+            for dst, src in ((q, hq), (k, hk), (v, hv), (do, hdo)):
+                dst.copy_(src, non_blocking=True)
+            fa.fwd(q, k, v, causal=causal, scale=scale, out=o, lse=lse)
+            fa.bwd(q, k, v, o, do, lse, causal=causal, scale=scale, dq=dq, dk=dk, dv=dv,
+                   workspace=ws)
+            for dst, src in ((ho, o), (hlse, lse), (hdq, dq), (hdk, dk), (hdv, dv)):
+                dst.copy_(src, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize(dev)
+        barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier()
+        fa.check_device_status()
+        e2e_sec = reduce_max(e0.elapsed_time(e1) / 1e3)
+        h2d = 4 * in_bytes
+        d2h = 4 * in_bytes + lse.numel() * 4
+        e2e = {"value": aggregate((ff + bf) * e2e_steps, world, e2e_sec), "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps}
+
+    # ------------------------------------------------------------ roofline
+    peaks, peak_kind = load_peaks()
+    peak = float(peaks["bf16_tflops"])
+    main_avg = per_kernel["bwd_main"] / args.steps
+    fwd_avg = per_kernel["fwd"] / args.steps
+    achieved = bf / main_avg / 1e12
+    roofline = {"bound": "tensor", "kernel": "fa_bwd_main_kernel<%d>" % d, "achieved": achieved,
+                "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                "peak_kind": "%s burst bf16 (MEASURED_PEAKS.json bf16_tflops)" % peak_kind
+                if peak_kind == "measured" else "fallback burst bf16",
+                "frac_of_sustained": achieved / float(peaks.get("bf16_tflops_sustained", peak)),
+                "traffic": profiled_traffic("fa_bwd_main_kernel_d%d_%s" % (d, w["name"]))}
+    kernels = {nm: {"ms_per_launch": per_kernel[nm] / args.steps * 1e3} for nm in names}
+    kernels["fwd"]["tflops"] = ff / fwd_avg / 1e12
+    kernels["fwd"]["frac_of_peak"] = ff / fwd_avg / 1e12 / peak
+    kernels["bwd_main"]["tflops"] = achieved
+    bwd_total = (per_kernel["bwd_prep"] + per_kernel["bwd_main"] + per_kernel["bwd_convert"]) / args.steps
+    kernels["bwd_total"] = {"ms_per_call": bwd_total * 1e3, "tflops": bf / bwd_total / 1e12,
+                            "frac_of_peak": bf / bwd_total / 1e12 / peak}
+    hbm_bytes = 8.0 * B * H * N * d + 4.0 * B * H * N  # fwd: Q, K, V read, O written, lse
+    kernels["fwd"]["algorithmic_hbm_gbs"] = hbm_bytes / fwd_avg / 1e9
+
+    # ------------------------------------------------------- CPU baseline
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        val, dt, threads = cpu_sample(w, args.cpu_heads)
+        cpu = {"value": val, "unit": UNIT, "cores": threads, "kind": "oracle",
+               "sample": "fwd+bwd of %d of %d heads (N=%d, d=%d), fp64 oracle, %.1f s"
+                         % (args.cpu_heads, B * H, N, d, dt)}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": max_elapsed / args.steps * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": w["name"], "B": B, "H": H, "N": N, "d": d,
+                       "causal": causal, "scale": scale, "step": "fa_fwd + fa_bwd",
+                       "parallelism": "replicas x%d (independent batches per GPU)" % world,
+                       "l2": l2_note, "seed": args.seed},
+            "clocks": clocks, "e2e": e2e, "gpu_launches": launches_per_step * args.steps,
+            "roofline": roofline, "cpu_baseline": cpu, "kernels": kernels,
+        }
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--workload", default=WORKLOAD["name"],
+                    help="one of the synthetic workloads (default: the headline one)")
+    ap.add_argument("--shape", default=None,
+                    help="B,H,N,d,causal: a custom iid N(0,1) workload (small profiling cases)")
+    ap.add_argument("--cpu-heads", type=int, default=2,
+                    help="heads of the workload the cpu_baseline leg times (GPU arm)")
+    ap.add_argument("--ref-heads", type=int, default=1,
+                    help="heads of the workload per step of the reference arm")
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if world != args.gpus and world > 1:
+        print("warning: WORLD_SIZE=%d but --gpus %d" % (world, args.gpus), file=sys.stderr)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo")
+    if args.shape:
+        B, H, N, d, c = (int(x) for x in args.shape.split(","))
+        w = dict(name="custom_B%d_H%d_N%d_d%d_%s" % (B, H, N, d, "causal" if c else "full"),
+                 B=B, H=H, N=N, d=d, causal=bool(c))
+    else:
+        w = workload_dict(args.workload)
+    try:
+        if args.impl == "reference":
+            return run_reference(args, w, rank, world)
+        return run_gpu(args, w, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -98,6 +98,20 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
            int causal, float scale, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * fa_bwd split into its three kernels, for callers that want to time or
+ * overlap them: bit 0 of phase_mask runs the preparation (D_i, lse_i * log2 e,
+ * zeroing of the dQ accumulator), bit 1 the main recomputation kernel
+ * (dK, dV and the dQ accumulation), bit 2 the dQ conversion to bf16.
+ * fa_bwd(...) is fa_bwd_phases(..., 7).  Phases must run in order on one
+ * stream with the same workspace; arguments and errors as fa_bwd, plus
+ * FA_ERR_ARG for a mask outside 1..7.
+ */
+int fa_bwd_phases(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                  const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+                  int causal, float scale, void* workspace, size_t workspace_bytes, void* stream,
+                  int phase_mask);
+
+/*
  * Synchronises `stream`, then returns and clears the status word of the
  * current device: FA_OK, FA_ERR_TIMEOUT if a kernel gave up on a pipeline
  * wait since the last call, or FA_ERR_LAUNCH if the stream holds a CUDA

@@ -172,6 +172,15 @@ size_t fa_bwd_workspace_size(int B, int H, int N, int d) {
 int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
            const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d, int causal,
            float scale, void* workspace, size_t workspace_bytes, void* stream) {
+  return fa_bwd_phases(q, k, v, o, dout, lse, dq, dk, dv, B, H, N, d, causal, scale, workspace,
+                       workspace_bytes, stream, 7);
+}
+
+int fa_bwd_phases(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                  const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+                  int causal, float scale, void* workspace, size_t workspace_bytes, void* stream,
+                  int phase_mask) {
+  if (phase_mask < 1 || phase_mask > 7) return FA_ERR_ARG;
   if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv) return FA_ERR_ARG;
   if (causal != 0 && causal != 1) return FA_ERR_ARG;
   int rc = check_shape(B, H, N, d, scale);
@@ -208,7 +217,7 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
   p.causal = causal;
   p.scale = scale;
   p.scale_log2 = scale * 1.4426950408889634f;
-  return launch_bwd(tq, tk, tv, tdo, p, d, static_cast<cudaStream_t>(stream));
+  return launch_bwd(tq, tk, tv, tdo, p, d, static_cast<cudaStream_t>(stream), phase_mask);
 }
 
 int fa_device_status(void* stream, int* site) {

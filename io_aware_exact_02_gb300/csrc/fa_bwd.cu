@@ -484,10 +484,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
 
 template <int D>
 int launch_bwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                 const CUtensorMap& tdo, const BwdParams& p, cudaStream_t stream) {
+                 const CUtensorMap& tdo, const BwdParams& p, cudaStream_t stream, int mask) {
   const long long npad = (long long)p.n_kv * kTile;
   // 1. prep: one warp per (32 / (D/8)) rows.
-  {
+  if (mask & 1) {
     const long long rows = (long long)p.BH * npad;
     const long long warps = (rows + (32 / (D / 8)) - 1) / (32 / (D / 8));
     const long long blocks = (warps * 32 + 255) / 256;
@@ -495,7 +495,7 @@ int launch_bwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap
     if (cudaGetLastError() != cudaSuccess) return FA_ERR_LAUNCH;
   }
   // 2. main
-  {
+  if (mask & 2) {
     const size_t smem = sizeof(BwdSmem<D>);
     if (cudaFuncSetAttribute(fa_bwd_main_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem) != cudaSuccess)
@@ -505,7 +505,7 @@ int launch_bwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap
     if (cudaGetLastError() != cudaSuccess) return FA_ERR_LAUNCH;
   }
   // 3. convert
-  {
+  if (mask & 4) {
     const long long total = (long long)p.BH * p.N * (D / 8);
     fa_bwd_convert_kernel<D><<<(unsigned)((total + 255) / 256), 256, 0, stream>>>(p);
     if (cudaGetLastError() != cudaSuccess) return FA_ERR_LAUNCH;
@@ -516,9 +516,10 @@ int launch_bwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap
 }  // namespace
 
 int launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-               const CUtensorMap& tdo, const BwdParams& p, int d, cudaStream_t stream) {
-  if (d == 128) return launch_bwd_d<128>(tq, tk, tv, tdo, p, stream);
-  if (d == 64) return launch_bwd_d<64>(tq, tk, tv, tdo, p, stream);
+               const CUtensorMap& tdo, const BwdParams& p, int d, cudaStream_t stream,
+               int phase_mask) {
+  if (d == 128) return launch_bwd_d<128>(tq, tk, tv, tdo, p, stream, phase_mask);
+  if (d == 64) return launch_bwd_d<64>(tq, tk, tv, tdo, p, stream, phase_mask);
   return FA_ERR_UNSUPPORTED_D;
 }
 

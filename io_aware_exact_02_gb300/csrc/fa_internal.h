@@ -90,7 +90,9 @@ inline BwdWorkspace bwd_workspace_layout(long long BH, int N, int d) {
   return w;
 }
 
+// phase_mask: bit 0 prep, bit 1 main, bit 2 convert.
 int launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-               const CUtensorMap& tdo, const BwdParams& p, int d, cudaStream_t stream);
+               const CUtensorMap& tdo, const BwdParams& p, int d, cudaStream_t stream,
+               int phase_mask);
 
 }  // namespace fa

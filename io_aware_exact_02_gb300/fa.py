@@ -38,6 +38,8 @@ SIGNATURES = {
     "fa_bwd_workspace_size": (_sz, [_i, _i, _i, _i]),
     "fa_bwd": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f,
                     _vp, _sz, _vp]),
+    "fa_bwd_phases": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f,
+                           _vp, _sz, _vp, _i]),
     "fa_device_status": (_i, [_vp, _ip]),
     "fa_status_string": (ctypes.c_char_p, [_i]),
     "fa_fwd_schedule": (_i, [_i, _i, _i, _i, _ip, _ip, _ip, _i]),
@@ -126,8 +128,12 @@ def bwd_workspace_size(B: int, H: int, N: int, d: int) -> int:
 
 
 def bwd(q, k, v, o, dout, lse, causal: bool = False, scale: float | None = None,
-        dq=None, dk=None, dv=None, workspace=None):
-    """dq, dk, dv of L = sum(dout * O).  Returns (dq, dk, dv)."""
+        dq=None, dk=None, dv=None, workspace=None, phases: int = 7):
+    """dq, dk, dv of L = sum(dout * O).  Returns (dq, dk, dv).
+
+    ``phases`` selects the backward kernels to run (bit 0 prep, bit 1 main,
+    bit 2 dQ convert); the default runs all three, as fa_bwd does.
+    """
     B, H, N, d = q.shape
     scale = default_scale(d) if scale is None else float(scale)
     for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("dout", dout)):
@@ -142,11 +148,13 @@ def bwd(q, k, v, o, dout, lse, causal: bool = False, scale: float | None = None,
     if workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     nbytes = workspace.numel() * workspace.element_size()
-    rc = load().fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(),
-                       lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, N, d,
-                       int(bool(causal)), ctypes.c_float(scale), workspace.data_ptr(), nbytes,
-                       _stream_of(q))
-    _check("fa_bwd", rc)
+    args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(),
+            lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, N, d,
+            int(bool(causal)), ctypes.c_float(scale), workspace.data_ptr(), nbytes, _stream_of(q))
+    if phases == 7:
+        _check("fa_bwd", load().fa_bwd(*args))
+    else:
+        _check("fa_bwd_phases", load().fa_bwd_phases(*args, int(phases)))
     return dq, dk, dv
 
 
