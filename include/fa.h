@@ -112,6 +112,34 @@ int fa_bwd_phases(const void* q, const void* k, const void* v, const void* o, co
                   int phase_mask);
 
 /*
+ * Size of the scratch array fa_bwd_noalloc uses: 32 MiB of static device
+ * data on every GPU that loads the library, held until the process exits.
+ */
+#define FA_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
+
+/*
+ * fa_bwd for callers that cannot allocate device memory.  The pages have no
+ * counterpart: this is a deployment variant of fa_bwd, not part of the method.
+ * Callers under a memory manager that owns all device memory, callers that
+ * cannot afford cudaMalloc's implicit device-wide synchronisation, and
+ * plugins given no allocator cannot provide fa_bwd's workspace; this entry
+ * point takes it from a fixed scratch array in the library's static device
+ * data instead and allocates nothing.
+ *   Arguments, layouts and results as fa_bwd, without the workspace.
+ *   Returns FA_ERR_WORKSPACE, launching nothing, when
+ *   fa_bwd_workspace_size(B, H, N, d) > FA_NOALLOC_SCRATCH_BYTES (for
+ *   d = 128 about 64K padded rows B*H*ceil(N/128)*128; for d = 64 about 127K).
+ *   The first call on a device looks up the scratch array's device address
+ *   (cudaGetSymbolAddress, with that device current); make that first call
+ *   before any stream capture.  All calls on a device share the one array
+ *   and it keeps the previous call's contents (every part that is read is
+ *   rewritten first): calls that overlap on the GPU race on it.
+ */
+int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                   const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+                   int causal, float scale, void* stream);
+
+/*
  * Synchronises `stream`, then returns and clears the status word of the
  * current device: FA_OK, FA_ERR_TIMEOUT if a kernel gave up on a pipeline
  * wait since the last call, or FA_ERR_LAUNCH if the stream holds a CUDA

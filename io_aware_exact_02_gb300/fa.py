@@ -40,6 +40,8 @@ SIGNATURES = {
                     _vp, _sz, _vp]),
     "fa_bwd_phases": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f,
                            _vp, _sz, _vp, _i]),
+    "fa_bwd_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f,
+                            _vp]),
     "fa_device_status": (_i, [_vp, _ip]),
     "fa_status_string": (ctypes.c_char_p, [_i]),
     "fa_fwd_schedule": (_i, [_i, _i, _i, _i, _ip, _ip, _ip, _i]),
@@ -155,6 +157,29 @@ def bwd(q, k, v, o, dout, lse, causal: bool = False, scale: float | None = None,
         _check("fa_bwd", load().fa_bwd(*args))
     else:
         _check("fa_bwd_phases", load().fa_bwd_phases(*args, int(phases)))
+    return dq, dk, dv
+
+
+def bwd_noalloc(q, k, v, o, dout, lse, causal: bool = False, scale: float | None = None,
+                dq=None, dk=None, dv=None):
+    """fa_bwd without a caller workspace: the library's fixed scratch array is
+    used instead (for callers that cannot allocate device memory).  Calls
+    that overlap on the GPU race on that array.  Returns (dq, dk, dv)."""
+    B, H, N, d = q.shape
+    scale = default_scale(d) if scale is None else float(scale)
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("dout", dout)):
+        _check_qkv(name, t, (B, H, N, d))
+    _check_qkv("lse", lse, (B, H, N), torch.float32)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(q) if dk is None else dk
+    dv = torch.empty_like(q) if dv is None else dv
+    for name, t in (("dq", dq), ("dk", dk), ("dv", dv)):
+        _check_qkv(name, t, (B, H, N, d))
+    rc = load().fa_bwd_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                               dout.data_ptr(), lse.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                               dv.data_ptr(), B, H, N, d, int(bool(causal)),
+                               ctypes.c_float(scale), _stream_of(q))
+    _check("fa_bwd_noalloc", rc)
     return dq, dk, dv
 
 
