@@ -177,7 +177,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
 
       auto issue_s = [&](int t, int kslot) {
         const uint32_t kb = smem_u32(sm.kv[kslot]);
-#pragma unroll
+#pragma unroll 1
         for (int kk = 0; kk < Cfg::kKSteps; ++kk)
           mma_ss(tmem + Cfg::col_s(t), kmajor_desc(q_addr[t], kk), kmajor_desc(kb, kk), id_s,
                  kk > 0);
@@ -185,7 +185,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
       };
       auto issue_pv = [&](int t, int vslot, bool accumulate) {
         const uint32_t vb = smem_u32(sm.kv[vslot]);
-#pragma unroll
+#pragma unroll 1
         for (int kk = 0; kk < kTile / 16; ++kk)
           mma_ts(tmem + Cfg::col_o(t), tmem + Cfg::col_s(t) + kk * 8, mnmajor_desc(vb, kk), id_pv,
                  (accumulate || kk > 0) ? 1u : 0u);
@@ -251,7 +251,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
       drain_wait(&sm.drain, 0);
     }
     __syncwarp();
-  } else {
+  } else if (warp < 8) {
     // ------------------------------------------------------------ softmax
     const int t = warp >> 2;             // which Q tile
     const int r = tid & 127;             // row within the tile
@@ -291,20 +291,34 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
             if (col >= p.N || (p.causal && col > R)) sr[c][i] = __float_as_uint(neutral);
           }
       }
-      // Tile extreme of the raw scores (max for scale >= 0, min otherwise).
-      float mx = __uint_as_float(sr[0][0]);
+      // Tile extreme of the raw scores (max for scale >= 0, min otherwise),
+      // as eight independent chains joined by a tree (max/min are exact, so
+      // the order does not change the result).
+      float mx8[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) mx8[u] = neutral;
       if (!neg) {
 #pragma unroll
         for (int c = 0; c < 4; ++c)
 #pragma unroll
-          for (int i = 0; i < 32; ++i) mx = fmaxf(mx, __uint_as_float(sr[c][i]));
+          for (int i = 0; i < 32; ++i)
+            mx8[i & 7] = fmaxf(mx8[i & 7], __uint_as_float(sr[c][i]));
+#pragma unroll
+        for (int w = 4; w > 0; w >>= 1)
+#pragma unroll
+          for (int u = 0; u < w; ++u) mx8[u] = fmaxf(mx8[u], mx8[u + w]);
       } else {
 #pragma unroll
         for (int c = 0; c < 4; ++c)
 #pragma unroll
-          for (int i = 0; i < 32; ++i) mx = fminf(mx, __uint_as_float(sr[c][i]));
+          for (int i = 0; i < 32; ++i)
+            mx8[i & 7] = fminf(mx8[i & 7], __uint_as_float(sr[c][i]));
+#pragma unroll
+        for (int w = 4; w > 0; w >>= 1)
+#pragma unroll
+          for (int u = 0; u < w; ++u) mx8[u] = fminf(mx8[u], mx8[u + w]);
       }
-      const float m_tile = mx * c2;
+      const float m_tile = mx8[0] * c2;
       float alpha = 1.f;
       if (m_tile > m_ref + kRescaleSlack) {
         alpha = ex2_approx(m_ref - m_tile);  // 0 on the first tile (m_ref = -inf)
@@ -312,7 +326,9 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
       }
       l *= alpha;
       const float neg_m = -m_ref;
-      float lsum = 0.f;
+      float ls8[8];  // eight partial row sums, joined by a tree below
+#pragma unroll
+      for (int u = 0; u < 8; ++u) ls8[u] = 0.f;
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         uint32_t pk[32];
@@ -328,13 +344,17 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
               if (col >= p.N || (p.causal && col > R)) p0 = 0.f;
               if (col + 1 >= p.N || (p.causal && col + 1 > R)) p1 = 0.f;
             }
-            lsum += p0 + p1;
+            ls8[(i >> 1) & 7] += p0 + p1;
             pk[c2i * 16 + i / 2] = pack_bf16x2(p0, p1);
           }
         }
         tmem_st32(colS + h * 32, pk);
       }
-      l += lsum;
+#pragma unroll
+      for (int w = 4; w > 0; w >>= 1)
+#pragma unroll
+        for (int u = 0; u < w; ++u) ls8[u] += ls8[u + w];
+      l += ls8[0];
       tmem_wait_st();
       // Correct the O accumulator if this row's reference moved (warp-wide
       // decision: TMEM loads/stores are warp-collective).
