@@ -90,7 +90,9 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
   }
 }
 
-template <int D>
+// kNeg: the scale is negative, so the tile's extreme is a minimum of the raw
+// scores (the exponent scale * s is largest where s is smallest).
+template <int D, bool kNeg>
 __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, const FwdParams p) {
@@ -258,9 +260,10 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const int n_t = t == 0 ? n_t0 : n_t1;
     const int R = row0 + t * kTile + r;  // global query row
-    const float c2 = p.scale_log2;
-    const bool neg = c2 < 0.f;
-    const float neutral = neg ? __int_as_float(0x7f800000) : __int_as_float(0xff800000);
+    const float c2 = p.scale_log2;  // nonzero: a zero scale arrives as a tiny positive one
+    // A masked score is replaced by the value that loses every max (min)
+    // and whose exponent c2 * s is -inf, so its probability is exactly 0.
+    const float neutral = kNeg ? __int_as_float(0x7f800000) : __int_as_float(0xff800000);
     const uint32_t colS = tmem + lane_base + Cfg::col_s(t);
     const uint32_t colO = tmem + lane_base + Cfg::col_o(t);
     const int diag_tile = p.causal ? (row0 + t * kTile) / kTile : -1;
@@ -283,41 +286,31 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
 
       const bool need_mask = (j + 1) * kTile > p.N || j == diag_tile;
       if (need_mask) {
+        // Keys at columns >= lim of this tile are masked for this row.
+        int lim = p.N - j * kTile;
+        if (p.causal && R + 1 - j * kTile < lim) lim = R + 1 - j * kTile;
 #pragma unroll
         for (int c = 0; c < 4; ++c)
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const int col = j * kTile + c * 32 + i;
-            if (col >= p.N || (p.causal && col > R)) sr[c][i] = __float_as_uint(neutral);
-          }
+          for (int i = 0; i < 32; ++i)
+            if (c * 32 + i >= lim) sr[c][i] = __float_as_uint(neutral);
       }
-      // Tile extreme of the raw scores (max for scale >= 0, min otherwise),
-      // as eight independent chains joined by a tree (max/min are exact, so
-      // the order does not change the result).
+      // Tile extreme of the raw scores, as eight independent chains joined
+      // by a tree (max/min are exact, so the order does not change it).
       float mx8[8];
 #pragma unroll
       for (int u = 0; u < 8; ++u) mx8[u] = neutral;
-      if (!neg) {
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
+      for (int c = 0; c < 4; ++c)
 #pragma unroll
-          for (int i = 0; i < 32; ++i)
-            mx8[i & 7] = fmaxf(mx8[i & 7], __uint_as_float(sr[c][i]));
+        for (int i = 0; i < 32; ++i)
+          mx8[i & 7] = kNeg ? fminf(mx8[i & 7], __uint_as_float(sr[c][i]))
+                            : fmaxf(mx8[i & 7], __uint_as_float(sr[c][i]));
 #pragma unroll
-        for (int w = 4; w > 0; w >>= 1)
+      for (int w = 4; w > 0; w >>= 1)
 #pragma unroll
-          for (int u = 0; u < w; ++u) mx8[u] = fmaxf(mx8[u], mx8[u + w]);
-      } else {
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-#pragma unroll
-          for (int i = 0; i < 32; ++i)
-            mx8[i & 7] = fminf(mx8[i & 7], __uint_as_float(sr[c][i]));
-#pragma unroll
-        for (int w = 4; w > 0; w >>= 1)
-#pragma unroll
-          for (int u = 0; u < w; ++u) mx8[u] = fminf(mx8[u], mx8[u + w]);
-      }
+        for (int u = 0; u < w; ++u)
+          mx8[u] = kNeg ? fminf(mx8[u], mx8[u + w]) : fmaxf(mx8[u], mx8[u + w]);
       const float m_tile = mx8[0] * c2;
       float alpha = 1.f;
       if (m_tile > m_ref + kRescaleSlack) {
@@ -337,13 +330,8 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
           const int c = 2 * h + c2i;
 #pragma unroll
           for (int i = 0; i < 32; i += 2) {
-            float p0 = ex2_approx(fmaf(__uint_as_float(sr[c][i]), c2, neg_m));
-            float p1 = ex2_approx(fmaf(__uint_as_float(sr[c][i + 1]), c2, neg_m));
-            if (need_mask) {
-              const int col = j * kTile + c * 32 + i;
-              if (col >= p.N || (p.causal && col > R)) p0 = 0.f;
-              if (col + 1 >= p.N || (p.causal && col + 1 > R)) p1 = 0.f;
-            }
+            const float p0 = ex2_approx(fmaf(__uint_as_float(sr[c][i]), c2, neg_m));
+            const float p1 = ex2_approx(fmaf(__uint_as_float(sr[c][i + 1]), c2, neg_m));
             ls8[(i >> 1) & 7] += p0 + p1;
             pk[c2i * 16 + i / 2] = pack_bf16x2(p0, p1);
           }
@@ -408,16 +396,26 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
   }
 }
 
-template <int D>
-int launch_fwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                 const FwdParams& p, cudaStream_t stream) {
+template <int D, bool kNeg>
+int launch_fwd_dn(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                  const FwdParams& p, cudaStream_t stream) {
   const size_t smem = sizeof(FwdSmem<D>) + 1024;
-  if (cudaFuncSetAttribute(fa_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (cudaFuncSetAttribute(fa_fwd_kernel<D, kNeg>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)smem) != cudaSuccess)
     return FA_ERR_LAUNCH;
   const unsigned grid = (unsigned)p.BH * (unsigned)p.n_pairs;
-  fa_fwd_kernel<D><<<grid, FwdCfg<D>::kThreads, smem, stream>>>(tq, tk, tv, p);
+  fa_fwd_kernel<D, kNeg><<<grid, FwdCfg<D>::kThreads, smem, stream>>>(tq, tk, tv, p);
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+}
+
+template <int D>
+int launch_fwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                 FwdParams p, cudaStream_t stream) {
+  // A zero scale makes every unmasked probability equal; it runs as the
+  // smallest normal positive scale, whose exponents round to exactly 0.
+  if (p.scale_log2 == 0.f) p.scale_log2 = 1.17549435e-38f;
+  if (p.scale_log2 < 0.f) return launch_fwd_dn<D, true>(tq, tk, tv, p, stream);
+  return launch_fwd_dn<D, false>(tq, tk, tv, p, stream);
 }
 
 }  // namespace
