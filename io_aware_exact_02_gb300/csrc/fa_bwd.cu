@@ -19,19 +19,24 @@
 //        S^T  = K_j Q_i^T           (tcgen05, both operands in smem)
 //        dP^T = V_j dO_i^T
 //        P^T  = exp2(S^T c - lse_i log2 e)  -> bf16 in TMEM over S^T
+//               (masked scores replaced by the value whose exponent is -inf)
 //        dV  += P^T dO_i                    (A operand from TMEM)
 //        dS^T = P^T o (dP^T - D_i)          -> bf16 in smem (128B swizzle)
 //        dK  += dS^T Q_i
 //        dQ_i = dS K_j  -> TMEM (over dP^T) -> fp32 vector atomics into the
-//                          workspace, by a dedicated warpgroup
+//                          workspace, by the compute warpgroups
 //   3. convert: dQ = bf16(scale * accumulator).
 //
-// Warp roles of the main kernel (384 threads):
-//   warps 0-3  compute (thread r owns key row r of the tile): P, dS, epilogue
-//   warps 4-7  dQ drain: TMEM -> registers -> atomic adds
+// Warp roles of the main kernel (320 threads):
+//   warps 0-7  compute: two warpgroups, each owning 64 of the 128 query
+//              columns (thread r owns key row r of the tile): P, dS, then
+//              half of dQ_i's columns from TMEM to the fp32 accumulator with
+//              atomic adds; finally the dV (warpgroup 0) / dK (warpgroup 1)
+//              epilogue
 //   warp 8     TMA producer;  warp 9 MMA issuer and TMEM owner
-// Tensor memory: [0,128) S^T / P^T, [128,256) dP^T / dQ, [256,256+d) dV,
-// [256+d, 256+2d) dK.
+// Tensor memory: [0,128) S^T, with P^T (bf16 pairs) over columns 0-31
+// (queries 0-63) and 64-95 (queries 64-127); [128,256) dP^T, then dQ;
+// [256,256+d) dV; [256+d, 256+2d) dK.
 #include "fa_internal.h"
 #include "sm100_ptx.cuh"
 
@@ -44,7 +49,7 @@ template <int D>
 struct BwdCfg {
   static constexpr int kTileBytes = kTile * D * 2;  // one 128 x d bf16 tile
   static constexpr int kStages = 2;                  // Q/dO ring
-  static constexpr int kThreads = 384;
+  static constexpr int kThreads = 320;  // 2 compute warpgroups, producer, MMA
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D;
 };
@@ -65,6 +70,8 @@ struct BwdSmem {
   uint32_t tmem_base;
   int abort_flag;
 };
+
+constexpr int kWarpLoad = 8, kWarpMma = 9;
 
 enum : int {
   kSiteKvFull = 201, kSiteQFull, kSiteQEmpty, kSiteSFull, kSiteDpFull, kSitePReady,
@@ -219,16 +226,16 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     }
     mbar_init(&sm.s_full, 1);
     mbar_init(&sm.dp_full, 1);
-    mbar_init(&sm.p_ready, 128);
-    mbar_init(&sm.ds_ready, 128);
+    mbar_init(&sm.p_ready, 256);
+    mbar_init(&sm.ds_ready, 256);
     mbar_init(&sm.dq_full, 1);
-    mbar_init(&sm.dq_empty, 128);
+    mbar_init(&sm.dq_empty, 256);
     mbar_init(&sm.acc_full, 1);
     mbar_init(&sm.drain, 1);
     sm.abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 9) {
+  if (warp == kWarpMma) {
     tmem_alloc(&sm.tmem_base, Cfg::kTmemCols);
     tmem_relinquish();
   }
@@ -243,7 +250,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
   const int n_iter = p.n_kv - i0;
   const int npad = p.n_kv * kTile;
 
-  if (warp == 8) {
+  if (warp == kWarpLoad) {
     // ------------------------------------------------------------ producer
     if (lane_id() == 0) {
       prefetch_tmap(&tq);
@@ -275,7 +282,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       }
     }
     __syncwarp();
-  } else if (warp == 9) {
+  } else if (warp == kWarpMma) {
     // ------------------------------------------------------------ MMA issuer
     if (lane_id() == 0) {
       const uint32_t id_s = idesc_bf16(128, 128, false, false);   // S^T, dP^T
@@ -291,7 +298,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         if (!ok) break;
         tc_fence_after();
         // S^T = K_j Q_i^T
-#pragma unroll
+#pragma unroll 1
         for (int kk = 0; kk < D / 16; ++kk)
           mma_ss(tmem + Cfg::kColS, kmajor_desc(kb, kk), kmajor_desc(qb, kk), id_s, kk > 0);
         tc_commit(&sm.s_full);
@@ -301,28 +308,29 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
           if (!ok) break;
           tc_fence_after();
         }
-#pragma unroll
+#pragma unroll 1
         for (int kk = 0; kk < D / 16; ++kk)
           mma_ss(tmem + Cfg::kColDP, kmajor_desc(vb, kk), kmajor_desc(dob, kk), id_s, kk > 0);
         tc_commit(&sm.dp_full);
-        // dV += P^T dO_i
+        // dV += P^T dO_i.  P^T for query columns 0-63 sits in TMEM columns
+        // 0-31, for query columns 64-127 in columns 64-95 (bf16 pairs).
         ok = mbar_wait(&sm.p_ready, par, p.status, abortf, kSitePReady);
         if (!ok) break;
         tc_fence_after();
-#pragma unroll
+#pragma unroll 1
         for (int kk = 0; kk < kTile / 16; ++kk)
-          mma_ts(tmem + Cfg::kColDV, tmem + Cfg::kColS + kk * 8, mnmajor_desc(dob, kk), id_acc,
-                 (it > 0 || kk > 0) ? 1u : 0u);
+          mma_ts(tmem + Cfg::kColDV, tmem + Cfg::kColS + (kk >> 2) * 64 + (kk & 3) * 8,
+                 mnmajor_desc(dob, kk), id_acc, (it > 0 || kk > 0) ? 1u : 0u);
         // dK += dS^T Q_i ; dQ_i = dS K_j
         ok = mbar_wait(&sm.ds_ready, par, p.status, abortf, kSiteDsReady);
         if (!ok) break;
         tc_fence_after();
-#pragma unroll
+#pragma unroll 1
         for (int kk = 0; kk < kTile / 16; ++kk)
           mma_ss(tmem + Cfg::kColDK, kmajor_desc(dsb, kk), mnmajor_desc(qb, kk), id_acc,
                  (it > 0 || kk > 0) ? 1u : 0u);
         tc_commit(&sm.q_empty[s]);
-#pragma unroll
+#pragma unroll 1
         for (int kk = 0; kk < kTile / 16; ++kk)
           mma_ss(tmem + Cfg::kColDP, mnmajor_desc(dsb, kk), mnmajor_desc(kb, kk), id_dq, kk > 0);
         tc_commit(&sm.dq_full);
@@ -332,52 +340,55 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       drain_wait(&sm.drain, 0);
     }
     __syncwarp();
-  } else if (warp < 4) {
+  } else if (warp < 8) {
     // ------------------------------------------------------------ compute
-    const int r = tid;  // key row within the tile
+    // Warpgroup g handles query columns [64g, 64g + 64) of the tile; thread
+    // r of either warpgroup owns key row r (TMEM lane r).
+    const int g = warp >> 2;
+    const int r = tid & 127;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-    const uint32_t colS = tmem + lane_base + Cfg::kColS;
-    const uint32_t colDP = tmem + lane_base + Cfg::kColDP;
-    const float c2 = p.scale_log2;
+    const uint32_t colS = tmem + lane_base + Cfg::kColS + g * 64;
+    const uint32_t colDP = tmem + lane_base + Cfg::kColDP + g * 64;
+    const uint32_t colDQ = tmem + lane_base + Cfg::kColDP + g * (D / 2);
+    const float c2 = p.scale_log2;  // nonzero: a zero scale arrives as a tiny positive one
+    // A masked score is replaced by the value whose exponent c2 * s is -inf.
+    const float neutral = c2 < 0.f ? __int_as_float(0x7f800000) : __int_as_float(0xff800000);
     const int kv_row = j * kTile + r;
     bool ok = true;
     for (int it = 0; it < n_iter; ++it) {
       const int s = it % NS;
       const uint32_t par = it & 1;
       const int i = i0 + it;
-      const bool diag = p.causal && i == j;
       ok = mbar_wait(&sm.q_full[s], (it / NS) & 1, p.status, abortf, kSiteQFull);
       if (ok) ok = mbar_wait(&sm.s_full, par, p.status, abortf, kSiteSFull);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
-      const float* lse2 = sm.lse2[s];
-      uint32_t pk[64];  // P^T row, bf16 pairs
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        uint32_t sr[2][32];
-        tmem_ld32(colS + h * 64, sr[0]);
-        tmem_ld32(colS + h * 64 + 32, sr[1]);
-        tmem_wait_ld(sr[0]);
-        tmem_wait_ld(sr[1]);
+      uint32_t sr[2][32];
+      tmem_ld32(colS, sr[0]);
+      tmem_ld32(colS + 32, sr[1]);
+      tmem_wait_ld(sr[0]);
+      tmem_wait_ld(sr[1]);
+      if (p.causal && i == j) {
+        // Diagonal tile: key row r is masked for query columns < r.
 #pragma unroll
         for (int c = 0; c < 2; ++c)
 #pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            const int col = h * 64 + c * 32 + e;  // query column within the tile
-            float p0 = ex2_approx(fmaf(__uint_as_float(sr[c][e]), c2, -lse2[col]));
-            float p1 = ex2_approx(fmaf(__uint_as_float(sr[c][e + 1]), c2, -lse2[col + 1]));
-            if (diag) {
-              if (r > col) p0 = 0.f;
-              if (r > col + 1) p1 = 0.f;
-            }
-            pk[h * 32 + c * 16 + e / 2] = pack_bf16x2(p0, p1);
-          }
-        uint32_t st[32];
-#pragma unroll
-        for (int e = 0; e < 32; ++e) st[e] = pk[h * 32 + e];
-        tmem_st32(colS + h * 32, st);
+          for (int e = 0; e < 32; ++e)
+            if (r > g * 64 + c * 32 + e) sr[c][e] = __float_as_uint(neutral);
       }
+      const float* lse2 = sm.lse2[s] + g * 64;
+      uint32_t pk[32];  // P^T for this warpgroup's 64 query columns, bf16 pairs
+#pragma unroll
+      for (int c = 0; c < 2; ++c)
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          const float p0 = ex2_approx(fmaf(__uint_as_float(sr[c][e]), c2, -lse2[c * 32 + e]));
+          const float p1 = ex2_approx(fmaf(__uint_as_float(sr[c][e + 1]), c2, -lse2[c * 32 + e + 1]));
+          pk[c * 16 + e / 2] = pack_bf16x2(p0, p1);
+        }
+      // Over the first 32 of this warpgroup's own S columns (already read).
+      tmem_st32(colS, pk);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&sm.p_ready);
@@ -386,97 +397,90 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
-      const float* dl = sm.delta[s];
-      uint8_t* ds_row = sm.ds + r * 128;  // row r of both 64-column blocks
+      uint32_t dp[2][32];
+      tmem_ld32(colDP, dp[0]);
+      tmem_ld32(colDP + 32, dp[1]);
+      tmem_wait_ld(dp[0]);
+      tmem_wait_ld(dp[1]);
+      const float* dl = sm.delta[s] + g * 64;
+      // dS^T row r, query columns [64g, 64g+64) = column block g of the
+      // 128B-swizzled [key][query] tile: eight 16-byte chunks.
+      uint8_t* ds_row = sm.ds + g * 16384 + r * 128;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t dp[32];
-        tmem_ld32(colDP + c * 32, dp);
-        tmem_wait_ld(dp);
-        uint32_t w[16];
+      for (int ch = 0; ch < 8; ++ch) {
+        uint32_t w[4];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const int col = c * 32 + 2 * e;
+        for (int e = 0; e < 4; ++e) {
+          const int col = ch * 8 + 2 * e;  // 0..63 within this warpgroup's columns
           const float2 pf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pk[col / 2]));
-          const float d0 = pf.x * (__uint_as_float(dp[2 * e]) - dl[col]);
-          const float d1 = pf.y * (__uint_as_float(dp[2 * e + 1]) - dl[col + 1]);
+          const float d0 = pf.x * (__uint_as_float(dp[col >> 5][col & 31]) - dl[col]);
+          const float d1 = pf.y * (__uint_as_float(dp[(col + 1) >> 5][(col + 1) & 31]) - dl[col + 1]);
           w[e] = pack_bf16x2(d0, d1);
         }
-        // 32 bf16 = four 16-byte chunks of the 128B-swizzled row.
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          const int chunk = c * 4 + q4;       // 0..15 over the 128 columns
-          const int blk = chunk >> 3, ch = chunk & 7;
-          *reinterpret_cast<uint4*>(ds_row + blk * 16384 + ((ch ^ (r & 7)) << 4)) =
-              make_uint4(w[4 * q4], w[4 * q4 + 1], w[4 * q4 + 2], w[4 * q4 + 3]);
-        }
+        *reinterpret_cast<uint4*>(ds_row + ((ch ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
       }
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(&sm.ds_ready);
+
+      // dQ_i drain: TMEM lane r is query row r of dQ_i; warpgroup g reads
+      // its D/2 columns, releases the TMEM (the next dP^T reuses it) and adds
+      // them to the fp32 accumulator while the tensor core computes the next
+      // S^T.
+      ok = mbar_wait(&sm.dq_full, par, p.status, abortf, kSiteDqFull);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      {
+        uint32_t a[D / 64][32];
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c) tmem_ld32(colDQ + c * 32, a[c]);
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c) tmem_wait_ld(a[c]);
+        tc_fence_before();
+        mbar_arrive(&sm.dq_empty);
+        float* base = p.dq_acc + dqacc_index<D>(bh, p.n_kv, i * kTile + r, g * (D / 8));
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c)
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const float4 val = make_float4(__uint_as_float(a[c][4 * e]), __uint_as_float(a[c][4 * e + 1]),
+                                           __uint_as_float(a[c][4 * e + 2]), __uint_as_float(a[c][4 * e + 3]));
+            atomicAdd(reinterpret_cast<float4*>(base + (size_t)(c * 8 + e) * kTile * 4), val);
+          }
+      }
     }
-    // Epilogue: dV and scale * dK of this key row.
+    // Epilogue: warpgroup 0 stores dV, warpgroup 1 stores scale * dK.
     if (ok) ok = mbar_wait(&sm.acc_full, 0, p.status, abortf, kSiteAccFull);
     ok = __all_sync(0xffffffffu, ok);
     if (ok) {
       tc_fence_after();
+      const uint32_t col = tmem + lane_base + (g == 0 ? Cfg::kColDV : Cfg::kColDK);
+      const float mul = g == 0 ? 1.f : p.scale;
+      __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(g == 0 ? p.dv : p.dk) +
+                           ((size_t)bh * p.N + kv_row) * D;
 #pragma unroll
-      for (int which = 0; which < 2; ++which) {
-        const uint32_t col = tmem + lane_base + (which == 0 ? Cfg::kColDV : Cfg::kColDK);
-        const float mul = which == 0 ? 1.f : p.scale;
-        __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(which == 0 ? p.dv : p.dk) +
-                             ((size_t)bh * p.N + kv_row) * D;
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t a[32];
+        tmem_ld32(col + c * 32, a);
+        tmem_wait_ld(a);
+        if (kv_row < p.N) {
+          uint4 v[4];
+          uint32_t* w = reinterpret_cast<uint32_t*>(v);
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t a[32];
-          tmem_ld32(col + c * 32, a);
-          tmem_wait_ld(a);
-          if (kv_row < p.N) {
-            uint4 v[4];
-            uint32_t* w = reinterpret_cast<uint32_t*>(v);
+          for (int e = 0; e < 16; ++e)
+            w[e] = pack_bf16x2(__uint_as_float(a[2 * e]) * mul, __uint_as_float(a[2 * e + 1]) * mul);
+          uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
 #pragma unroll
-            for (int e = 0; e < 16; ++e)
-              w[e] = pack_bf16x2(__uint_as_float(a[2 * e]) * mul, __uint_as_float(a[2 * e + 1]) * mul);
-            uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) d4[e] = v[e];
-          }
+          for (int e = 0; e < 4; ++e) d4[e] = v[e];
         }
       }
-    }
-  } else if (warp < 8) {
-    // ------------------------------------------------------------ dQ drain
-    const int r = tid - 128;  // query row within the tile
-    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-    const uint32_t colDQ = tmem + lane_base + Cfg::kColDP;
-    for (int it = 0; it < n_iter; ++it) {
-      bool ok = mbar_wait(&sm.dq_full, it & 1, p.status, abortf, kSiteDqFull);
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) break;
-      tc_fence_after();
-      uint32_t a[D / 32][32];
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) tmem_ld32(colDQ + c * 32, a[c]);
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) tmem_wait_ld(a[c]);
-      tc_fence_before();
-      mbar_arrive(&sm.dq_empty);
-      const int row = (i0 + it) * kTile + r;
-      float* base = p.dq_acc + dqacc_index<D>(bh, p.n_kv, row, 0);
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c)
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const float4 val = make_float4(__uint_as_float(a[c][4 * e]), __uint_as_float(a[c][4 * e + 1]),
-                                         __uint_as_float(a[c][4 * e + 2]), __uint_as_float(a[c][4 * e + 3]));
-          atomicAdd(reinterpret_cast<float4*>(base + (size_t)(c * 8 + e) * kTile * 4), val);
-        }
     }
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == kWarpMma) {
     tc_fence_after();
     tmem_dealloc(tmem, Cfg::kTmemCols);
   }
@@ -484,7 +488,11 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
 
 template <int D>
 int launch_bwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                 const CUtensorMap& tdo, const BwdParams& p, cudaStream_t stream, int mask) {
+                 const CUtensorMap& tdo, BwdParams p, cudaStream_t stream, int mask) {
+  // As in the forward pass, a zero scale runs its exponents with the smallest
+  // normal positive scale (they round to exactly the same values); dQ and dK
+  // are still multiplied by the exact scale.
+  if (p.scale_log2 == 0.f) p.scale_log2 = 1.17549435e-38f;
   const long long npad = (long long)p.n_kv * kTile;
   // 1. prep: one warp per (32 / (D/8)) rows.
   if (mask & 1) {
