@@ -22,7 +22,7 @@
 //               (masked scores replaced by the value whose exponent is -inf)
 //        dV  += P^T dO_i                    (A operand from TMEM)
 //        dS^T = P^T o (dP^T - D_i)          -> bf16 in smem (128B swizzle)
-//        dK  += dS^T Q_i
+//        dK  += dS^T Q_i                   (A operand from TMEM)
 //        dQ_i = dS K_j  -> TMEM (over dP^T) -> fp32 vector atomics into the
 //                          workspace, by the compute warpgroups
 //   3. convert: dQ = bf16(scale * accumulator).
@@ -35,8 +35,9 @@
 //              epilogue
 //   warp 8     TMA producer;  warp 9 MMA issuer and TMEM owner
 // Tensor memory: [0,128) S^T, with P^T (bf16 pairs) over columns 0-31
-// (queries 0-63) and 64-95 (queries 64-127); [128,256) dP^T, then dQ;
-// [256,256+d) dV; [256+d, 256+2d) dK.
+// (queries 0-63) and 64-95 (queries 64-127) and dS^T over columns 32-63 and
+// 96-127, so that dV += P^T dO and dK += dS^T Q take their A operand from
+// tensor memory; [128,256) dP^T, then dQ; [256,256+d) dV; [256+d, 256+2d) dK.
 #include "fa_internal.h"
 #include "sm100_ptx.cuh"
 
@@ -327,8 +328,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         tc_fence_after();
 #pragma unroll 1
         for (int kk = 0; kk < kTile / 16; ++kk)
-          mma_ss(tmem + Cfg::kColDK, kmajor_desc(dsb, kk), mnmajor_desc(qb, kk), id_acc,
-                 (it > 0 || kk > 0) ? 1u : 0u);
+          mma_ts(tmem + Cfg::kColDK, tmem + Cfg::kColS + 32 + (kk >> 2) * 64 + (kk & 3) * 8,
+                 mnmajor_desc(qb, kk), id_acc, (it > 0 || kk > 0) ? 1u : 0u);
         tc_commit(&sm.q_empty[s]);
 #pragma unroll 1
         for (int kk = 0; kk < kTile / 16; ++kk)
@@ -406,19 +407,23 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       // dS^T row r, query columns [64g, 64g+64) = column block g of the
       // 128B-swizzled [key][query] tile: eight 16-byte chunks.
       uint8_t* ds_row = sm.ds + g * 16384 + r * 128;
+      uint32_t dsw[32];  // dS^T row, bf16 pairs: also the A operand of dK in TMEM
 #pragma unroll
       for (int ch = 0; ch < 8; ++ch) {
-        uint32_t w[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int col = ch * 8 + 2 * e;  // 0..63 within this warpgroup's columns
           const float2 pf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pk[col / 2]));
           const float d0 = pf.x * (__uint_as_float(dp[col >> 5][col & 31]) - dl[col]);
           const float d1 = pf.y * (__uint_as_float(dp[(col + 1) >> 5][(col + 1) & 31]) - dl[col + 1]);
-          w[e] = pack_bf16x2(d0, d1);
+          dsw[ch * 4 + e] = pack_bf16x2(d0, d1);
         }
-        *reinterpret_cast<uint4*>(ds_row + ((ch ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+        *reinterpret_cast<uint4*>(ds_row + ((ch ^ (r & 7)) << 4)) =
+            make_uint4(dsw[ch * 4], dsw[ch * 4 + 1], dsw[ch * 4 + 2], dsw[ch * 4 + 3]);
       }
+      // Over S^T columns [64g + 32, 64g + 64), read in the P phase already.
+      tmem_st32(colS + 32, dsw);
+      tmem_wait_st();
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(&sm.ds_ready);
