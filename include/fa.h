@@ -152,16 +152,32 @@ int fa_device_status(void* stream, int* site);
 const char* fa_status_string(int status);
 
 /*
- * The order in which the forward kernel's persistent CTAs take work items.
- * A work item is one (b*H + h, q-tile pair) unit: 256 query rows of one
- * head.  Writes up to max_items entries of item_bh, item_pair and
- * item_cost (the item's number of 128-key tiles summed over its two query
- * tiles) and returns the number of items, or a negative FA_ERR_* code.
- * Causal work is ordered longest first (the LPT rule of the CMU post's
- * slide pages 27-46); host-only, needs no device.
+ * The forward kernel's work list and its split over persistent CTAs.  A
+ * work item is one (b*H + h, q-tile pair) unit: 256 query rows of one head.
+ * Items are listed with heads in groups of 8 and, inside a group, longest
+ * first (the LPT rule of the CMU post's slide pages 27-46: under a causal
+ * mask later query tiles see more keys).  Without a mask the kernel runs
+ * min(items, num_ctas) persistent CTAs (num_ctas = the device's SM count)
+ * and CTA c takes the list in snake order (fa_snake_assign); under a causal
+ * mask every item gets its own CTA and the hardware dispatches them in list
+ * order as SMs free up (greedy list scheduling).  Writes up to max_items
+ * entries of item_bh, item_pair, item_cost (the item's number of 128-key
+ * tiles summed over its two query tiles) and item_cta (any of them may be
+ * NULL) and returns the number of items, or a negative FA_ERR_* code.
+ * Host only; needs no device.
  */
-int fa_fwd_schedule(int B, int H, int N, int causal, int* item_bh, int* item_pair,
-                    int* item_cost, int max_items);
+int fa_fwd_schedule(int B, int H, int N, int causal, int num_ctas, int* item_bh,
+                    int* item_pair, int* item_cost, int* item_cta, int max_items);
+
+/*
+ * The static assignment of a list of n work items to `workers` persistent
+ * workers used by the kernels: round k = i / workers of the list is dealt
+ * to workers 0..workers-1 when k is even and in reverse when k is odd.  On
+ * a longest-first list this balances the workers the way the LPT rule does
+ * (the CMU post's example: costs 4,4,3,3,2,2,1,1 on 3 SMs give loads
+ * 7,7,6).  Writes worker_of_item[0..n); returns FA_OK or FA_ERR_ARG.
+ */
+int fa_snake_assign(int n, int workers, int* worker_of_item);
 
 /* Library version, for the loader's sanity check. */
 int fa_version(void);

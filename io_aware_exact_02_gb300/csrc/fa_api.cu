@@ -25,6 +25,7 @@ struct DeviceState {
   bool checked = false;
   bool supported = false;
   int* status = nullptr;  // device address of g_status
+  int sm_count = 0;
 };
 
 std::mutex g_mu;
@@ -48,6 +49,12 @@ int device_state(DeviceState** out) {
       return FA_ERR_DEVICE;
     }
     s.supported = (major == 10 && minor == 3);
+    if (s.supported &&
+        (cudaDeviceGetAttribute(&s.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+         s.sm_count < 1)) {
+      cudaGetLastError();
+      return FA_ERR_DEVICE;
+    }
     if (s.supported) {
       void* addr = nullptr;
       if (cudaGetSymbolAddress(&addr, g_status) != cudaSuccess) {
@@ -161,6 +168,7 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
   p.n_pairs = ceil_div(N, kPairRows);
   p.causal = causal;
   p.scale_log2 = scale * 1.4426950408889634f;
+  p.grid = fwd_grid(BH, p.n_pairs, causal, ds->sm_count);
   return launch_fwd(tq, tk, tv, p, d, static_cast<cudaStream_t>(stream));
 }
 
@@ -240,15 +248,17 @@ int fa_device_status(void* stream, int* site) {
   return h[0];
 }
 
-int fa_fwd_schedule(int B, int H, int N, int causal, int* item_bh, int* item_pair,
-                    int* item_cost, int max_items) {
+int fa_fwd_schedule(int B, int H, int N, int causal, int num_ctas, int* item_bh, int* item_pair,
+                    int* item_cost, int* item_cta, int max_items) {
   if (causal != 0 && causal != 1) return FA_ERR_ARG;
+  if (num_ctas < 1) return FA_ERR_ARG;
   int rc = check_shape(B, H, N, 64, 1.0f);
   if (rc != FA_OK) return rc;
   const int BH = B * H;
   const int n_pairs = ceil_div(N, kPairRows);
   const int n_kv = ceil_div(N, kTile);
   const long long total = (long long)BH * n_pairs;
+  const int ctas = fwd_grid(BH, n_pairs, causal, num_ctas);
   for (long long t = 0; t < total && t < max_items; ++t) {
     int bh, pair;
     fwd_item((int)t, BH, n_pairs, &bh, &pair);
@@ -256,8 +266,15 @@ int fa_fwd_schedule(int B, int H, int N, int causal, int* item_bh, int* item_pai
     if (item_pair) item_pair[t] = pair;
     if (item_cost)
       item_cost[t] = fwd_kv_tiles(2 * pair, n_kv, causal) + fwd_kv_tiles(2 * pair + 1, n_kv, causal);
+    if (item_cta) item_cta[t] = snake_cta((int)t, ctas);
   }
   return (int)total;
+}
+
+int fa_snake_assign(int n, int workers, int* worker_of_item) {
+  if (n < 0 || workers < 1 || (n > 0 && !worker_of_item)) return FA_ERR_ARG;
+  for (int i = 0; i < n; ++i) worker_of_item[i] = snake_cta(i, workers);
+  return FA_OK;
 }
 
 }  // extern "C"

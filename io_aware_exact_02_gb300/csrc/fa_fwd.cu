@@ -1,11 +1,16 @@
 // fa_fwd.cu -- forward pass of exact attention on sm_103a.
 //
-// One CTA computes 256 query rows (two 128-row Q tiles) of one head.  It
-// keeps both Q tiles in shared memory, streams the head's K and V tiles
-// through a ring of shared-memory slots filled by TMA, and never writes a
-// score to HBM: S lives in tensor memory, P replaces it there as bf16, and
-// only O and the per-row logsumexp are stored (cs2680 Lecture 9, sec. 9.2 and
-// 9.4; "Reading CMU 11-868 LLM Systems: FlashAttention", slide pages 9-12).
+// A work item is 256 query rows (two 128-row Q tiles) of one head.  Without
+// a mask the grid is persistent (one CTA per SM, each walking a share of the
+// items; CMU 11-868 FlashAttention post, slide page 26), so the next item's
+// Q and K/V loads overlap the end of the current one; under a causal mask
+// each item gets a CTA and the block scheduler dispatches the longest-first
+// list greedily (slide pages 27-46).  A CTA keeps both Q tiles in
+// shared memory, streams the head's K and V tiles through a ring of
+// shared-memory slots filled by TMA, and never writes a score to HBM: S
+// lives in tensor memory, P replaces it there as bf16, and only O and the
+// per-row logsumexp are stored (cs2680 Lecture 9, sec. 9.2 and 9.4; CMU post,
+// slide pages 9-12).
 //
 // Warp roles (320 threads):
 //   warps 0-3  softmax for Q tile 0 (thread r owns row r of the tile)
@@ -54,11 +59,13 @@ struct alignas(1024) FwdSmem {
   uint8_t q[2][FwdCfg<D>::kTileBytes];
   uint8_t kv[FwdCfg<D>::kStages][FwdCfg<D>::kTileBytes];
   uint64_t q_full;
+  uint64_t q_empty;  // both Q tiles consumed by the item's last S product
   uint64_t kv_full[FwdCfg<D>::kStages];
   uint64_t kv_empty[FwdCfg<D>::kStages];
   uint64_t s_full[2];
   uint64_t p_full[2];
   uint64_t o_full[2];
+  uint64_t o_empty[2];  // softmax t has read O_t of the item (epilogue done)
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
@@ -66,7 +73,8 @@ struct alignas(1024) FwdSmem {
 
 // Wait sites reported through the status word.
 enum : int {
-  kSiteQFull = 101, kSiteKvEmpty, kSiteKvFull, kSitePFull, kSiteSFull, kSiteOFull, kSiteDrain
+  kSiteQFull = 101, kSiteKvEmpty, kSiteKvFull, kSitePFull, kSiteSFull, kSiteOFull, kSiteDrain,
+  kSiteQEmpty, kSiteOEmpty
 };
 
 // Descriptor of the K-major, 128B-swizzled tile at `base` for MMA K-step kk:
@@ -107,6 +115,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
 
   if (tid == 0) {
     mbar_init(&sm.q_full, 1);
+    mbar_init(&sm.q_empty, 1);
     for (int s = 0; s < S; ++s) {
       mbar_init(&sm.kv_full[s], 1);
       mbar_init(&sm.kv_empty[s], 1);
@@ -115,6 +124,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
       mbar_init(&sm.s_full[t], 1);
       mbar_init(&sm.p_full[t], 128);
       mbar_init(&sm.o_full[t], 1);
+      mbar_init(&sm.o_empty[t], 128);
     }
     mbar_init(&sm.drain, 1);
     sm.abort_flag = 0;
@@ -129,11 +139,26 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
 
-  int bh, pair;
-  fwd_item(blockIdx.x, p.BH, p.n_pairs, &bh, &pair);
-  const int row0 = pair * kPairRows;
-  const int n_t0 = fwd_kv_tiles(2 * pair, p.n_kv, p.causal);
-  const int n_t1 = fwd_kv_tiles(2 * pair + 1, p.n_kv, p.causal);  // n_t0 <= n_t1 <= n_t0 + 1
+  // Persistent CTAs: CTA c takes the work items of the longest-first list
+  // in "snake" order -- items c, 2G-1-c, 2G+c, 4G-1-c, ... for G CTAs -- so
+  // that every CTA gets a similar mix of long and short items.
+  const int num_items = p.BH * p.n_pairs;
+  const int G = gridDim.x;
+  auto item_of_round = [&](int k) -> int {
+    const int base = k * G;
+    return (k & 1) ? base + (G - 1 - (int)blockIdx.x) : base + (int)blockIdx.x;
+  };
+  struct Item {
+    int bh, pair, row0, n_t0, n_t1;
+  };
+  auto decode = [&](int idx) -> Item {
+    Item it;
+    fwd_item(idx, p.BH, p.n_pairs, &it.bh, &it.pair);
+    it.row0 = it.pair * kPairRows;
+    it.n_t0 = fwd_kv_tiles(2 * it.pair, p.n_kv, p.causal);
+    it.n_t1 = fwd_kv_tiles(2 * it.pair + 1, p.n_kv, p.causal);  // n_t0 <= n_t1 <= n_t0 + 1
+    return it;
+  };
 
   if (warp == 8) {
     // ------------------------------------------------------------ producer
@@ -141,29 +166,41 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
       prefetch_tmap(&tq);
       prefetch_tmap(&tk);
       prefetch_tmap(&tv);
-      mbar_arrive_expect_tx(&sm.q_full, 2 * Cfg::kTileBytes);
-      for (int t = 0; t < 2; ++t)
-        for (int h = 0; h < D / 64; ++h)
-          tma_load_3d(sm.q[t] + h * 16384, &tq, &sm.q_full, h * 64, row0 + t * kTile, bh);
-      int c = 0;
+      int c = 0;         // K/V loads issued, over all items
+      int q_issued = 0;  // Q pairs issued
       bool ok = true;
-      for (int j = 0; j < n_t1 && ok; ++j) {
-        for (int w = 0; w < 2 && ok; ++w, ++c) {
-          const int slot = c % S, use = c / S;
-          if (use > 0 &&
-              !mbar_wait(&sm.kv_empty[slot], (use - 1) & 1, p.status, abortf, kSiteKvEmpty)) {
-            ok = false;
-            break;
-          }
-          mbar_arrive_expect_tx(&sm.kv_full[slot], Cfg::kTileBytes);
+      for (int k = 0; ok && k * G < num_items; ++k) {
+        const int idx = item_of_round(k);
+        if (idx >= num_items) continue;
+        const Item it = decode(idx);
+        if (q_issued > 0 &&
+            !mbar_wait(&sm.q_empty, (q_issued - 1) & 1, p.status, abortf, kSiteQEmpty)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(&sm.q_full, 2 * Cfg::kTileBytes);
+        for (int t = 0; t < 2; ++t)
           for (int h = 0; h < D / 64; ++h)
-            tma_load_3d(sm.kv[slot] + h * 16384, w == 0 ? &tk : &tv, &sm.kv_full[slot], h * 64,
-                        j * kTile, bh);
+            tma_load_3d(sm.q[t] + h * 16384, &tq, &sm.q_full, h * 64, it.row0 + t * kTile, it.bh);
+        ++q_issued;
+        for (int j = 0; j < it.n_t1 && ok; ++j) {
+          for (int w = 0; w < 2 && ok; ++w, ++c) {
+            const int slot = c % S, use = c / S;
+            if (use > 0 &&
+                !mbar_wait(&sm.kv_empty[slot], (use - 1) & 1, p.status, abortf, kSiteKvEmpty)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(&sm.kv_full[slot], Cfg::kTileBytes);
+            for (int h = 0; h < D / 64; ++h)
+              tma_load_3d(sm.kv[slot] + h * 16384, w == 0 ? &tk : &tv, &sm.kv_full[slot], h * 64,
+                          j * kTile, it.bh);
+          }
         }
       }
       if (!ok) {
         // Let the copies already issued land before the CTA exits.
-        drain_wait(&sm.q_full, 0);
+        if (q_issued > 0) drain_wait(&sm.q_full, (q_issued - 1) & 1);
         for (int cc = c - 1; cc >= 0 && cc >= c - S; --cc) drain_wait(&sm.kv_full[cc % S], (cc / S) & 1);
       }
     }
@@ -175,7 +212,9 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
       const uint32_t id_pv = idesc_bf16(128, D, false, true);
       const uint32_t q_addr[2] = {smem_u32(sm.q[0]), smem_u32(sm.q[1])};
       uint32_t p_par[2] = {0, 0};
-      bool ok = mbar_wait(&sm.q_full, 0, p.status, abortf, kSiteQFull);
+      int cb = 0;       // K/V loads consumed before the current item
+      int n_done = 0;   // items finished by this CTA
+      bool ok = true;
 
       auto issue_s = [&](int t, int kslot) {
         const uint32_t kb = smem_u32(sm.kv[kslot]);
@@ -185,12 +224,20 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
                  kk > 0);
         tc_commit(&sm.s_full[t]);
       };
-      auto issue_pv = [&](int t, int vslot, bool accumulate) {
+      // O_t += P_t V; the item's first product overwrites O_t, so it waits
+      // until softmax t has stored the previous item's O_t.
+      auto issue_pv = [&](int t, int vslot, bool accumulate) -> bool {
+        if (!accumulate && n_done > 0) {
+          if (!mbar_wait(&sm.o_empty[t], (n_done - 1) & 1, p.status, abortf, kSiteOEmpty))
+            return false;
+          tc_fence_after();
+        }
         const uint32_t vb = smem_u32(sm.kv[vslot]);
 #pragma unroll 1
         for (int kk = 0; kk < kTile / 16; ++kk)
           mma_ts(tmem + Cfg::col_o(t), tmem + Cfg::col_s(t) + kk * 8, mnmajor_desc(vb, kk), id_pv,
                  (accumulate || kk > 0) ? 1u : 0u);
+        return true;
       };
       auto wait_full = [&](int cnt) -> bool {
         return mbar_wait(&sm.kv_full[cnt % S], (cnt / S) & 1, p.status, abortf, kSiteKvFull);
@@ -201,52 +248,67 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
         return r;
       };
 
-      if (ok) ok = wait_full(0);
-      if (ok) {
-        tc_fence_after();
-        issue_s(0, 0);
-        issue_s(1, 0);
-        tc_commit(&sm.kv_empty[0]);
-      }
-      for (int j = 1; j < n_t1 && ok; ++j) {
-        const int kc = 2 * j, vc = 2 * j - 1;
-        ok = wait_full(kc) && wait_full(vc);
-        if (!ok) break;
-        ok = wait_p(0);
-        if (!ok) break;
-        tc_fence_after();
-        issue_pv(0, vc % S, j - 1 > 0);
-        if (j < n_t0) {
-          issue_s(0, kc % S);
-        } else {
-          tc_commit(&sm.o_full[0]);  // tile 0 has no more keys (causal)
-        }
-        ok = wait_p(1);
-        if (!ok) break;
-        tc_fence_after();
-        issue_pv(1, vc % S, j - 1 > 0);
-        tc_commit(&sm.kv_empty[vc % S]);
-        issue_s(1, kc % S);
-        tc_commit(&sm.kv_empty[kc % S]);
-      }
-      if (ok) {
-        const int vc = 2 * n_t1 - 1;
-        ok = wait_full(vc);
-        if (ok && n_t0 == n_t1) {
-          ok = wait_p(0);
-          if (ok) {
-            tc_fence_after();
-            issue_pv(0, vc % S, n_t1 - 1 > 0);
-            tc_commit(&sm.o_full[0]);
-          }
-        }
-        if (ok) ok = wait_p(1);
+      for (int k = 0; ok && k * G < num_items; ++k) {
+        const int idx = item_of_round(k);
+        if (idx >= num_items) continue;
+        const Item it = decode(idx);
+        const int n_t0 = it.n_t0, n_t1 = it.n_t1;
+        ok = mbar_wait(&sm.q_full, n_done & 1, p.status, abortf, kSiteQFull);
+        if (ok) ok = wait_full(cb);
         if (ok) {
           tc_fence_after();
-          issue_pv(1, vc % S, n_t1 - 1 > 0);
-          tc_commit(&sm.o_full[1]);
-          tc_commit(&sm.kv_empty[vc % S]);
+          issue_s(0, cb % S);
+          issue_s(1, cb % S);
+          tc_commit(&sm.kv_empty[cb % S]);
+          if (n_t1 == 1) tc_commit(&sm.q_empty);
         }
+        for (int j = 1; j < n_t1 && ok; ++j) {
+          const int kc = cb + 2 * j, vc = cb + 2 * j - 1;
+          ok = wait_full(kc) && wait_full(vc);
+          if (!ok) break;
+          ok = wait_p(0);
+          if (!ok) break;
+          tc_fence_after();
+          ok = issue_pv(0, vc % S, j - 1 > 0);
+          if (!ok) break;
+          if (j < n_t0) {
+            issue_s(0, kc % S);
+          } else {
+            tc_commit(&sm.o_full[0]);  // tile 0 has no more keys (causal)
+          }
+          ok = wait_p(1);
+          if (!ok) break;
+          tc_fence_after();
+          ok = issue_pv(1, vc % S, j - 1 > 0);
+          if (!ok) break;
+          tc_commit(&sm.kv_empty[vc % S]);
+          issue_s(1, kc % S);
+          tc_commit(&sm.kv_empty[kc % S]);
+          if (j == n_t1 - 1) tc_commit(&sm.q_empty);  // last product reading Q
+        }
+        if (ok) {
+          const int vc = cb + 2 * n_t1 - 1;
+          ok = wait_full(vc);
+          if (ok && n_t0 == n_t1) {
+            ok = wait_p(0);
+            if (ok) {
+              tc_fence_after();
+              ok = issue_pv(0, vc % S, n_t1 - 1 > 0);
+              if (ok) tc_commit(&sm.o_full[0]);
+            }
+          }
+          if (ok) ok = wait_p(1);
+          if (ok) {
+            tc_fence_after();
+            ok = issue_pv(1, vc % S, n_t1 - 1 > 0);
+          }
+          if (ok) {
+            tc_commit(&sm.o_full[1]);
+            tc_commit(&sm.kv_empty[vc % S]);
+          }
+        }
+        cb += 2 * n_t1;
+        ++n_done;
       }
       // Every MMA issued so far must finish before TMEM is released.
       tc_commit(&sm.drain);
@@ -258,112 +320,118 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
     const int t = warp >> 2;             // which Q tile
     const int r = tid & 127;             // row within the tile
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-    const int n_t = t == 0 ? n_t0 : n_t1;
-    const int R = row0 + t * kTile + r;  // global query row
     const float c2 = p.scale_log2;  // nonzero: a zero scale arrives as a tiny positive one
     // A masked score is replaced by the value that loses every max (min)
     // and whose exponent c2 * s is -inf, so its probability is exactly 0.
     const float neutral = kNeg ? __int_as_float(0x7f800000) : __int_as_float(0xff800000);
     const uint32_t colS = tmem + lane_base + Cfg::col_s(t);
     const uint32_t colO = tmem + lane_base + Cfg::col_o(t);
-    const int diag_tile = p.causal ? (row0 + t * kTile) / kTile : -1;
-
-    float m_ref = __int_as_float(0xff800000);  // -inf
-    float l = 0.f;
     uint32_t s_par = 0;
+    int n_done = 0;
     bool ok = true;
-    for (int j = 0; j < n_t; ++j) {
-      ok = mbar_wait(&sm.s_full[t], s_par, p.status, abortf, kSiteSFull);
-      ok = __all_sync(0xffffffffu, ok);  // keep the warp's collective TMEM ops converged
-      s_par ^= 1;
-      if (!ok) break;
-      tc_fence_after();
-      uint32_t sr[4][32];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(colS + c * 32, sr[c]);
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_wait_ld(sr[c]);
 
-      const bool need_mask = (j + 1) * kTile > p.N || j == diag_tile;
-      if (need_mask) {
-        // Keys at columns >= lim of this tile are masked for this row.
-        int lim = p.N - j * kTile;
-        if (p.causal && R + 1 - j * kTile < lim) lim = R + 1 - j * kTile;
+    for (int k = 0; ok && k * G < num_items; ++k) {
+      const int idx = item_of_round(k);
+      if (idx >= num_items) continue;
+      const Item item = decode(idx);
+      const int bh = item.bh;
+      const int n_t = t == 0 ? item.n_t0 : item.n_t1;
+      const int R = item.row0 + t * kTile + r;  // global query row
+      const int diag_tile = p.causal ? (item.row0 + t * kTile) / kTile : -1;
+      float m_ref = __int_as_float(0xff800000);  // -inf
+      float l = 0.f;
+      for (int j = 0; j < n_t; ++j) {
+        ok = mbar_wait(&sm.s_full[t], s_par, p.status, abortf, kSiteSFull);
+        ok = __all_sync(0xffffffffu, ok);  // keep the warp's collective TMEM ops converged
+        s_par ^= 1;
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t sr[4][32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_ld32(colS + c * 32, sr[c]);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_wait_ld(sr[c]);
+
+        const bool need_mask = (j + 1) * kTile > p.N || j == diag_tile;
+        if (need_mask) {
+          // Keys at columns >= lim of this tile are masked for this row.
+          int lim = p.N - j * kTile;
+          if (p.causal && R + 1 - j * kTile < lim) lim = R + 1 - j * kTile;
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (c * 32 + i >= lim) sr[c][i] = __float_as_uint(neutral);
+        }
+        // Tile extreme of the raw scores, as eight independent chains joined
+        // by a tree (max/min are exact, so the order does not change it).
+        float mx8[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) mx8[u] = neutral;
 #pragma unroll
         for (int c = 0; c < 4; ++c)
 #pragma unroll
           for (int i = 0; i < 32; ++i)
-            if (c * 32 + i >= lim) sr[c][i] = __float_as_uint(neutral);
-      }
-      // Tile extreme of the raw scores, as eight independent chains joined
-      // by a tree (max/min are exact, so the order does not change it).
-      float mx8[8];
+            mx8[i & 7] = kNeg ? fminf(mx8[i & 7], __uint_as_float(sr[c][i]))
+                              : fmaxf(mx8[i & 7], __uint_as_float(sr[c][i]));
 #pragma unroll
-      for (int u = 0; u < 8; ++u) mx8[u] = neutral;
+        for (int w = 4; w > 0; w >>= 1)
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
+          for (int u = 0; u < w; ++u)
+            mx8[u] = kNeg ? fminf(mx8[u], mx8[u + w]) : fmaxf(mx8[u], mx8[u + w]);
+        const float m_tile = mx8[0] * c2;
+        float alpha = 1.f;
+        if (m_tile > m_ref + kRescaleSlack) {
+          alpha = ex2_approx(m_ref - m_tile);  // 0 on the first tile (m_ref = -inf)
+          m_ref = m_tile;
+        }
+        l *= alpha;
+        const float neg_m = -m_ref;
+        float ls8[8];  // eight partial row sums, joined by a tree below
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-          mx8[i & 7] = kNeg ? fminf(mx8[i & 7], __uint_as_float(sr[c][i]))
-                            : fmaxf(mx8[i & 7], __uint_as_float(sr[c][i]));
+        for (int u = 0; u < 8; ++u) ls8[u] = 0.f;
 #pragma unroll
-      for (int w = 4; w > 0; w >>= 1)
+        for (int h = 0; h < 2; ++h) {
+          uint32_t pk[32];
 #pragma unroll
-        for (int u = 0; u < w; ++u)
-          mx8[u] = kNeg ? fminf(mx8[u], mx8[u + w]) : fmaxf(mx8[u], mx8[u + w]);
-      const float m_tile = mx8[0] * c2;
-      float alpha = 1.f;
-      if (m_tile > m_ref + kRescaleSlack) {
-        alpha = ex2_approx(m_ref - m_tile);  // 0 on the first tile (m_ref = -inf)
-        m_ref = m_tile;
-      }
-      l *= alpha;
-      const float neg_m = -m_ref;
-      float ls8[8];  // eight partial row sums, joined by a tree below
+          for (int c2i = 0; c2i < 2; ++c2i) {
+            const int c = 2 * h + c2i;
 #pragma unroll
-      for (int u = 0; u < 8; ++u) ls8[u] = 0.f;
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        uint32_t pk[32];
-#pragma unroll
-        for (int c2i = 0; c2i < 2; ++c2i) {
-          const int c = 2 * h + c2i;
-#pragma unroll
-          for (int i = 0; i < 32; i += 2) {
-            const float p0 = ex2_approx(fmaf(__uint_as_float(sr[c][i]), c2, neg_m));
-            const float p1 = ex2_approx(fmaf(__uint_as_float(sr[c][i + 1]), c2, neg_m));
-            ls8[(i >> 1) & 7] += p0 + p1;
-            pk[c2i * 16 + i / 2] = pack_bf16x2(p0, p1);
+            for (int i = 0; i < 32; i += 2) {
+              const float p0 = ex2_approx(fmaf(__uint_as_float(sr[c][i]), c2, neg_m));
+              const float p1 = ex2_approx(fmaf(__uint_as_float(sr[c][i + 1]), c2, neg_m));
+              ls8[(i >> 1) & 7] += p0 + p1;
+              pk[c2i * 16 + i / 2] = pack_bf16x2(p0, p1);
+            }
           }
+          tmem_st32(colS + h * 32, pk);
         }
-        tmem_st32(colS + h * 32, pk);
-      }
 #pragma unroll
-      for (int w = 4; w > 0; w >>= 1)
+        for (int w = 4; w > 0; w >>= 1)
 #pragma unroll
-        for (int u = 0; u < w; ++u) ls8[u] += ls8[u + w];
-      l += ls8[0];
-      tmem_wait_st();
-      // Correct the O accumulator if this row's reference moved (warp-wide
-      // decision: TMEM loads/stores are warp-collective).
-      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t orow[32];
-          tmem_ld32(colO + c * 32, orow);
-          tmem_wait_ld(orow);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) orow[i] = __float_as_uint(__uint_as_float(orow[i]) * alpha);
-          tmem_st32(colO + c * 32, orow);
-        }
+          for (int u = 0; u < w; ++u) ls8[u] += ls8[u + w];
+        l += ls8[0];
         tmem_wait_st();
+        // Correct the O accumulator if this row's reference moved (warp-wide
+        // decision: TMEM loads/stores are warp-collective).
+        if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t orow[32];
+            tmem_ld32(colO + c * 32, orow);
+            tmem_wait_ld(orow);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) orow[i] = __float_as_uint(__uint_as_float(orow[i]) * alpha);
+            tmem_st32(colO + c * 32, orow);
+          }
+          tmem_wait_st();
+        }
+        tc_fence_before();
+        mbar_arrive(&sm.p_full[t]);
       }
-      tc_fence_before();
-      mbar_arrive(&sm.p_full[t]);
-    }
-    if (ok) ok = mbar_wait(&sm.o_full[t], 0, p.status, abortf, kSiteOFull);
-    ok = __all_sync(0xffffffffu, ok);
-    if (ok) {
+      if (ok) ok = mbar_wait(&sm.o_full[t], n_done & 1, p.status, abortf, kSiteOFull);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
       tc_fence_after();
       const float inv_l = 1.f / l;
       __nv_bfloat16* orow_g = reinterpret_cast<__nv_bfloat16*>(p.o) + ((size_t)bh * p.N + R) * D;
@@ -385,6 +453,10 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
         }
       }
       if (R < p.N) p.lse[(size_t)bh * p.N + R] = (m_ref + __log2f(l)) * kLn2;
+      // O_t may now be overwritten by the next item's first product.
+      tc_fence_before();
+      mbar_arrive(&sm.o_empty[t]);
+      ++n_done;
     }
   }
 
@@ -403,8 +475,7 @@ int launch_fwd_dn(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMa
   if (cudaFuncSetAttribute(fa_fwd_kernel<D, kNeg>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)smem) != cudaSuccess)
     return FA_ERR_LAUNCH;
-  const unsigned grid = (unsigned)p.BH * (unsigned)p.n_pairs;
-  fa_fwd_kernel<D, kNeg><<<grid, FwdCfg<D>::kThreads, smem, stream>>>(tq, tk, tv, p);
+  fa_fwd_kernel<D, kNeg><<<(unsigned)p.grid, FwdCfg<D>::kThreads, smem, stream>>>(tq, tk, tv, p);
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 

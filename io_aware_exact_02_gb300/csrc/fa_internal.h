@@ -46,7 +46,28 @@ struct FwdParams {
   int n_pairs;      // ceil(N / 256)
   int causal;
   float scale_log2;  // scale * log2(e)
+  int grid;          // persistent CTAs: min(work items, SMs)
 };
+
+// CTA that runs work item `idx` of a longest-first list on `ctas` persistent
+// CTAs: round k = idx / ctas is taken in order when k is even and in
+// reverse when k is odd ("snake" order).
+__host__ __device__ inline int snake_cta(int idx, int ctas) {
+  const int k = idx / ctas, pos = idx % ctas;
+  return (k & 1) ? ctas - 1 - pos : pos;
+}
+
+// The forward kernel's grid.  Without a mask every item costs the same and
+// min(items, SMs) persistent CTAs split the list statically.  Under a causal
+// mask item costs differ by up to N/128 and there are few items per SM, so
+// every item gets its own CTA: the hardware hands CTAs to SMs in list order
+// as SMs free up, i.e. greedy list scheduling of the longest-first list
+// (the LPT rule), which a static split cannot match.
+__host__ __device__ inline int fwd_grid(int BH, int n_pairs, int causal, int sm_count) {
+  const long long items = (long long)BH * n_pairs;
+  if (causal) return (int)items;
+  return (int)(items < sm_count ? items : sm_count);
+}
 
 struct BwdParams {
   const void* o;     // [BH][N][d] bf16 (forward output)

@@ -44,7 +44,8 @@ SIGNATURES = {
                             _vp]),
     "fa_device_status": (_i, [_vp, _ip]),
     "fa_status_string": (ctypes.c_char_p, [_i]),
-    "fa_fwd_schedule": (_i, [_i, _i, _i, _i, _ip, _ip, _ip, _i]),
+    "fa_fwd_schedule": (_i, [_i, _i, _i, _i, _i, _ip, _ip, _ip, _ip, _i]),
+    "fa_snake_assign": (_i, [_i, _i, _ip]),
     "fa_version": (_i, []),
 }
 
@@ -197,14 +198,22 @@ def check_device_status(stream=None):
         raise FaError("kernel", code, status_string(code) + " (site %d)" % site)
 
 
-def fwd_schedule(B: int, H: int, N: int, causal: bool):
-    """The forward kernel's work order: list of (bh, pair, cost)."""
+def fwd_schedule(B: int, H: int, N: int, causal: bool, num_ctas: int = 152):
+    """The forward kernel's work list: (bh, pair, cost, cta) per item, in list order."""
     lib = load()
-    n = lib.fa_fwd_schedule(B, H, N, int(bool(causal)), None, None, None, 0)
+    n = lib.fa_fwd_schedule(B, H, N, int(bool(causal)), int(num_ctas), None, None, None, None, 0)
     if n < 0:
         _check("fa_fwd_schedule", n)
     bh = (ctypes.c_int * n)()
     pr = (ctypes.c_int * n)()
     cost = (ctypes.c_int * n)()
-    lib.fa_fwd_schedule(B, H, N, int(bool(causal)), bh, pr, cost, n)
-    return list(zip(bh, pr, cost))
+    cta = (ctypes.c_int * n)()
+    lib.fa_fwd_schedule(B, H, N, int(bool(causal)), int(num_ctas), bh, pr, cost, cta, n)
+    return list(zip(bh, pr, cost, cta))
+
+
+def snake_assign(n: int, workers: int):
+    """The kernels' static assignment of n listed items to persistent workers."""
+    out = (ctypes.c_int * max(n, 1))()
+    _check("fa_snake_assign", load().fa_snake_assign(int(n), int(workers), out))
+    return list(out)[:n]

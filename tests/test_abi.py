@@ -121,7 +121,7 @@ def golden_lpt():
     return vals["lpt_in_order"], vals["lpt_longest_first"]
 
 
-def test_lpt_example_of_the_pages():
+def test_lpt_example_of_the_pages(lib):
     # Two batches of four causal query tiles costing 1, 2, 3, 4 key tiles,
     # three SMs: in order the SMs end with [9, 5, 6]; longest first gives
     # [7, 7, 6] (CMU 11-868 post, LPT paragraph).
@@ -129,17 +129,28 @@ def test_lpt_example_of_the_pages():
     costs = [1, 2, 3, 4, 1, 2, 3, 4]
     assert greedy(costs, 3) == in_order
     assert greedy(sorted(costs, reverse=True), 3) == lpt
+    # The kernels' static persistent assignment reproduces the LPT loads on
+    # the longest-first list.
+    ordered = sorted(costs, reverse=True)
+    workers = fa.snake_assign(len(ordered), 3)
+    loads = [sum(c for c, w in zip(ordered, workers) if w == k) for k in range(3)]
+    assert loads == lpt
+    assert fa.snake_assign(7, 3) == [0, 1, 2, 2, 1, 0, 0]
 
 
 @pytest.mark.parametrize("B,H,N,causal", [(1, 2, 1024, 1), (2, 5, 3000, 1), (3, 4, 700, 0),
                                           (1, 17, 4096, 1), (1, 1, 1, 0)])
 def test_schedule_covers_every_item_once_longest_first(lib, B, H, N, causal):
-    items = fa.fwd_schedule(B, H, N, causal)
+    items = fa.fwd_schedule(B, H, N, causal, num_ctas=7)
     n_pairs = -(-N // 256)
-    assert sorted((bh, p) for bh, p, _ in items) == [(bh, p) for bh in range(B * H)
-                                                    for p in range(n_pairs)]
+    assert sorted((bh, p) for bh, p, _, _ in items) == [(bh, p) for bh in range(B * H)
+                                                       for p in range(n_pairs)]
+    ctas = len(items) if causal else min(len(items), 7)
+    assert [c for _, _, _, c in items] == fa.snake_assign(len(items), ctas)
+    if causal:
+        assert [c for _, _, _, c in items] == list(range(len(items)))
     n_kv = -(-N // 128)
-    for bh, p, c in items:
+    for bh, p, c, _ in items:
         expect = (min(2 * p + 1, n_kv) + min(2 * p + 2, n_kv)) if causal else 2 * n_kv
         assert c == expect
     # Within each group of heads the costs never increase (LPT order), and the
@@ -147,9 +158,9 @@ def test_schedule_covers_every_item_once_longest_first(lib, B, H, N, causal):
     group = 8 * n_pairs
     for g0 in range(0, len(items), group):
         chunk = items[g0:g0 + group]
-        costs = [c for _, _, c in chunk]
+        costs = [c for _, _, c, _ in chunk]
         assert costs == sorted(costs, reverse=True)
-    if causal and B * H >= 1:
-        loads_lpt = greedy([c for _, _, c in items], 3)
-        loads_fwd = greedy(sorted([c for _, _, c in items]), 3)
+    if causal:
+        loads_lpt = greedy([c for _, _, c, _ in items], 3)
+        loads_fwd = greedy(sorted([c for _, _, c, _ in items]), 3)
         assert max(loads_lpt) <= max(loads_fwd)
