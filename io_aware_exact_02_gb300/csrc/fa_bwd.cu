@@ -104,6 +104,17 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
       : "memory");
 }
 
+// Adds 32 consecutive dQ columns of one row (8 groups of 4) to the
+// tile-blocked accumulator, whose groups are 128 * 4 floats apart.
+__device__ __forceinline__ void add_dq_chunk(float* base, const uint32_t (&a)[32]) {
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    const float4 val = make_float4(__uint_as_float(a[4 * e]), __uint_as_float(a[4 * e + 1]),
+                                   __uint_as_float(a[4 * e + 2]), __uint_as_float(a[4 * e + 3]));
+    atomicAdd(reinterpret_cast<float4*>(base + (size_t)e * kTile * 4), val);
+  }
+}
+
 // Work order of the main kernel: heads in groups of kHeadGroup; inside a
 // group the key tiles go first to last (under a causal mask key tile j
 // visits n_kv - j query tiles, so the longest work items start first).
@@ -355,6 +366,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     // A masked score is replaced by the value whose exponent c2 * s is -inf.
     const float neutral = c2 < 0.f ? __int_as_float(0x7f800000) : __int_as_float(0xff800000);
     const int kv_row = j * kTile + r;
+    uint32_t held[32];
+    float* held_base = nullptr;  // dQ columns waiting to be added (see the drain)
     bool ok = true;
     for (int it = 0; it < n_iter; ++it) {
       const int s = it % NS;
@@ -393,6 +406,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&sm.p_ready);
+      if (held_base) {
+        add_dq_chunk(held_base, held);
+        held_base = nullptr;
+      }
 
       ok = mbar_wait(&sm.dp_full, par, p.status, abortf, kSiteDpFull);
       ok = __all_sync(0xffffffffu, ok);
@@ -445,16 +462,18 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         tc_fence_before();
         mbar_arrive(&sm.dq_empty);
         float* base = p.dq_acc + dqacc_index<D>(bh, p.n_kv, i * kTile + r, g * (D / 8));
+        add_dq_chunk(base, a[0]);
+        if (D == 128) {
+          // The second half waits in registers until after the next step's
+          // P phase, so that the reductions do not all compete with the
+          // next S^T and dP^T products for the shared-memory/L1 data path.
 #pragma unroll
-        for (int c = 0; c < D / 64; ++c)
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const float4 val = make_float4(__uint_as_float(a[c][4 * e]), __uint_as_float(a[c][4 * e + 1]),
-                                           __uint_as_float(a[c][4 * e + 2]), __uint_as_float(a[c][4 * e + 3]));
-            atomicAdd(reinterpret_cast<float4*>(base + (size_t)(c * 8 + e) * kTile * 4), val);
-          }
+          for (int e = 0; e < 32; ++e) held[e] = a[D / 64 - 1][e];
+          held_base = base + (size_t)8 * kTile * 4;
+        }
       }
     }
+    if (held_base) add_dq_chunk(held_base, held);
     // Epilogue: warpgroup 0 stores dV, warpgroup 1 stores scale * dK.
     if (ok) ok = mbar_wait(&sm.acc_full, 0, p.status, abortf, kSiteAccFull);
     ok = __all_sync(0xffffffffu, ok);
