@@ -391,15 +391,21 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
           for (int e = 0; e < 32; ++e)
             if (r > g * 64 + c * 32 + e) sr[c][e] = __float_as_uint(neutral);
       }
-      const float* lse2 = sm.lse2[s] + g * 64;
+      // lse2 pairs as packed f32x2 (8-byte aligned shared loads).
+      const uint64_t* lse2x2 = reinterpret_cast<const uint64_t*>(sm.lse2[s] + g * 64);
+      const uint64_t c2x2 = f2_pack(c2, c2);
+      const uint64_t minus1 = f2_pack(-1.f, -1.f);
       uint32_t pk[32];  // P^T for this warpgroup's 64 query columns, bf16 pairs
 #pragma unroll
       for (int c = 0; c < 2; ++c)
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
-          const float p0 = ex2_approx(fmaf(__uint_as_float(sr[c][e]), c2, -lse2[c * 32 + e]));
-          const float p1 = ex2_approx(fmaf(__uint_as_float(sr[c][e + 1]), c2, -lse2[c * 32 + e + 1]));
-          pk[c * 16 + e / 2] = pack_bf16x2(p0, p1);
+          // c2 * s - lse2 = fma(s, c2, -lse2), two columns per instruction.
+          float x0, x1;
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1])), c2x2,
+                           f2_mul(lse2x2[(c * 32 + e) / 2], minus1)),
+                    x0, x1);
+          pk[c * 16 + e / 2] = pack_bf16x2(ex2_approx(x0), ex2_approx(x1));
         }
       // Over the first 32 of this warpgroup's own S columns (already read).
       tmem_st32(colS, pk);
@@ -420,7 +426,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       tmem_ld32(colDP + 32, dp[1]);
       tmem_wait_ld(dp[0]);
       tmem_wait_ld(dp[1]);
-      const float* dl = sm.delta[s] + g * 64;
+      const uint64_t* dlx2 = reinterpret_cast<const uint64_t*>(sm.delta[s] + g * 64);
       // dS^T row r, query columns [64g, 64g+64) = column block g of the
       // 128B-swizzled [key][query] tile: eight 16-byte chunks.
       uint8_t* ds_row = sm.ds + g * 16384 + r * 128;
@@ -431,8 +437,12 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         for (int e = 0; e < 4; ++e) {
           const int col = ch * 8 + 2 * e;  // 0..63 within this warpgroup's columns
           const float2 pf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pk[col / 2]));
-          const float d0 = pf.x * (__uint_as_float(dp[col >> 5][col & 31]) - dl[col]);
-          const float d1 = pf.y * (__uint_as_float(dp[(col + 1) >> 5][(col + 1) & 31]) - dl[col + 1]);
+          // dS = P * (dP - D), two columns per packed instruction.
+          const uint64_t dpd = f2_add(f2_pack(__uint_as_float(dp[col >> 5][col & 31]),
+                                              __uint_as_float(dp[col >> 5][(col & 31) + 1])),
+                                      f2_mul(dlx2[col / 2], f2_pack(-1.f, -1.f)));
+          float d0, d1;
+          f2_unpack(f2_mul(f2_pack(pf.x, pf.y), dpd), d0, d1);
           dsw[ch * 4 + e] = pack_bf16x2(d0, d1);
         }
         *reinterpret_cast<uint4*>(ds_row + ((ch ^ (r & 7)) << 4)) =

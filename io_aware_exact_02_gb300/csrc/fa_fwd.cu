@@ -363,17 +363,19 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
             for (int i = 0; i < 32; ++i)
               if (c * 32 + i >= lim) sr[c][i] = __float_as_uint(neutral);
         }
-        // Tile extreme of the raw scores, as eight independent chains joined
-        // by a tree (max/min are exact, so the order does not change it).
+        // Tile extreme of the raw scores: eight independent chains of
+        // three-input max (min), joined by a tree (exact in any order).
         float mx8[8];
 #pragma unroll
         for (int u = 0; u < 8; ++u) mx8[u] = neutral;
 #pragma unroll
         for (int c = 0; c < 4; ++c)
 #pragma unroll
-          for (int i = 0; i < 32; ++i)
-            mx8[i & 7] = kNeg ? fminf(mx8[i & 7], __uint_as_float(sr[c][i]))
-                              : fmaxf(mx8[i & 7], __uint_as_float(sr[c][i]));
+          for (int i = 0; i < 32; i += 2) {
+            const int u = (i >> 1) & 7;
+            mx8[u] = kNeg ? fmin3(mx8[u], __uint_as_float(sr[c][i]), __uint_as_float(sr[c][i + 1]))
+                          : fmax3(mx8[u], __uint_as_float(sr[c][i]), __uint_as_float(sr[c][i + 1]));
+          }
 #pragma unroll
         for (int w = 4; w > 0; w >>= 1)
 #pragma unroll
@@ -386,10 +388,13 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
           m_ref = m_tile;
         }
         l *= alpha;
-        const float neg_m = -m_ref;
-        float ls8[8];  // eight partial row sums, joined by a tree below
+        // p = 2^(c2 * s - m) for pairs of scores with packed f32x2 FMAs;
+        // four packed partial row sums, joined by a tree below.
+        const uint64_t c2x2 = f2_pack(c2, c2);
+        const uint64_t negm2 = f2_pack(-m_ref, -m_ref);
+        uint64_t ls4[4];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) ls8[u] = 0.f;
+        for (int u = 0; u < 4; ++u) ls4[u] = 0;
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           uint32_t pk[32];
@@ -398,19 +403,22 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
             const int c = 2 * h + c2i;
 #pragma unroll
             for (int i = 0; i < 32; i += 2) {
-              const float p0 = ex2_approx(fmaf(__uint_as_float(sr[c][i]), c2, neg_m));
-              const float p1 = ex2_approx(fmaf(__uint_as_float(sr[c][i + 1]), c2, neg_m));
-              ls8[(i >> 1) & 7] += p0 + p1;
+              float x0, x1;
+              f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[c][i]), __uint_as_float(sr[c][i + 1])),
+                               c2x2, negm2),
+                        x0, x1);
+              const float p0 = ex2_approx(x0);
+              const float p1 = ex2_approx(x1);
+              ls4[(i >> 1) & 3] = f2_add(ls4[(i >> 1) & 3], f2_pack(p0, p1));
               pk[c2i * 16 + i / 2] = pack_bf16x2(p0, p1);
             }
           }
           tmem_st32(colS + h * 32, pk);
         }
-#pragma unroll
-        for (int w = 4; w > 0; w >>= 1)
-#pragma unroll
-          for (int u = 0; u < w; ++u) ls8[u] += ls8[u + w];
-        l += ls8[0];
+        ls4[0] = f2_add(f2_add(ls4[0], ls4[1]), f2_add(ls4[2], ls4[3]));
+        float lsa, lsb;
+        f2_unpack(ls4[0], lsa, lsb);
+        l += lsa + lsb;
         tmem_wait_st();
         // Correct the O accumulator if this row's reference moved (warp-wide
         // decision: TMEM loads/stores are warp-collective).
