@@ -60,6 +60,9 @@ def bind(path: str):
     lib.oracle_attn_probs.argtypes = [dp, dp, i64, i64, i64, cint, dbl, dp]
     lib.oracle_attn_bwd.argtypes = [dp, dp, dp, dp, i64, i64, i64, cint, dbl,
                                     dp, dp, dp]
+    lib.oracle_attn_fwd_gqa.argtypes = [dp, dp, dp, i64, i64, i64, i64, i64, i64, cint, dbl,
+                                        dp, dp]
+    lib.oracle_combine_splits.argtypes = [dp, dp, i64, i64, i64, dp, dp]
     lib.oracle_fwd_flops.argtypes = [i64, i64, i64, cint]
     lib.oracle_fwd_flops.restype = dbl
     lib.oracle_recompute_flops.argtypes = [i64, i64]
@@ -68,6 +71,7 @@ def bind(path: str):
     lib.oracle_set_num_threads.argtypes = [cint]
     for f in (lib.oracle_attn_fwd, lib.oracle_attn_fwd_rows,
               lib.oracle_attn_probs, lib.oracle_attn_bwd,
+              lib.oracle_attn_fwd_gqa, lib.oracle_combine_splits,
               lib.oracle_set_num_threads):
         f.restype = None
     return lib
@@ -165,6 +169,35 @@ def attn_bwd(q, k, v, dout, causal: bool, scale: float, lib=None):
     (lib or _load()).oracle_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), B * H, N, d,
                             int(bool(causal)), float(scale), _ptr(dq), _ptr(dk), _ptr(dv))
     return dq, dk, dv
+
+
+def attn_fwd_gqa(q, k, v, causal: bool, scale: float, lib=None):
+    """General forward: q (B, Hq, Nq, d), k and v (B, Hkv, Nkv, d), Hq a
+    multiple of Hkv; causal is aligned bottom-right.  Returns (o, lse)."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, Hq, Nq, d = _shape4(q)
+    Bk, Hkv, Nkv, dk = _shape4(k)
+    if Bk != B or dk != d or v.shape != k.shape or Hkv < 1 or Hq % Hkv:
+        raise ValueError("incompatible q / k / v shapes")
+    o = np.zeros((B, Hq, Nq, d))
+    lse = np.zeros((B, Hq, Nq))
+    (lib or _load()).oracle_attn_fwd_gqa(_ptr(q), _ptr(k), _ptr(v), B, Hq, Hkv, Nq, Nkv, d,
+                                         int(bool(causal)), float(scale), _ptr(o), _ptr(lse))
+    return o, lse
+
+
+def combine_splits(o_parts, lse_parts, lib=None):
+    """Merge partial (O_s, lse_s) over key ranges: o_parts (S, ..., d),
+    lse_parts (S, ...).  Returns (o, lse) with the trailing shapes."""
+    o_parts, lse_parts = _f64(o_parts), _f64(lse_parts)
+    S = o_parts.shape[0]
+    d = o_parts.shape[-1]
+    R = int(np.prod(o_parts.shape[1:-1]))
+    o = np.zeros(o_parts.shape[1:])
+    lse = np.zeros(lse_parts.shape[1:])
+    (lib or _load()).oracle_combine_splits(_ptr(o_parts), _ptr(lse_parts), S, R, d, _ptr(o),
+                                           _ptr(lse))
+    return o, lse
 
 
 def fwd_flops(B: int, H: int, N: int, d: int, causal: bool) -> float:

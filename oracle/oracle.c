@@ -39,10 +39,23 @@
  *   lse receives no upstream gradient.
  *
  * Layout: every tensor is a dense row-major fp64 array [BH][N][d] (lse and
- * D are [BH][N]).  Loops are parallelised with OpenMP over independent rows
- * (forward, dQ) or independent key rows (dK, dV); each output element is
- * computed by one thread with a plain sequential sum, so results do not
- * depend on the thread count.
+ * D are [BH][N]).
+ *
+ * General form (oracle_attn_fwd_gqa): N_q query rows per head against N_kv
+ * keys, and H_q query heads sharing H_kv key/value heads in groups of
+ * G = H_q / H_kv (query head h reads key/value head h / G).  The causal
+ * mask is aligned bottom-right: query i is the (N_kv - N_q + i)-th position
+ * of the key sequence and attends to keys j <= i + N_kv - N_q, which is the
+ * square top-left mask when N_q = N_kv.  A row with no key has O = 0 and
+ * lse = -inf.  The split-KV combine of cs2680 Lecture 9 sec. 9.8 merges
+ * partial results (O_s, lse_s) over key ranges s by the same rescaling as
+ * sec. 9.4: lse = ln sum_s exp(lse_s), O = sum_s exp(lse_s - lse) O_s
+ * (oracle_combine_splits).
+ *
+ * Loops are parallelised with OpenMP over independent rows (forward, dQ) or
+ * independent key rows (dK, dV); each output element is computed by one
+ * thread with a plain sequential sum, so results do not depend on the thread
+ * count.
  */
 #include <math.h>
 #include <stdint.h>
@@ -263,4 +276,71 @@ double oracle_fwd_flops(int64_t BH, int64_t N, int64_t d, int causal)
 double oracle_recompute_flops(int64_t N, int64_t d)
 {
     return 2.0 * (double)N * (double)N * (double)d;
+}
+
+/* General forward (see the header): q, o are [B][Hq][Nq][d], k, v are
+ * [B][Hkv][Nkv][d], lse is [B][Hq][Nq]. */
+void oracle_attn_fwd_gqa(const double* q, const double* k, const double* v, int64_t B,
+                         int64_t Hq, int64_t Hkv, int64_t Nq, int64_t Nkv, int64_t d, int causal,
+                         double scale, double* o, double* lse)
+{
+    const int64_t G = Hq / Hkv;
+#pragma omp parallel
+    {
+        double* s = (double*)malloc(sizeof(double) * (size_t)(Nkv > 0 ? Nkv : 1));
+#pragma omp for schedule(dynamic, 16)
+        for (int64_t r = 0; r < B * Hq * Nq; ++r) {
+            const int64_t b = r / (Hq * Nq), h = (r / Nq) % Hq, i = r % Nq;
+            const int64_t hk = h / G;
+            const double* qi = q + r * d;
+            const double* kh = k + (b * Hkv + hk) * Nkv * d;
+            const double* vh = v + (b * Hkv + hk) * Nkv * d;
+            int64_t len = Nkv;
+            if (causal) {
+                int64_t lim = i + Nkv - Nq + 1;  /* keys j < lim are visible */
+                len = lim < 0 ? 0 : (lim < Nkv ? lim : Nkv);
+            }
+            double* orow = o + r * d;
+            for (int64_t c = 0; c < d; ++c) orow[c] = 0.0;
+            if (len == 0) { lse[r] = -INFINITY; continue; }
+            for (int64_t j = 0; j < len; ++j) {
+                const double* kj = kh + j * d;
+                double acc = 0.0;
+                for (int64_t c = 0; c < d; ++c) acc += qi[c] * kj[c];
+                s[j] = scale * acc;
+            }
+            const double l = logsumexp_row(s, len);
+            lse[r] = l;
+            for (int64_t j = 0; j < len; ++j) {
+                const double a = exp(s[j] - l);
+                const double* vj = vh + j * d;
+                for (int64_t c = 0; c < d; ++c) orow[c] += a * vj[c];
+            }
+        }
+        free(s);
+    }
+}
+
+/* Merge S partial results over disjoint key ranges: o_parts is [S][R][d],
+ * lse_parts is [S][R] (a part with no key has lse = -inf and is ignored). */
+void oracle_combine_splits(const double* o_parts, const double* lse_parts, int64_t S, int64_t R,
+                           int64_t d, double* o, double* lse)
+{
+    for (int64_t r = 0; r < R; ++r) {
+        double m = -INFINITY;
+        for (int64_t t = 0; t < S; ++t) if (lse_parts[t * R + r] > m) m = lse_parts[t * R + r];
+        double* orow = o + r * d;
+        for (int64_t c = 0; c < d; ++c) orow[c] = 0.0;
+        if (m == -INFINITY) { lse[r] = -INFINITY; continue; }
+        double sum = 0.0;
+        for (int64_t t = 0; t < S; ++t) sum += exp(lse_parts[t * R + r] - m);
+        const double l = m + log(sum);
+        lse[r] = l;
+        for (int64_t t = 0; t < S; ++t) {
+            const double w = exp(lse_parts[t * R + r] - l);
+            if (w == 0.0) continue;
+            const double* part = o_parts + (t * R + r) * d;
+            for (int64_t c = 0; c < d; ++c) orow[c] += w * part[c];
+        }
+    }
 }

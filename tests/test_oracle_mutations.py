@@ -19,7 +19,14 @@ import oracle
 SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.c")
 
 MUTATIONS = {
-    "scores_drop_scale": ("s[j] = scale * acc;", "s[j] = acc;"),
+    "scores_drop_scale": ("        s[j] = scale * acc;\n    }\n    return len;",
+                          "        s[j] = acc;\n    }\n    return len;"),
+    "gqa_wrong_kv_head": ("const int64_t hk = h / G;", "const int64_t hk = h % Hkv;"),
+    "gqa_causal_top_left": ("int64_t lim = i + Nkv - Nq + 1;", "int64_t lim = i + 1;"),
+    "gqa_drop_scale": ("                s[j] = scale * acc;", "                s[j] = acc;"),
+    "combine_unweighted": ("const double w = exp(lse_parts[t * R + r] - l);",
+                           "const double w = 1.0 / (double)S;"),
+    "combine_lse_no_max": ("const double l = m + log(sum);", "const double l = log(sum);"),
     "lse_drop_max": ("return m + log(l);", "return log(l);"),
     "causal_off_by_one": ("return causal ? (i + 1 < N ? i + 1 : N) : N;",
                           "return causal ? (i < N ? i : N) : N;"),
@@ -79,6 +86,26 @@ def battery(lib):
     o, lse = oracle.attn_fwd(q, k, v, True, scale, lib=lib)
     if np.abs(o[:, :, 0] - v[:, :, 0]).max() > 1e-15:
         failed.append("causal_row0")
+    # general form: GQA + bottom-right causal against torch, and the combine
+    Hq, Hkv, Nq, Nkv = 4, 2, 3, 11
+    gq, gk, gv = rnd((1, Hq, Nq, d), 20), rnd((1, Hkv, Nkv, d), 21), rnd((1, Hkv, Nkv, d), 22)
+    for causal in (False, True):
+        i = np.arange(Nq)[:, None]
+        j = np.arange(Nkv)[None, :]
+        mask = torch.tensor(j <= i + Nkv - Nq) if causal else None
+        ref = torch.nn.functional.scaled_dot_product_attention(
+            torch.tensor(gq), torch.tensor(gk), torch.tensor(gv), attn_mask=mask, scale=scale,
+            enable_gqa=True).numpy()
+        go, _ = oracle.attn_fwd_gqa(gq, gk, gv, causal, scale, lib=lib)
+        if np.abs(go - ref).max() > 1e-12:
+            failed.append("gqa_sdpa_%d" % causal)
+    parts = [oracle.attn_fwd_gqa(gq, gk[:, :, a:b], gv[:, :, a:b], False, scale, lib=lib)
+             for a, b in ((0, 4), (4, 11))]
+    co, clse = oracle.combine_splits(np.stack([p[0] for p in parts]), np.stack([p[1] for p in parts]),
+                                     lib=lib)
+    fo, flse = oracle.attn_fwd_gqa(gq, gk, gv, False, scale, lib=lib)
+    if np.abs(co - fo).max() > 1e-12 or np.abs(clse - flse).max() > 1e-12:
+        failed.append("combine")
     o, lse = oracle.attn_fwd(q, k, v, False, 0.0, lib=lib)
     if np.abs(o - v.mean(2, keepdims=True)).max() > 1e-12 or np.abs(lse - math.log(N)).max() > 1e-12:
         failed.append("scale0")
