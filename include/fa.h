@@ -68,6 +68,40 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
            int N, int d, int causal, float scale, void* stream);
 
 /*
+ * General forward pass: grouped query heads, N_q != N_kv, key splits.
+ *   q, o   : [B][Hq][Nq][d] bf16 (o written); lse : [B][Hq][Nq] fp32 (written).
+ *   k, v   : [B][Hkv][Nkv][d] bf16; Hq is a multiple of Hkv and query head h
+ *            reads key/value head h / (Hq / Hkv) (GQA; MQA when Hkv = 1).
+ *   causal : aligned bottom-right: query i sees keys j <= i + Nkv - Nq (the
+ *            square top-left mask when Nq = Nkv); a query row that sees no
+ *            key gets O = 0 and lse = -inf.
+ *   num_splits >= 1: the keys are cut into that many ranges of whole
+ *            128-key tiles (fewer if there are fewer tiles), processed in
+ *            parallel and merged by their logsumexp -- the split-KV
+ *            ("Flash-Decoding") scheme of cs2680 Lecture 9 sec. 9.8 and the
+ *            CMU post's slide page 58, for short queries over long keys.
+ *   workspace: with more than one effective split, a device buffer of at
+ *            least fa_fwd_gqa_workspace_size(...) bytes, 256-byte aligned
+ *            (per-split fp32 O and lse); otherwise it may be NULL.
+ * The query heads of one key/value head are packed into the same 128-row
+ * tiles (CMU post, slide page 59).  fa_fwd(...) is
+ * fa_fwd_gqa(..., H, H, N, N, ..., 1, NULL, 0, stream).
+ */
+int fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+               int Hkv, int Nq, int Nkv, int d, int causal, float scale, int num_splits,
+               void* workspace, size_t workspace_bytes, void* stream);
+
+/* Workspace bytes fa_fwd_gqa needs for these sizes and splits (0 when the
+ * effective number of splits is 1 or the sizes are invalid). */
+size_t fa_fwd_gqa_workspace_size(int B, int Hq, int Hkv, int Nq, int Nkv, int d, int num_splits);
+
+/* A number of key splits that fills `sm_count` SMs for these sizes: 1 when
+ * the (key/value head, query-row pair) items already do, else enough splits
+ * of at least two 128-key tiles each.  Host only; negative FA_ERR_* on bad
+ * arguments. */
+int fa_fwd_gqa_splits(int B, int Hq, int Hkv, int Nq, int Nkv, int d, int causal, int sm_count);
+
+/*
  * Bytes of device workspace fa_bwd needs for these sizes: an fp32 dQ
  * accumulator of B*H*ceil(N/128)*128*d floats, then two per-row fp32
  * terms of B*H*ceil(N/128)*128 floats each (D_i = sum_k dO_ik O_ik and

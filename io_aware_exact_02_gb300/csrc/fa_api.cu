@@ -105,6 +105,37 @@ int check_shape(int B, int H, int N, int d, float scale) {
   return FA_OK;
 }
 
+// Shape checks and derived sizes of the general forward pass.
+struct GqaShape {
+  int BH, rows, n_kv, n_pairs, splits, tiles_per_split;
+  FwdWorkspace ws;
+};
+
+int gqa_shape(int B, int Hq, int Hkv, int Nq, int Nkv, int d, int num_splits, float scale,
+              GqaShape* g) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || Nq < 1 || Nkv < 1 || num_splits < 1) return FA_ERR_ARG;
+  if (Hq % Hkv != 0) return FA_ERR_ARG;
+  if (!std::isfinite(scale)) return FA_ERR_ARG;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED_D;
+  const long long bh = (long long)B * Hkv;
+  const long long rows = (long long)(Hq / Hkv) * Nq;
+  if (bh > (1LL << 30) || rows > (1LL << 30)) return FA_ERR_ARG;
+  const int n_kv = ceil_div(Nkv, kTile);
+  const int tps = ceil_div(n_kv, num_splits < n_kv ? num_splits : n_kv);
+  const int splits = ceil_div(n_kv, tps);
+  const long long n_pairs = (rows + kPairRows - 1) / kPairRows;
+  if (bh * n_pairs * splits > 0x7fffffffLL) return FA_ERR_ARG;
+  if ((double)splits * (double)bh * (double)rows * (double)d * 4.0 > 9.0e18) return FA_ERR_ARG;
+  g->BH = (int)bh;
+  g->rows = (int)rows;
+  g->n_kv = n_kv;
+  g->n_pairs = (int)n_pairs;
+  g->splits = splits;
+  g->tiles_per_split = tps;
+  g->ws = fwd_workspace_layout(splits, bh, (long long)rows, d);
+  return FA_OK;
+}
+
 }  // namespace
 
 int make_tmap_bhnd(const void* base, int BH, int N, int d, CUtensorMap* out) {
@@ -145,30 +176,72 @@ const char* fa_status_string(int status) {
 
 int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
            int d, int causal, float scale, void* stream) {
+  return fa_fwd_gqa(q, k, v, o, lse, B, H, H, N, N, d, causal, scale, 1, nullptr, 0, stream);
+}
+
+size_t fa_fwd_gqa_workspace_size(int B, int Hq, int Hkv, int Nq, int Nkv, int d, int num_splits) {
+  GqaShape g;
+  if (gqa_shape(B, Hq, Hkv, Nq, Nkv, d, num_splits, 1.0f, &g) != FA_OK) return 0;
+  return g.splits > 1 ? g.ws.total : 0;
+}
+
+int fa_fwd_gqa_splits(int B, int Hq, int Hkv, int Nq, int Nkv, int d, int causal, int sm_count) {
+  GqaShape g;
+  int rc = gqa_shape(B, Hq, Hkv, Nq, Nkv, d, 1, 1.0f, &g);
+  if (rc != FA_OK) return rc;
+  if (sm_count < 1 || (causal != 0 && causal != 1)) return FA_ERR_ARG;
+  // Split the keys only when the (K/V head, row pair) items cannot fill the
+  // SMs, keeping at least two 128-key tiles per split.
+  const long long items = (long long)g.BH * g.n_pairs;
+  if (items >= sm_count) return 1;
+  long long splits = (sm_count + items - 1) / items;
+  const int max_splits = g.n_kv / 2 > 1 ? g.n_kv / 2 : 1;
+  if (splits > max_splits) splits = max_splits;
+  if (splits > 256) splits = 256;
+  return (int)splits;
+}
+
+int fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+               int Hkv, int Nq, int Nkv, int d, int causal, float scale, int num_splits,
+               void* workspace, size_t workspace_bytes, void* stream) {
   if (!q || !k || !v || !o || !lse) return FA_ERR_ARG;
   if (causal != 0 && causal != 1) return FA_ERR_ARG;
-  int rc = check_shape(B, H, N, d, scale);
+  GqaShape g;
+  int rc = gqa_shape(B, Hq, Hkv, Nq, Nkv, d, num_splits, scale, &g);
   if (rc != FA_OK) return rc;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
     return FA_ERR_ALIGN;
+  if (g.splits > 1 && (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
+                       workspace_bytes < g.ws.total))
+    return FA_ERR_WORKSPACE;
   DeviceState* ds;
   if ((rc = device_state(&ds)) != FA_OK) return rc;
-  const int BH = B * H;
   CUtensorMap tq, tk, tv;
-  if ((rc = make_tmap_bhnd(q, BH, N, d, &tq)) != FA_OK) return rc;
-  if ((rc = make_tmap_bhnd(k, BH, N, d, &tk)) != FA_OK) return rc;
-  if ((rc = make_tmap_bhnd(v, BH, N, d, &tv)) != FA_OK) return rc;
+  if ((rc = make_tmap_bhnd(q, g.BH, g.rows, d, &tq)) != FA_OK) return rc;
+  if ((rc = make_tmap_bhnd(k, g.BH, Nkv, d, &tk)) != FA_OK) return rc;
+  if ((rc = make_tmap_bhnd(v, g.BH, Nkv, d, &tv)) != FA_OK) return rc;
   FwdParams p;
   p.o = o;
   p.lse = lse;
+  p.o_part = nullptr;
+  p.lse_part = nullptr;
+  if (g.splits > 1) {
+    p.o_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + g.ws.o_part);
+    p.lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + g.ws.lse_part);
+  }
   p.status = ds->status;
-  p.BH = BH;
-  p.N = N;
-  p.n_kv = ceil_div(N, kTile);
-  p.n_pairs = ceil_div(N, kPairRows);
+  p.BH = g.BH;
+  p.rows = g.rows;
+  p.Nq = Nq;
+  p.Nkv = Nkv;
+  p.causal_off = Nkv - Nq;
+  p.n_kv = g.n_kv;
+  p.n_pairs = g.n_pairs;
+  p.splits = g.splits;
+  p.tiles_per_split = g.tiles_per_split;
   p.causal = causal;
   p.scale_log2 = scale * 1.4426950408889634f;
-  p.grid = fwd_grid(BH, p.n_pairs, causal, ds->sm_count);
+  p.grid = fwd_grid(g.BH, g.n_pairs * g.splits, causal, ds->sm_count);
   return launch_fwd(tq, tk, tv, p, d, static_cast<cudaStream_t>(stream));
 }
 

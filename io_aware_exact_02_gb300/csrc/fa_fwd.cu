@@ -100,7 +100,9 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
 
 // kNeg: the scale is negative, so the tile's extreme is a minimum of the raw
 // scores (the exponent scale * s is largest where s is smallest).
-template <int D, bool kNeg>
+// kGeneral: grouped heads, N_q != N_kv or key splits; without it the kernel
+// is the square case (rows = N_q = N_kv, one split) in its simplest form.
+template <int D, bool kNeg, bool kGeneral>
 __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, const FwdParams p) {
@@ -141,22 +143,41 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
 
   // Persistent CTAs: CTA c takes the work items of the longest-first list
   // in "snake" order -- items c, 2G-1-c, 2G+c, 4G-1-c, ... for G CTAs -- so
-  // that every CTA gets a similar mix of long and short items.
-  const int num_items = p.BH * p.n_pairs;
+  // that every CTA gets a similar mix of long and short items.  With one CTA
+  // per item (G = items) each CTA takes exactly item c.
+  const int splits = kGeneral ? p.splits : 1;
+  const int num_items = p.BH * p.n_pairs * splits;
   const int G = gridDim.x;
   auto item_of_round = [&](int k) -> int {
     const int base = k * G;
     return (k & 1) ? base + (G - 1 - (int)blockIdx.x) : base + (int)blockIdx.x;
   };
+  // An item: K/V head bh, pair `pair` of its packed query rows, key split.
+  // Q tile t's rows see key tiles [j0, j0 + n_t[t]) of the split.
   struct Item {
-    int bh, pair, row0, n_t0, n_t1;
+    int bh, pair, split, row0, j0, n_t[2], nmax;
   };
   auto decode = [&](int idx) -> Item {
     Item it;
-    fwd_item(idx, p.BH, p.n_pairs, &it.bh, &it.pair);
+    it.split = idx % splits;
+    fwd_item(idx / splits, p.BH, p.n_pairs, &it.bh, &it.pair);
     it.row0 = it.pair * kPairRows;
-    it.n_t0 = fwd_kv_tiles(2 * it.pair, p.n_kv, p.causal);
-    it.n_t1 = fwd_kv_tiles(2 * it.pair + 1, p.n_kv, p.causal);  // n_t0 <= n_t1 <= n_t0 + 1
+    it.j0 = it.split * p.tiles_per_split;
+    const int j1 = min(it.j0 + p.tiles_per_split, p.n_kv);
+    it.nmax = 0;
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+      const int r0 = it.row0 + t * kTile;
+      int hi;
+      if (kGeneral) {
+        hi = fwd_tile_key_tiles(r0, p);
+      } else {  // rows = N_kv: the causal tile r0/128 ends on the diagonal
+        hi = r0 >= p.rows ? 0 : (p.causal ? min(r0 / kTile + 1, p.n_kv) : p.n_kv);
+      }
+      const int n = min(hi, j1) - it.j0;
+      it.n_t[t] = n > 0 ? n : 0;
+      it.nmax = max(it.nmax, it.n_t[t]);
+    }
     return it;
   };
 
@@ -173,6 +194,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
         const int idx = item_of_round(k);
         if (idx >= num_items) continue;
         const Item it = decode(idx);
+        if (it.nmax == 0) continue;  // no key visible to any row of the item
         if (q_issued > 0 &&
             !mbar_wait(&sm.q_empty, (q_issued - 1) & 1, p.status, abortf, kSiteQEmpty)) {
           ok = false;
@@ -183,7 +205,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
           for (int h = 0; h < D / 64; ++h)
             tma_load_3d(sm.q[t] + h * 16384, &tq, &sm.q_full, h * 64, it.row0 + t * kTile, it.bh);
         ++q_issued;
-        for (int j = 0; j < it.n_t1 && ok; ++j) {
+        for (int j = 0; j < it.nmax && ok; ++j) {
           for (int w = 0; w < 2 && ok; ++w, ++c) {
             const int slot = c % S, use = c / S;
             if (use > 0 &&
@@ -194,7 +216,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
             mbar_arrive_expect_tx(&sm.kv_full[slot], Cfg::kTileBytes);
             for (int h = 0; h < D / 64; ++h)
               tma_load_3d(sm.kv[slot] + h * 16384, w == 0 ? &tk : &tv, &sm.kv_full[slot], h * 64,
-                          j * kTile, it.bh);
+                          (it.j0 + j) * kTile, it.bh);
           }
         }
       }
@@ -213,7 +235,8 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
       const uint32_t q_addr[2] = {smem_u32(sm.q[0]), smem_u32(sm.q[1])};
       uint32_t p_par[2] = {0, 0};
       int cb = 0;       // K/V loads consumed before the current item
-      int n_done = 0;   // items finished by this CTA
+      int n_done = 0;   // items finished by this CTA (o_full / o_empty phases)
+      int q_used = 0;   // items that loaded Q (q_full / q_empty phases)
       bool ok = true;
 
       auto issue_s = [&](int t, int kslot) {
@@ -252,62 +275,61 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
         const int idx = item_of_round(k);
         if (idx >= num_items) continue;
         const Item it = decode(idx);
-        const int n_t0 = it.n_t0, n_t1 = it.n_t1;
-        ok = mbar_wait(&sm.q_full, n_done & 1, p.status, abortf, kSiteQFull);
+        const int nmax = it.nmax;
+        // A Q tile without keys is final at once (its rows get O = 0).
+        for (int t = 0; t < 2; ++t)
+          if (it.n_t[t] == 0) tc_commit(&sm.o_full[t]);
+        if (nmax == 0) {
+          ++n_done;
+          continue;
+        }
+        ok = mbar_wait(&sm.q_full, q_used & 1, p.status, abortf, kSiteQFull);
         if (ok) ok = wait_full(cb);
         if (ok) {
           tc_fence_after();
-          issue_s(0, cb % S);
-          issue_s(1, cb % S);
+          for (int t = 0; t < 2; ++t)
+            if (it.n_t[t] > 0) issue_s(t, cb % S);
           tc_commit(&sm.kv_empty[cb % S]);
-          if (n_t1 == 1) tc_commit(&sm.q_empty);
+          if (nmax == 1) tc_commit(&sm.q_empty);
         }
-        for (int j = 1; j < n_t1 && ok; ++j) {
+        // Key tile j: PV_t(j-1) then S_t(j) for each Q tile that has them.
+        for (int j = 1; j < nmax && ok; ++j) {
           const int kc = cb + 2 * j, vc = cb + 2 * j - 1;
           ok = wait_full(kc) && wait_full(vc);
           if (!ok) break;
-          ok = wait_p(0);
-          if (!ok) break;
-          tc_fence_after();
-          ok = issue_pv(0, vc % S, j - 1 > 0);
-          if (!ok) break;
-          if (j < n_t0) {
-            issue_s(0, kc % S);
-          } else {
-            tc_commit(&sm.o_full[0]);  // tile 0 has no more keys (causal)
-          }
-          ok = wait_p(1);
-          if (!ok) break;
-          tc_fence_after();
-          ok = issue_pv(1, vc % S, j - 1 > 0);
-          if (!ok) break;
-          tc_commit(&sm.kv_empty[vc % S]);
-          issue_s(1, kc % S);
-          tc_commit(&sm.kv_empty[kc % S]);
-          if (j == n_t1 - 1) tc_commit(&sm.q_empty);  // last product reading Q
-        }
-        if (ok) {
-          const int vc = cb + 2 * n_t1 - 1;
-          ok = wait_full(vc);
-          if (ok && n_t0 == n_t1) {
-            ok = wait_p(0);
-            if (ok) {
-              tc_fence_after();
-              ok = issue_pv(0, vc % S, n_t1 - 1 > 0);
-              if (ok) tc_commit(&sm.o_full[0]);
+          for (int t = 0; t < 2 && ok; ++t) {
+            if (j - 1 >= it.n_t[t]) continue;
+            ok = wait_p(t);
+            if (!ok) break;
+            tc_fence_after();
+            ok = issue_pv(t, vc % S, j - 1 > 0);
+            if (!ok) break;
+            if (j < it.n_t[t]) {
+              issue_s(t, kc % S);
+            } else {
+              tc_commit(&sm.o_full[t]);  // tile t has no more keys
             }
           }
-          if (ok) ok = wait_p(1);
-          if (ok) {
-            tc_fence_after();
-            ok = issue_pv(1, vc % S, n_t1 - 1 > 0);
-          }
-          if (ok) {
-            tc_commit(&sm.o_full[1]);
-            tc_commit(&sm.kv_empty[vc % S]);
-          }
+          if (!ok) break;
+          tc_commit(&sm.kv_empty[vc % S]);
+          tc_commit(&sm.kv_empty[kc % S]);
+          if (j == nmax - 1) tc_commit(&sm.q_empty);  // last product reading Q
         }
-        cb += 2 * n_t1;
+        if (ok) {
+          const int vc = cb + 2 * nmax - 1;
+          ok = wait_full(vc);
+          for (int t = 0; t < 2 && ok; ++t) {
+            if (it.n_t[t] != nmax) continue;
+            ok = wait_p(t);
+            if (!ok) break;
+            tc_fence_after();
+            ok = issue_pv(t, vc % S, nmax - 1 > 0);
+            if (ok) tc_commit(&sm.o_full[t]);
+          }
+          if (ok) tc_commit(&sm.kv_empty[vc % S]);
+        }
+        cb += 2 * nmax;
+        ++q_used;
         ++n_done;
       }
       // Every MMA issued so far must finish before TMEM is released.
@@ -324,6 +346,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
     // A masked score is replaced by the value that loses every max (min)
     // and whose exponent c2 * s is -inf, so its probability is exactly 0.
     const float neutral = kNeg ? __int_as_float(0x7f800000) : __int_as_float(0xff800000);
+    const float ninf = __int_as_float(0xff800000);
     const uint32_t colS = tmem + lane_base + Cfg::col_s(t);
     const uint32_t colO = tmem + lane_base + Cfg::col_o(t);
     uint32_t s_par = 0;
@@ -335,12 +358,16 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
       if (idx >= num_items) continue;
       const Item item = decode(idx);
       const int bh = item.bh;
-      const int n_t = t == 0 ? item.n_t0 : item.n_t1;
-      const int R = item.row0 + t * kTile + r;  // global query row
-      const int diag_tile = p.causal ? (item.row0 + t * kTile) / kTile : -1;
-      float m_ref = __int_as_float(0xff800000);  // -inf
+      const int n_t = item.n_t[t];
+      const int R = item.row0 + t * kTile + r;  // packed query row of this K/V head
+      // Keys visible to this row: [0, lim) (bottom-right causal alignment).
+      int lim = p.Nkv;
+      if (p.causal)
+        lim = kGeneral ? min(max(R % p.Nq + p.causal_off + 1, 0), p.Nkv) : min(R + 1, p.Nkv);
+      float m_ref = ninf;
       float l = 0.f;
       for (int j = 0; j < n_t; ++j) {
+        const int jj = item.j0 + j;  // key tile
         ok = mbar_wait(&sm.s_full[t], s_par, p.status, abortf, kSiteSFull);
         ok = __all_sync(0xffffffffu, ok);  // keep the warp's collective TMEM ops converged
         s_par ^= 1;
@@ -352,16 +379,14 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
 #pragma unroll
         for (int c = 0; c < 4; ++c) tmem_wait_ld(sr[c]);
 
-        const bool need_mask = (j + 1) * kTile > p.N || j == diag_tile;
-        if (need_mask) {
-          // Keys at columns >= lim of this tile are masked for this row.
-          int lim = p.N - j * kTile;
-          if (p.causal && R + 1 - j * kTile < lim) lim = R + 1 - j * kTile;
+        if ((jj + 1) * kTile > lim) {
+          // Keys at columns >= tlim of this tile are masked for this row.
+          const int tlim = lim - jj * kTile;
 #pragma unroll
           for (int c = 0; c < 4; ++c)
 #pragma unroll
             for (int i = 0; i < 32; ++i)
-              if (c * 32 + i >= lim) sr[c][i] = __float_as_uint(neutral);
+              if (c * 32 + i >= tlim) sr[c][i] = __float_as_uint(neutral);
         }
         // Tile extreme of the raw scores: eight independent chains of
         // three-input max (min), joined by a tree (exact in any order).
@@ -388,10 +413,12 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
           m_ref = m_tile;
         }
         l *= alpha;
-        // p = 2^(c2 * s - m) for pairs of scores with packed f32x2 FMAs;
-        // four packed partial row sums, joined by a tree below.
+        // p = 2^(c2 * s - m) for pairs of scores with packed f32x2 FMAs (a
+        // row that has seen no key yet keeps m = -inf and all p = 0); four
+        // packed partial row sums, joined by a tree below.
+        const float neg_m = m_ref == ninf ? 0.f : -m_ref;
         const uint64_t c2x2 = f2_pack(c2, c2);
-        const uint64_t negm2 = f2_pack(-m_ref, -m_ref);
+        const uint64_t negm2 = f2_pack(neg_m, neg_m);
         uint64_t ls4[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) ls4[u] = 0;
@@ -441,26 +468,49 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
-      const float inv_l = 1.f / l;
-      __nv_bfloat16* orow_g = reinterpret_cast<__nv_bfloat16*>(p.o) + ((size_t)bh * p.N + R) * D;
+      // Epilogue: O / l (0 for a row that saw no key) and lse; with several
+      // key splits, the split's normalised fp32 O and its lse, for the combine.
+      const bool any = l > 0.f;
+      const float inv_l = any ? 1.f / l : 0.f;
+      const bool valid = R < p.rows;
+      const size_t row_g = (size_t)bh * p.rows + R;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t orow[32];
         tmem_ld32(colO + c * 32, orow);
         tmem_wait_ld(orow);
-        if (R < p.N) {
+        if (!valid) continue;
+        if (splits == 1) {
           uint4 v[4];
           uint32_t* w = reinterpret_cast<uint32_t*>(v);
 #pragma unroll
           for (int i = 0; i < 16; ++i)
-            w[i] = pack_bf16x2(__uint_as_float(orow[2 * i]) * inv_l,
-                               __uint_as_float(orow[2 * i + 1]) * inv_l);
-          uint4* dst = reinterpret_cast<uint4*>(orow_g + c * 32);
+            w[i] = any ? pack_bf16x2(__uint_as_float(orow[2 * i]) * inv_l,
+                                     __uint_as_float(orow[2 * i + 1]) * inv_l)
+                       : 0u;
+          uint4* dst =
+              reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.o) + row_g * D + c * 32);
 #pragma unroll
           for (int i = 0; i < 4; ++i) dst[i] = v[i];
+        } else {
+          float4* dst = reinterpret_cast<float4*>(
+              p.o_part + ((size_t)item.split * p.BH * p.rows + row_g) * D + c * 32);
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            dst[i] = any ? make_float4(__uint_as_float(orow[4 * i]) * inv_l,
+                                       __uint_as_float(orow[4 * i + 1]) * inv_l,
+                                       __uint_as_float(orow[4 * i + 2]) * inv_l,
+                                       __uint_as_float(orow[4 * i + 3]) * inv_l)
+                         : make_float4(0.f, 0.f, 0.f, 0.f);
         }
       }
-      if (R < p.N) p.lse[(size_t)bh * p.N + R] = (m_ref + __log2f(l)) * kLn2;
+      if (valid) {
+        const float lse_row = any ? (m_ref + __log2f(l)) * kLn2 : ninf;
+        if (splits == 1)
+          p.lse[row_g] = lse_row;
+        else
+          p.lse_part[(size_t)item.split * p.BH * p.rows + row_g] = lse_row;
+      }
       // O_t may now be overwritten by the next item's first product.
       tc_fence_before();
       mbar_arrive(&sm.o_empty[t]);
@@ -476,15 +526,75 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
   }
 }
 
-template <int D, bool kNeg>
+// Merge the key splits of the general forward pass: per row,
+// lse = ln sum_s exp(lse_s) and O = sum_s exp(lse_s - lse) O_s (the split-KV
+// combine of cs2680 Lecture 9 sec. 9.8, the rescaling of sec. 9.4).  One
+// warp per row; lane l owns the d/32 consecutive columns starting at
+// l * d/32.
+template <int D>
+__global__ void __launch_bounds__(256) fa_combine_kernel(const FwdParams p) {
+  constexpr int kPer = D / 32;  // 4 or 2 columns per lane
+  const long long row = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  const long long rows_total = (long long)p.BH * p.rows;
+  if (row >= rows_total) return;
+  const float ninf = __int_as_float(0xff800000);
+  constexpr float kL2e = 1.4426950408889634f;
+  float m = ninf;
+  for (int s = 0; s < p.splits; ++s) m = fmaxf(m, p.lse_part[s * rows_total + row]);
+  float acc[kPer];
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) acc[i] = 0.f;
+  float lse_row = ninf;
+  if (m != ninf) {
+    float sum = 0.f;
+    for (int s = 0; s < p.splits; ++s) sum += exp2f((p.lse_part[s * rows_total + row] - m) * kL2e);
+    lse_row = m + logf(sum);
+    for (int s = 0; s < p.splits; ++s) {
+      const float w = exp2f((p.lse_part[s * rows_total + row] - lse_row) * kL2e);
+      if (w == 0.f) continue;
+      const float* src = p.o_part + (s * rows_total + row) * D + lane * kPer;
+      if (kPer == 4) {
+        const float4 v = *reinterpret_cast<const float4*>(src);
+        acc[0] += w * v.x;
+        acc[1] += w * v.y;
+        acc[kPer - 2] += w * v.z;
+        acc[kPer - 1] += w * v.w;
+      } else {
+        const float2 v = *reinterpret_cast<const float2*>(src);
+        acc[0] += w * v.x;
+        acc[1] += w * v.y;
+      }
+    }
+  }
+  __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.o) + (size_t)row * D + lane * kPer;
+  if (kPer == 4) {
+    uint2 out;
+    out.x = pack_bf16x2(acc[0], acc[1]);
+    out.y = pack_bf16x2(acc[kPer - 2], acc[kPer - 1]);
+    *reinterpret_cast<uint2*>(dst) = out;
+  } else {
+    *reinterpret_cast<uint32_t*>(dst) = pack_bf16x2(acc[0], acc[1]);
+  }
+  if (lane == 0) p.lse[row] = lse_row;
+}
+
+template <int D, bool kNeg, bool kGeneral>
 int launch_fwd_dn(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                   const FwdParams& p, cudaStream_t stream) {
   const size_t smem = sizeof(FwdSmem<D>) + 1024;
-  if (cudaFuncSetAttribute(fa_fwd_kernel<D, kNeg>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)smem) != cudaSuccess)
+  if (cudaFuncSetAttribute(fa_fwd_kernel<D, kNeg, kGeneral>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return FA_ERR_LAUNCH;
-  fa_fwd_kernel<D, kNeg><<<(unsigned)p.grid, FwdCfg<D>::kThreads, smem, stream>>>(tq, tk, tv, p);
-  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+  fa_fwd_kernel<D, kNeg, kGeneral>
+      <<<(unsigned)p.grid, FwdCfg<D>::kThreads, smem, stream>>>(tq, tk, tv, p);
+  if (cudaGetLastError() != cudaSuccess) return FA_ERR_LAUNCH;
+  if (p.splits > 1) {
+    const long long threads = (long long)p.BH * p.rows * 32;
+    fa_combine_kernel<D><<<(unsigned)((threads + 255) / 256), 256, 0, stream>>>(p);
+    if (cudaGetLastError() != cudaSuccess) return FA_ERR_LAUNCH;
+  }
+  return FA_OK;
 }
 
 template <int D>
@@ -493,8 +603,13 @@ int launch_fwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap
   // A zero scale makes every unmasked probability equal; it runs as the
   // smallest normal positive scale, whose exponents round to exactly 0.
   if (p.scale_log2 == 0.f) p.scale_log2 = 1.17549435e-38f;
-  if (p.scale_log2 < 0.f) return launch_fwd_dn<D, true>(tq, tk, tv, p, stream);
-  return launch_fwd_dn<D, false>(tq, tk, tv, p, stream);
+  const bool general = p.splits > 1 || p.Nq != p.rows || p.Nkv != p.rows;
+  if (general) {
+    if (p.scale_log2 < 0.f) return launch_fwd_dn<D, true, true>(tq, tk, tv, p, stream);
+    return launch_fwd_dn<D, false, true>(tq, tk, tv, p, stream);
+  }
+  if (p.scale_log2 < 0.f) return launch_fwd_dn<D, true, false>(tq, tk, tv, p, stream);
+  return launch_fwd_dn<D, false, false>(tq, tk, tv, p, stream);
 }
 
 }  // namespace

@@ -37,17 +37,45 @@ __host__ __device__ inline void fwd_item(int t, int BH, int n_pairs, int* bh, in
   *bh = g * kHeadGroup + idx % gsize;
 }
 
+// Forward parameters.  The general form has H_q query heads sharing H_kv
+// K/V heads in groups of G = H_q / H_kv; the G * N_q query rows of one K/V
+// head are contiguous in a [B][H_q][N_q][d] array, so the kernel treats them
+// as one packed row space of `rows` rows per K/V head.  Row r is query
+// position r % N_q.  The square entry point is G = 1, N_q = N_kv = N.
 struct FwdParams {
-  void* o;          // [BH][N][d] bf16
-  float* lse;       // [BH][N] fp32
-  int* status;      // device status word (2 ints: code, site)
-  int BH, N;
-  int n_kv;         // ceil(N / 128)
-  int n_pairs;      // ceil(N / 256)
+  void* o;           // [BH][rows][d] bf16
+  float* lse;        // [BH][rows] fp32
+  float* o_part;     // splits > 1: [splits][BH][rows][d] fp32, each split's O
+  float* lse_part;   // splits > 1: [splits][BH][rows] fp32, each split's lse
+  int* status;       // device status word (2 ints: code, site)
+  int BH;            // B * H_kv
+  int rows;          // packed query rows per K/V head: G * N_q
+  int Nq;            // query positions per query head
+  int Nkv;           // keys per K/V head
+  int causal_off;    // N_kv - N_q: query i sees keys j <= i + causal_off
+  int n_kv;          // ceil(N_kv / 128)
+  int n_pairs;       // ceil(rows / 256)
+  int splits;        // key splits (1: O and lse written directly)
+  int tiles_per_split;
   int causal;
   float scale_log2;  // scale * log2(e)
-  int grid;          // persistent CTAs: min(work items, SMs)
+  int grid;          // CTAs launched
 };
+
+// Number of 128-key tiles, counted from key 0, that the query rows
+// [r0, min(r0 + 128, rows)) of a K/V head need: all of them without a mask,
+// else up to the last key visible to the row with the largest position.
+__host__ __device__ inline int fwd_tile_key_tiles(int r0, const FwdParams& p) {
+  if (r0 >= p.rows) return 0;
+  if (!p.causal) return p.n_kv;
+  const int len = (r0 + kTile < p.rows ? r0 + kTile : p.rows) - r0;
+  const int i0 = r0 % p.Nq;
+  const int maxi = (i0 + len - 1 >= p.Nq) ? p.Nq - 1 : i0 + len - 1;
+  long long lim = (long long)maxi + p.causal_off + 1;
+  if (lim <= 0) return 0;
+  if (lim > p.Nkv) lim = p.Nkv;
+  return ceil_div((int)lim, kTile);
+}
 
 // CTA that runs work item `idx` of a longest-first list on `ctas` persistent
 // CTAs: round k = idx / ctas is taken in order when k is even and in
@@ -94,6 +122,20 @@ int make_tmap_bhnd(const void* base, int BH, int N, int d, CUtensorMap* out);
 
 int launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                const FwdParams& p, int d, cudaStream_t stream);
+
+// Byte offsets of the general forward pass's split workspace: each split's
+// fp32 O, then each split's lse, 256-byte aligned.
+struct FwdWorkspace {
+  size_t o_part, lse_part, total;
+};
+inline FwdWorkspace fwd_workspace_layout(long long splits, long long BH, long long rows, int d) {
+  auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
+  FwdWorkspace w;
+  w.o_part = 0;
+  w.lse_part = up((size_t)(splits * BH * rows) * (size_t)d * sizeof(float));
+  w.total = w.lse_part + up((size_t)(splits * BH * rows) * sizeof(float));
+  return w;
+}
 
 // Byte offsets of the backward workspace's parts for these sizes:
 // the fp32 dQ accumulator, then D, then lse * log2(e), each 256-byte aligned.

@@ -35,6 +35,10 @@ _vp, _i, _f, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_
 _ip = ctypes.POINTER(ctypes.c_int)
 SIGNATURES = {
     "fa_fwd": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp]),
+    "fa_fwd_gqa": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _f, _i, _vp, _sz,
+                        _vp]),
+    "fa_fwd_gqa_workspace_size": (_sz, [_i, _i, _i, _i, _i, _i, _i]),
+    "fa_fwd_gqa_splits": (_i, [_i, _i, _i, _i, _i, _i, _i, _i]),
     "fa_bwd_workspace_size": (_sz, [_i, _i, _i, _i]),
     "fa_bwd": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f,
                     _vp, _sz, _vp]),
@@ -123,6 +127,51 @@ def fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse
     rc = load().fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
                        B, H, N, d, int(bool(causal)), ctypes.c_float(scale), _stream_of(q))
     _check("fa_fwd", rc)
+    return out, lse
+
+
+def fwd_gqa_splits(B, Hq, Hkv, Nq, Nkv, d, causal=False, sm_count=None) -> int:
+    """Key splits that fill the device's SMs (fa_fwd_gqa_splits)."""
+    if sm_count is None:
+        sm_count = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    n = load().fa_fwd_gqa_splits(B, Hq, Hkv, Nq, Nkv, d, int(bool(causal)), int(sm_count))
+    if n < 0:
+        _check("fa_fwd_gqa_splits", n)
+    return n
+
+
+def fwd_gqa_workspace_size(B, Hq, Hkv, Nq, Nkv, d, num_splits) -> int:
+    return int(load().fa_fwd_gqa_workspace_size(B, Hq, Hkv, Nq, Nkv, d, int(num_splits)))
+
+
+def fwd_gqa(q, k, v, causal: bool = False, scale: float | None = None, num_splits=None,
+            out=None, lse=None, workspace=None):
+    """General forward: q (B, Hq, Nq, d), k and v (B, Hkv, Nkv, d), Hq a
+    multiple of Hkv; causal aligned bottom-right; the keys cut into
+    ``num_splits`` ranges (None: fa_fwd_gqa_splits).  Returns (o, lse)."""
+    B, Hq, Nq, d = q.shape
+    Bk, Hkv, Nkv, dk = k.shape
+    scale = default_scale(d) if scale is None else float(scale)
+    _check_qkv("q", q, (B, Hq, Nq, d))
+    _check_qkv("k", k, (B, Hkv, Nkv, d))
+    _check_qkv("v", v, (B, Hkv, Nkv, d))
+    if num_splits is None:
+        num_splits = fwd_gqa_splits(B, Hq, Hkv, Nq, Nkv, d, causal)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, Hq, Nq), dtype=torch.float32, device=q.device)
+    _check_qkv("out", out, (B, Hq, Nq, d))
+    _check_qkv("lse", lse, (B, Hq, Nq), torch.float32)
+    need = fwd_gqa_workspace_size(B, Hq, Hkv, Nq, Nkv, d, num_splits)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    rc = load().fa_fwd_gqa(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                           lse.data_ptr(), B, Hq, Hkv, Nq, Nkv, d, int(bool(causal)),
+                           ctypes.c_float(scale), int(num_splits), ws_ptr, ws_bytes, _stream_of(q))
+    _check("fa_fwd_gqa", rc)
     return out, lse
 
 

@@ -164,3 +164,35 @@ def test_schedule_covers_every_item_once_longest_first(lib, B, H, N, causal):
         loads_lpt = greedy([c for _, _, c, _ in items], 3)
         loads_fwd = greedy(sorted([c for _, _, c, _ in items]), 3)
         assert max(loads_lpt) <= max(loads_fwd)
+
+
+def test_fwd_gqa_sizes_and_splits(lib):
+    # No workspace with one effective split; otherwise per-split fp32 O and
+    # lse of every packed row, each part rounded up to 256 bytes.
+    assert lib.fa_fwd_gqa_workspace_size(2, 8, 2, 1, 1000, 128, 1) == 0
+    rows = 2 * 2 * 4  # B * Hkv * (G * Nq)
+    up = lambda x: (x + 255) // 256 * 256
+    assert lib.fa_fwd_gqa_workspace_size(2, 8, 2, 1, 1000, 128, 3) == up(3 * rows * 128 * 4) + up(3 * rows * 4)
+    # 1000 keys = 8 tiles: 50 requested splits become 8 (one tile each)
+    assert lib.fa_fwd_gqa_workspace_size(1, 2, 2, 3, 1000, 64, 50) == up(8 * 6 * 64 * 4) + up(8 * 6 * 4)
+    assert lib.fa_fwd_gqa_workspace_size(1, 3, 2, 3, 1000, 64, 2) == 0   # Hq not a multiple
+    assert lib.fa_fwd_gqa_splits(8, 16, 16, 8192, 8192, 128, 0, 152) == 1
+    s = lib.fa_fwd_gqa_splits(1, 8, 1, 1, 32768, 128, 1, 152)
+    assert s == 128  # 1 item; capped at n_kv / 2 = 128 tiles of two
+    assert lib.fa_fwd_gqa_splits(1, 8, 1, 1, 300, 128, 0, 152) == 1
+    assert lib.fa_fwd_gqa_splits(1, 8, 1, 1, 300, 128, 0, 0) == fa.FA_ERR_ARG
+
+
+def test_fwd_gqa_argument_errors_launch_nothing(lib):
+    def call(**kw):
+        a = dict(B=1, Hq=4, Hkv=2, Nq=3, Nkv=100, d=64, causal=0, splits=1, ws=None, wsb=0)
+        a.update(kw)
+        return lib.fa_fwd_gqa(FAKE, FAKE, FAKE, FAKE, FAKE, a["B"], a["Hq"], a["Hkv"], a["Nq"],
+                              a["Nkv"], a["d"], a["causal"], ctypes.c_float(0.1), a["splits"],
+                              a["ws"], a["wsb"], None)
+    assert call(Hq=3) == fa.FA_ERR_ARG
+    assert call(Hkv=0) == fa.FA_ERR_ARG
+    assert call(Nkv=0) == fa.FA_ERR_ARG
+    assert call(splits=0) == fa.FA_ERR_ARG
+    assert call(d=80) == fa.FA_ERR_UNSUPPORTED_D
+    assert call(splits=2, Nkv=1000) == fa.FA_ERR_WORKSPACE
