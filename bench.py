@@ -391,6 +391,86 @@ def run_gpu(args, w, rank, world, local_rank):
     return 0
 
 
+def run_gqa(args, wl, rank, world, local_rank):
+    """A general-form workload: decode (HBM-bound, GB/s) or GQA prefill
+    (TFLOPS), timed through fa_fwd_gqa with the library's split choice."""
+    import torch
+    from io_aware_exact_02_gb300 import fa, synth
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    fa.load()
+    q, k, v = synth.draw_gqa(wl, seed=rank_seed(args.seed, rank), device=dev)
+    splits = fa.fwd_gqa_splits(wl.B, wl.Hq, wl.Hkv, wl.Nq, wl.Nkv, wl.d, wl.causal)
+    o = torch.empty_like(q)
+    lse = torch.empty((wl.B, wl.Hq, wl.Nq), dtype=torch.float32, device=dev)
+    ws_bytes = fa.fwd_gqa_workspace_size(wl.B, wl.Hq, wl.Hkv, wl.Nq, wl.Nkv, wl.d, splits)
+    ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        fa.fwd_gqa(q, k, v, causal=wl.causal, scale=wl.softmax_scale, num_splits=splits,
+                   out=o, lse=lse, workspace=ws if ws_bytes else None)
+
+    for _ in range(args.warmup):
+        step()
+    fa.check_device_status()
+    sampler = ClockSampler(gpu_selector(local_rank))
+    sampler.start()
+    time.sleep(0.3)
+    barrier()
+    torch.cuda.synchronize(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    clocks = sampler.stop()
+    fa.check_device_status()
+    sec = reduce_max(e0.elapsed_time(e1) / 1e3)
+    per_call = sec / args.steps
+    kv_bytes = 2.0 * wl.B * wl.Hkv * wl.Nkv * wl.d * 2
+    qo_bytes = 2.0 * wl.B * wl.Hq * wl.Nq * wl.d * 2 + 4.0 * wl.B * wl.Hq * wl.Nq
+    alg_bytes = kv_bytes + qo_bytes
+    flops = 4.0 * wl.B * wl.Hq * wl.Nq * wl.Nkv * wl.d
+    if wl.causal and wl.Nq == wl.Nkv:
+        flops *= 0.5
+    peaks, peak_kind = load_peaks()
+    decode = wl.Nq <= 16
+    if decode:
+        value = world * alg_bytes / per_call / 1e9
+        unit, metric = "GB/s", "decode attention HBM GB/s (algorithmic bytes: Q, K, V read, O, lse written)"
+        peak = float(peaks["hbm_gbs"])
+        roofline = {"bound": "hbm", "kernel": "fa_fwd_kernel (general) + fa_combine_kernel",
+                    "achieved": value / world, "peak": peak, "unit": "GB/s",
+                    "frac": value / world / peak, "peak_kind": "%s HBM copy" % peak_kind,
+                    "traffic": None}
+    else:
+        value = world * flops / per_call / 1e12
+        unit, metric = "TFLOPS", "GQA prefill attention TFLOPS (bf16)"
+        peak = float(peaks["bf16_tflops"])
+        roofline = {"bound": "tensor", "kernel": "fa_fwd_kernel (general)",
+                    "achieved": value / world, "peak": peak, "unit": "TFLOP/s",
+                    "frac": value / world / peak, "peak_kind": "%s burst bf16" % peak_kind,
+                    "traffic": None}
+    if rank == 0:
+        print(json.dumps({
+            "metric": metric, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": per_call * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": wl.name, "B": wl.B, "Hq": wl.Hq, "Hkv": wl.Hkv, "Nq": wl.Nq,
+                       "Nkv": wl.Nkv, "d": wl.d, "causal": wl.causal, "splits": splits,
+                       "step": "fa_fwd_gqa", "l2": "K and V are %d MiB" % (kv_bytes / 2**20),
+                       "workspace_bytes": ws_bytes},
+            "clocks": clocks, "gpu_launches": args.steps * (2 if splits > 1 else 1),
+            "roofline": roofline, "tflops": flops / per_call / 1e12,
+            "hbm_gbs_algorithmic": alg_bytes / per_call / 1e9}), flush=True)
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -424,6 +504,13 @@ def main(argv=None):
         w = dict(name="custom_B%d_H%d_N%d_d%d_%s" % (B, H, N, d, "causal" if c else "full"),
                  B=B, H=H, N=N, d=d, causal=bool(c))
     else:
+        from io_aware_exact_02_gb300 import synth
+        if args.workload in [g.name for g in synth.GQA_ALL]:
+            if args.impl == "reference":
+                print(json.dumps({"impl": "reference", "unavailable":
+                                  "the reference arm times the square workloads only"}))
+                return 0
+            return run_gqa(args, synth.gqa_by_name(args.workload), rank, world, local_rank)
         w = workload_dict(args.workload)
     try:
         if args.impl == "reference":

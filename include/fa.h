@@ -95,10 +95,11 @@ int fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse,
  * effective number of splits is 1 or the sizes are invalid). */
 size_t fa_fwd_gqa_workspace_size(int B, int Hq, int Hkv, int Nq, int Nkv, int d, int num_splits);
 
-/* A number of key splits that fills `sm_count` SMs for these sizes: 1 when
- * the (key/value head, query-row pair) items already do, else enough splits
- * of at least two 128-key tiles each.  Host only; negative FA_ERR_* on bad
- * arguments. */
+/* A number of key splits for these sizes on `sm_count` SMs: the smallest
+ * split count, each split at least two 128-key tiles and at most 128 splits,
+ * whose work items fill whole waves of SMs within 90% of the best count
+ * (1 whenever the unsplit items already do).  Host only; negative FA_ERR_*
+ * on bad arguments. */
 int fa_fwd_gqa_splits(int B, int Hq, int Hkv, int Nq, int Nkv, int d, int causal, int sm_count);
 
 /*

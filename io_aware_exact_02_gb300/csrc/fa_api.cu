@@ -190,15 +190,23 @@ int fa_fwd_gqa_splits(int B, int Hq, int Hkv, int Nq, int Nkv, int d, int causal
   int rc = gqa_shape(B, Hq, Hkv, Nq, Nkv, d, 1, 1.0f, &g);
   if (rc != FA_OK) return rc;
   if (sm_count < 1 || (causal != 0 && causal != 1)) return FA_ERR_ARG;
-  // Split the keys only when the (K/V head, row pair) items cannot fill the
-  // SMs, keeping at least two 128-key tiles per split.
+  // The split count whose items fill whole waves of SMs best: for s splits
+  // of at least two 128-key tiles, wave efficiency = items*s /
+  // (ceil(items*s / sms) * sms); take the smallest s within 90% of the best
+  // (more splits also cost more combine work).
   const long long items = (long long)g.BH * g.n_pairs;
-  if (items >= sm_count) return 1;
-  long long splits = (sm_count + items - 1) / items;
-  const int max_splits = g.n_kv / 2 > 1 ? g.n_kv / 2 : 1;
-  if (splits > max_splits) splits = max_splits;
-  if (splits > 256) splits = 256;
-  return (int)splits;
+  int max_splits = g.n_kv / 2 > 1 ? g.n_kv / 2 : 1;
+  if (max_splits > 128) max_splits = 128;
+  auto eff = [&](int sp) {
+    const long long n = items * sp;
+    const long long waves = (n + sm_count - 1) / sm_count;
+    return (double)n / (double)(waves * sm_count);
+  };
+  double best = 0.0;
+  for (int sp = 1; sp <= max_splits; ++sp) best = eff(sp) > best ? eff(sp) : best;
+  for (int sp = 1; sp <= max_splits; ++sp)
+    if (eff(sp) >= 0.9 * best) return sp;
+  return 1;
 }
 
 int fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,

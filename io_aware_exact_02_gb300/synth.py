@@ -115,3 +115,47 @@ def draw_workload(w: Workload, seed: int = 0, device="cpu", with_dout: bool = Tr
     return draw(w.B, w.H, w.N, w.d, seed=seed, qkv_scale=w.qkv_scale,
                 heavy_frac=w.heavy_frac, heavy_factor=w.heavy_factor, device=device,
                 with_dout=with_dout)
+
+
+@dataclass(frozen=True)
+class GqaWorkload:
+    """A general-form workload: H_q query heads over H_kv key/value heads,
+    N_q query rows per head against N_kv keys (causal aligned bottom-right)."""
+    name: str
+    B: int
+    Hq: int
+    Hkv: int
+    Nq: int
+    Nkv: int
+    d: int
+    causal: bool
+
+    @property
+    def softmax_scale(self) -> float:
+        return 1.0 / math.sqrt(self.d)
+
+
+# One-token decode over a 32K-key cache with 4 query heads per K/V head, and
+# a causal GQA prefill at the LM-training shape's size.
+DECODE = GqaWorkload("decode_B8_Hq32_Hkv8_Nkv32768_d128", 8, 32, 8, 1, 32768, 128, True)
+GQA_PREFILL = GqaWorkload("gqa_prefill_B4_Hq32_Hkv8_N4096_d128", 4, 32, 8, 4096, 4096, 128, True)
+GQA_ALL = [DECODE, GQA_PREFILL]
+
+
+def gqa_by_name(name: str) -> GqaWorkload:
+    for w in GQA_ALL:
+        if w.name == name:
+            return w
+    raise KeyError(name)
+
+
+def draw_gqa(w: GqaWorkload, seed: int = 0, device="cpu"):
+    """(q, k, v) bf16: q (B, Hq, Nq, d), k and v (B, Hkv, Nkv, d), drawn in
+    that order from one generator seeded with ``seed``, iid N(0, 1)."""
+    device = torch.device(device)
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed))
+    q = torch.randn((w.B, w.Hq, w.Nq, w.d), generator=g, device=device).to(torch.bfloat16)
+    k = torch.randn((w.B, w.Hkv, w.Nkv, w.d), generator=g, device=device).to(torch.bfloat16)
+    v = torch.randn((w.B, w.Hkv, w.Nkv, w.d), generator=g, device=device).to(torch.bfloat16)
+    return q, k, v

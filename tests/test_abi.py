@@ -177,8 +177,13 @@ def test_fwd_gqa_sizes_and_splits(lib):
     assert lib.fa_fwd_gqa_workspace_size(1, 2, 2, 3, 1000, 64, 50) == up(8 * 6 * 64 * 4) + up(8 * 6 * 4)
     assert lib.fa_fwd_gqa_workspace_size(1, 3, 2, 3, 1000, 64, 2) == 0   # Hq not a multiple
     assert lib.fa_fwd_gqa_splits(8, 16, 16, 8192, 8192, 128, 0, 152) == 1
-    s = lib.fa_fwd_gqa_splits(1, 8, 1, 1, 32768, 128, 1, 152)
-    assert s == 128  # 1 item; capped at n_kv / 2 = 128 tiles of two
+    # 64 items (B*Hkv) on 152 SMs: 7 splits fill 448/456 of three waves
+    # (3 splits would leave 112 of 304 slots idle).
+    assert lib.fa_fwd_gqa_splits(8, 32, 8, 1, 32768, 128, 1, 152) == 7
+    # 256 items: 4 splits give 1024 of 1064 slots.
+    assert lib.fa_fwd_gqa_splits(32, 32, 8, 1, 32768, 128, 1, 152) == 4
+    # 1 item: at most 128 splits (128/152 of a wave); 116 is the first within 90%.
+    assert lib.fa_fwd_gqa_splits(1, 8, 1, 1, 32768, 128, 1, 152) == 116
     assert lib.fa_fwd_gqa_splits(1, 8, 1, 1, 300, 128, 0, 152) == 1
     assert lib.fa_fwd_gqa_splits(1, 8, 1, 1, 300, 128, 0, 0) == fa.FA_ERR_ARG
 

@@ -117,3 +117,28 @@ def test_fwd_gqa_errors():
     with pytest.raises(fa.FaError) as e:
         fa.fwd_gqa(q, k, k, num_splits=2, workspace=torch.zeros(16, dtype=torch.uint8, device=dev))
     assert e.value.code == fa.FA_ERR_WORKSPACE
+
+
+# ------------------------------------------ full-size general workloads
+
+def test_decode_workload_full_size():
+    w = synth.DECODE
+    q, k, v = synth.draw_gqa(w)
+    o, lse = run(q, k, v, w.causal, w.softmax_scale, None)
+    o_ref, lse_ref = oracle.attn_fwd_gqa(q, k, v, w.causal, w.softmax_scale)
+    compare(o, lse, o_ref, lse_ref, w.name)
+
+
+def test_gqa_prefill_workload_full_size_sampled():
+    # The GPU runs the whole workload; the oracle checks batch 1 and the
+    # query heads of two K/V heads (heads are independent).
+    w = synth.GQA_PREFILL
+    q, k, v = synth.draw_gqa(w)
+    o, lse = run(q, k, v, w.causal, w.softmax_scale, None)
+    G = w.Hq // w.Hkv
+    for hk in (0, w.Hkv - 1):
+        qs = q[1:2, hk * G:(hk + 1) * G]
+        o_ref, lse_ref = oracle.attn_fwd_gqa(qs, k[1:2, hk:hk + 1], v[1:2, hk:hk + 1], w.causal,
+                                             w.softmax_scale)
+        compare(o[1:2, hk * G:(hk + 1) * G], lse[1:2, hk * G:(hk + 1) * G], o_ref, lse_ref,
+                (w.name, hk))
