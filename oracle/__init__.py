@@ -63,6 +63,11 @@ def bind(path: str):
     lib.oracle_attn_fwd_gqa.argtypes = [dp, dp, dp, i64, i64, i64, i64, i64, i64, cint, dbl,
                                         dp, dp]
     lib.oracle_combine_splits.argtypes = [dp, dp, i64, i64, i64, dp, dp]
+    u8p = ctypes.POINTER(ctypes.c_ubyte)
+    lib.oracle_attn_fwd_blockmask.argtypes = [dp, dp, dp, i64, i64, i64, cint, dbl, u8p, i64,
+                                              dp, dp]
+    lib.oracle_attn_bwd_blockmask.argtypes = [dp, dp, dp, dp, i64, i64, i64, cint, dbl, u8p,
+                                              i64, dp, dp, dp]
     lib.oracle_fwd_flops.argtypes = [i64, i64, i64, cint]
     lib.oracle_fwd_flops.restype = dbl
     lib.oracle_recompute_flops.argtypes = [i64, i64]
@@ -72,6 +77,7 @@ def bind(path: str):
     for f in (lib.oracle_attn_fwd, lib.oracle_attn_fwd_rows,
               lib.oracle_attn_probs, lib.oracle_attn_bwd,
               lib.oracle_attn_fwd_gqa, lib.oracle_combine_splits,
+              lib.oracle_attn_fwd_blockmask, lib.oracle_attn_bwd_blockmask,
               lib.oracle_set_num_threads):
         f.restype = None
     return lib
@@ -198,6 +204,41 @@ def combine_splits(o_parts, lse_parts, lib=None):
     (lib or _load()).oracle_combine_splits(_ptr(o_parts), _ptr(lse_parts), S, R, d, _ptr(o),
                                            _ptr(lse))
     return o, lse
+
+
+def _blockmask(bm, N, bs):
+    bm = np.ascontiguousarray(bm, dtype=np.uint8)
+    nb = -(-N // bs)
+    if bm.shape != (nb, nb):
+        raise ValueError("block mask must be (%d, %d)" % (nb, nb))
+    return bm, bm.ctypes.data_as(ctypes.POINTER(ctypes.c_ubyte))
+
+
+def attn_fwd_blockmask(q, k, v, causal: bool, scale: float, block_mask, block=128, lib=None):
+    """Block-sparse forward: key j visible to query i iff
+    block_mask[i // block, j // block] (and j <= i when causal)."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, H, N, d = _shape4(q)
+    bm, bmp = _blockmask(block_mask, N, block)
+    o = np.zeros((B, H, N, d))
+    lse = np.zeros((B, H, N))
+    (lib or _load()).oracle_attn_fwd_blockmask(_ptr(q), _ptr(k), _ptr(v), B * H, N, d,
+                                               int(bool(causal)), float(scale), bmp, block,
+                                               _ptr(o), _ptr(lse))
+    return o, lse
+
+
+def attn_bwd_blockmask(q, k, v, dout, causal: bool, scale: float, block_mask, block=128,
+                       lib=None):
+    """dQ, dK, dV of the block-sparse forward."""
+    q, k, v, dout = _f64(q), _f64(k), _f64(v), _f64(dout)
+    B, H, N, d = _shape4(q)
+    bm, bmp = _blockmask(block_mask, N, block)
+    dq, dk, dv = (np.zeros((B, H, N, d)) for _ in range(3))
+    (lib or _load()).oracle_attn_bwd_blockmask(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), B * H, N,
+                                               d, int(bool(causal)), float(scale), bmp, block,
+                                               _ptr(dq), _ptr(dk), _ptr(dv))
+    return dq, dk, dv
 
 
 def fwd_flops(B: int, H: int, N: int, d: int, causal: bool) -> float:

@@ -52,6 +52,13 @@
  * sec. 9.4: lse = ln sum_s exp(lse_s), O = sum_s exp(lse_s - lse) O_s
  * (oracle_combine_splits).
  *
+ * Block-sparse form (oracle_attn_fwd_blockmask / oracle_attn_bwd_blockmask):
+ * a 0/1 mask bm over (bs-row query block, bs-key block) pairs, shared by all
+ * heads; key j is visible to query i when bm[i / bs][j / bs] is 1 (and
+ * j <= i under the causal mask).  This is dense attention with the masked
+ * scores at -inf, evaluated entry by entry; a row with no visible key has
+ * O = 0, lse = -inf and takes no part in the gradients.
+ *
  * Loops are parallelised with OpenMP over independent rows (forward, dQ) or
  * independent key rows (dK, dV); each output element is computed by one
  * thread with a plain sequential sum, so results do not depend on the thread
@@ -343,4 +350,117 @@ void oracle_combine_splits(const double* o_parts, const double* lse_parts, int64
             for (int64_t c = 0; c < d; ++c) orow[c] += w * part[c];
         }
     }
+}
+
+static int visible(int64_t i, int64_t j, int causal, const unsigned char* bm, int64_t nb,
+                   int64_t bs)
+{
+    if (causal && j > i) return 0;
+    return bm[(i / bs) * nb + j / bs] != 0;
+}
+
+/* Block-sparse forward (see the header); q, k, v, o are [BH][N][d]. */
+void oracle_attn_fwd_blockmask(const double* q, const double* k, const double* v, int64_t BH,
+                               int64_t N, int64_t d, int causal, double scale,
+                               const unsigned char* bm, int64_t bs, double* o, double* lse)
+{
+    const int64_t nb = (N + bs - 1) / bs;
+#pragma omp parallel
+    {
+        double* s = (double*)malloc(sizeof(double) * (size_t)(N > 0 ? N : 1));
+#pragma omp for schedule(dynamic, 16)
+        for (int64_t r = 0; r < BH * N; ++r) {
+            const int64_t h = r / N, i = r % N;
+            const double* qi = q + r * d;
+            double m = -INFINITY;
+            for (int64_t j = 0; j < N; ++j) {
+                if (!visible(i, j, causal, bm, nb, bs)) { s[j] = -INFINITY; continue; }
+                const double* kj = k + (h * N + j) * d;
+                double acc = 0.0;
+                for (int64_t c = 0; c < d; ++c) acc += qi[c] * kj[c];
+                s[j] = scale * acc;
+                if (s[j] > m) m = s[j];
+            }
+            double* orow = o + r * d;
+            for (int64_t c = 0; c < d; ++c) orow[c] = 0.0;
+            if (m == -INFINITY) { lse[r] = -INFINITY; continue; }
+            double l = 0.0;
+            for (int64_t j = 0; j < N; ++j) if (s[j] > -INFINITY) l += exp(s[j] - m);
+            const double ls = m + log(l);
+            lse[r] = ls;
+            for (int64_t j = 0; j < N; ++j) {
+                if (s[j] == -INFINITY) continue;
+                const double a = exp(s[j] - ls);
+                const double* vj = v + (h * N + j) * d;
+                for (int64_t c = 0; c < d; ++c) orow[c] += a * vj[c];
+            }
+        }
+        free(s);
+    }
+}
+
+/* Block-sparse backward: the textbook formulas over the visible entries
+ * (A = 0 elsewhere), in the two passes of oracle_attn_bwd. */
+void oracle_attn_bwd_blockmask(const double* q, const double* k, const double* v,
+                               const double* dout, int64_t BH, int64_t N, int64_t d, int causal,
+                               double scale, const unsigned char* bm, int64_t bs, double* dq,
+                               double* dk, double* dv)
+{
+    const int64_t nb = (N + bs - 1) / bs;
+    double* lse = (double*)malloc(sizeof(double) * (size_t)(BH * N > 0 ? BH * N : 1));
+    double* D = (double*)malloc(sizeof(double) * (size_t)(BH * N > 0 ? BH * N : 1));
+    double* o = (double*)malloc(sizeof(double) * (size_t)(BH * N * d > 0 ? BH * N * d : 1));
+    oracle_attn_fwd_blockmask(q, k, v, BH, N, d, causal, scale, bm, bs, o, lse);
+#pragma omp parallel for schedule(dynamic, 16)
+    for (int64_t r = 0; r < BH * N; ++r) {
+        const int64_t h = r / N, i = r % N;
+        const double* qi = q + r * d;
+        const double* doi = dout + r * d;
+        double* dqi = dq + r * d;
+        for (int64_t c = 0; c < d; ++c) dqi[c] = 0.0;
+        double Di = 0.0;
+        if (lse[r] == -INFINITY) { D[r] = 0.0; continue; }
+        for (int64_t j = 0; j < N; ++j) {
+            if (!visible(i, j, causal, bm, nb, bs)) continue;
+            const double* kj = k + (h * N + j) * d;
+            const double* vj = v + (h * N + j) * d;
+            double sd = 0.0, dd = 0.0;
+            for (int64_t c = 0; c < d; ++c) { sd += qi[c] * kj[c]; dd += doi[c] * vj[c]; }
+            Di += exp(scale * sd - lse[r]) * dd;
+        }
+        D[r] = Di;
+        for (int64_t j = 0; j < N; ++j) {
+            if (!visible(i, j, causal, bm, nb, bs)) continue;
+            const double* kj = k + (h * N + j) * d;
+            const double* vj = v + (h * N + j) * d;
+            double sd = 0.0, dd = 0.0;
+            for (int64_t c = 0; c < d; ++c) { sd += qi[c] * kj[c]; dd += doi[c] * vj[c]; }
+            const double ds = exp(scale * sd - lse[r]) * (dd - Di);
+            for (int64_t c = 0; c < d; ++c) dqi[c] += ds * kj[c];
+        }
+        for (int64_t c = 0; c < d; ++c) dqi[c] *= scale;
+    }
+#pragma omp parallel for schedule(dynamic, 16)
+    for (int64_t r = 0; r < BH * N; ++r) {
+        const int64_t h = r / N, j = r % N;
+        const double* kj = k + r * d;
+        const double* vj = v + r * d;
+        double* dkj = dk + r * d;
+        double* dvj = dv + r * d;
+        for (int64_t c = 0; c < d; ++c) { dkj[c] = 0.0; dvj[c] = 0.0; }
+        for (int64_t i = 0; i < N; ++i) {
+            if (!visible(i, j, causal, bm, nb, bs) || lse[h * N + i] == -INFINITY) continue;
+            const double* qi = q + (h * N + i) * d;
+            const double* doi = dout + (h * N + i) * d;
+            double sd = 0.0, dd = 0.0;
+            for (int64_t c = 0; c < d; ++c) { sd += qi[c] * kj[c]; dd += doi[c] * vj[c]; }
+            const double a = exp(scale * sd - lse[h * N + i]);
+            const double ds = a * (dd - D[h * N + i]);
+            for (int64_t c = 0; c < d; ++c) { dvj[c] += a * doi[c]; dkj[c] += ds * qi[c]; }
+        }
+        for (int64_t c = 0; c < d; ++c) dkj[c] *= scale;
+    }
+    free(lse);
+    free(D);
+    free(o);
 }

@@ -27,6 +27,10 @@ MUTATIONS = {
     "combine_unweighted": ("const double w = exp(lse_parts[t * R + r] - l);",
                            "const double w = 1.0 / (double)S;"),
     "combine_lse_no_max": ("const double l = m + log(sum);", "const double l = log(sum);"),
+    "blockmask_transposed": ("return bm[(i / bs) * nb + j / bs] != 0;",
+                             "return bm[(j / bs) * nb + i / bs] != 0;"),
+    "blockmask_dk_drops_scale": ("        for (int64_t c = 0; c < d; ++c) dkj[c] *= scale;\n    }\n    free(lse);\n    free(D);\n    free(o);",
+                                 "    }\n    free(lse);\n    free(D);\n    free(o);"),
     "lse_drop_max": ("return m + log(l);", "return log(l);"),
     "causal_off_by_one": ("return causal ? (i + 1 < N ? i + 1 : N) : N;",
                           "return causal ? (i < N ? i : N) : N;"),
@@ -106,6 +110,22 @@ def battery(lib):
     fo, flse = oracle.attn_fwd_gqa(gq, gk, gv, False, scale, lib=lib)
     if np.abs(co - fo).max() > 1e-12 or np.abs(clse - flse).max() > 1e-12:
         failed.append("combine")
+    # block-sparse form against torch with the expanded element mask
+    bs, Nb = 2, 6
+    bm = np.array([[1, 0, 1], [1, 1, 0], [0, 0, 1]], np.uint8)
+    bq, bk, bv, bdo = (rnd((1, 1, Nb, d), 30 + t) for t in range(4))
+    idx = np.arange(Nb)
+    em = torch.tensor(bm[idx[:, None] // bs, idx[None, :] // bs].astype(bool))
+    tq, tk, tv = (torch.tensor(x, requires_grad=True) for x in (bq, bk, bv))
+    to = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, attn_mask=em, scale=scale)
+    to.backward(torch.tensor(bdo))
+    bo, _ = oracle.attn_fwd_blockmask(bq, bk, bv, False, scale, bm, bs, lib=lib)
+    if np.abs(bo - to.detach().numpy()).max() > 1e-12:
+        failed.append("blockmask_fwd")
+    bg = oracle.attn_bwd_blockmask(bq, bk, bv, bdo, False, scale, bm, bs, lib=lib)
+    for name, g, t in zip("qkv", bg, (tq, tk, tv)):
+        if np.abs(g - t.grad.numpy()).max() > 1e-11:
+            failed.append("blockmask_d" + name)
     o, lse = oracle.attn_fwd(q, k, v, False, 0.0, lib=lib)
     if np.abs(o - v.mean(2, keepdims=True)).max() > 1e-12 or np.abs(lse - math.log(N)).max() > 1e-12:
         failed.append("scale0")
@@ -129,6 +149,8 @@ def test_unmodified_oracle_passes_battery():
 def test_planted_mistake_is_caught(name, tmp_path):
     before, after = MUTATIONS[name]
     text = open(SRC).read()
-    assert text.count(before) == 1, name
-    lib = _build(text.replace(before, after), tmp_path, name)
+    # The first occurrence is the mutated one (the square forms come first in
+    # the file; later forms that repeat an expression have their own entries).
+    assert text.count(before) >= 1, name
+    lib = _build(text.replace(before, after, 1), tmp_path, name)
     assert battery(lib), "mutation %s passed every pin" % name
