@@ -471,6 +471,111 @@ def run_gqa(args, wl, rank, world, local_rank):
     return 0
 
 
+def visible_pairs(mask, N, causal):
+    """(query, key) pairs a block mask leaves visible in one head: the
+    algorithmic work of the block-sparse passes is proportional to it."""
+    nb = len(mask)
+    total = 0
+    for r in range(nb):
+        r0, r1 = r * 128, min(N, (r + 1) * 128)
+        for c in range(nb):
+            if not mask[r][c]:
+                continue
+            c0, c1 = c * 128, min(N, (c + 1) * 128)
+            if not causal:
+                total += (r1 - r0) * (c1 - c0)
+            else:  # keys j <= i, row by row
+                for i in range(r0, r1):
+                    total += max(0, min(c1, i + 1) - c0)
+    return total
+
+
+def run_blocksparse(args, wl, rank, world, local_rank):
+    """Block-sparse fwd + bwd step (TFLOPS counted over the visible pairs)."""
+    import torch
+    from io_aware_exact_02_gb300 import fa, synth
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    fa.load()
+    dense = synth.Workload(wl.name, wl.B, wl.H, wl.N, wl.d, wl.causal)
+    q, k, v, do = synth.draw_workload(dense, seed=rank_seed(args.seed, rank), device=dev)
+    mask_cpu = synth.draw_block_mask(wl.n_blocks, wl.density, seed=args.seed)
+    mask = mask_cpu.to(dev)
+    o = torch.empty_like(q)
+    lse = torch.empty((wl.B, wl.H, wl.N), dtype=torch.float32, device=dev)
+    dq, dk, dv = (torch.empty_like(q) for _ in range(3))
+    ws = torch.empty(fa.bwd_workspace_size(wl.B, wl.H, wl.N, wl.d), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+    fwd_ms, bwd_ms = [], []
+
+    def step(record=False):
+        if record:
+            ev[0].record(stream)
+        fa.fwd_blocksparse(q, k, v, mask, causal=wl.causal, scale=wl.softmax_scale, out=o,
+                           lse=lse)
+        if record:
+            ev[1].record(stream)
+        fa.bwd_blocksparse(q, k, v, o, do, lse, mask, causal=wl.causal, scale=wl.softmax_scale,
+                           dq=dq, dk=dk, dv=dv, workspace=ws)
+        if record:
+            ev[2].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    fa.check_device_status()
+    sampler = ClockSampler(gpu_selector(local_rank))
+    sampler.start()
+    time.sleep(0.3)
+    barrier()
+    torch.cuda.synchronize(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    clocks = sampler.stop()
+    # Per-pass split, measured in separate steps after the timed region.
+    for _ in range(3):
+        step(record=True)
+        torch.cuda.synchronize(dev)
+        fwd_ms.append(ev[0].elapsed_time(ev[1]))
+        bwd_ms.append(ev[1].elapsed_time(ev[2]))
+    fa.check_device_status()
+    sec = reduce_max(e0.elapsed_time(e1) / 1e3)
+    per_step = sec / args.steps
+    pairs = visible_pairs(mask_cpu.tolist(), wl.N, wl.causal)
+    f_fwd = 4.0 * wl.B * wl.H * pairs * wl.d
+    f_bwd = 2.5 * f_fwd
+    value = world * (f_fwd + f_bwd) / per_step / 1e12
+    peaks, peak_kind = load_peaks()
+    peak = float(peaks["bf16_tflops"])
+    t_fwd, t_bwd = statistics.median(fwd_ms) / 1e3, statistics.median(bwd_ms) / 1e3
+    if rank == 0:
+        print(json.dumps({
+            "metric": "block-sparse attention fwd+bwd TFLOPS (bf16, FLOPs over visible pairs)",
+            "value": value, "unit": "TFLOPS", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": per_step * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": wl.name, "B": wl.B, "H": wl.H, "N": wl.N, "d": wl.d,
+                       "causal": wl.causal, "density": wl.density,
+                       "active_blocks": int(mask_cpu.sum()), "blocks": wl.n_blocks ** 2,
+                       "step": "fa_fwd_blocksparse + fa_bwd_blocksparse",
+                       "l2": "inputs larger than L2"},
+            "clocks": clocks, "gpu_launches": args.steps * 4,
+            "roofline": {"bound": "tensor", "kernel": "fa_bwd_main_kernel (sparse)",
+                         "achieved": f_bwd / t_bwd / 1e12, "peak": peak, "unit": "TFLOP/s",
+                         "frac": f_bwd / t_bwd / 1e12 / peak,
+                         "peak_kind": "%s burst bf16" % peak_kind, "traffic": None},
+            "fwd_tflops": f_fwd / t_fwd / 1e12, "bwd_tflops": f_bwd / t_bwd / 1e12,
+            "fwd_ms": t_fwd * 1e3, "bwd_ms": t_bwd * 1e3}), flush=True)
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -511,6 +616,13 @@ def main(argv=None):
                                   "the reference arm times the square workloads only"}))
                 return 0
             return run_gqa(args, synth.gqa_by_name(args.workload), rank, world, local_rank)
+        if args.workload in [b.name for b in synth.BLOCKSPARSE_ALL]:
+            if args.impl == "reference":
+                print(json.dumps({"impl": "reference", "unavailable":
+                                  "the reference arm times the square workloads only"}))
+                return 0
+            return run_blocksparse(args, synth.blocksparse_by_name(args.workload), rank, world,
+                                   local_rank)
         w = workload_dict(args.workload)
     try:
         if args.impl == "reference":

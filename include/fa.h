@@ -147,6 +147,29 @@ int fa_bwd_phases(const void* q, const void* k, const void* v, const void* o, co
                   int phase_mask);
 
 /*
+ * Block-sparse attention: the block-sparse extension of FlashAttention named
+ * in the reading guide of cs2680 Lecture 9.  block_mask is a device array of
+ * ceil(N/128) x ceil(N/128) bytes,
+ * row-major, shared by every batch entry and head: key j is visible to query
+ * i when block_mask[(i/128) * ceil(N/128) + j/128] is nonzero (and j <= i
+ * when causal).  The 128 x 128 blocks are the kernels' own tiles, so a zero
+ * entry skips that tile's loads and MMAs.  Masked scores count as -inf; a
+ * query row with no visible key gets O = 0 and lse = -inf, and its rows of
+ * the gradients are 0 (a key with no visible query gets dK = dV = 0).
+ * All-ones masks give results bitwise equal to fa_fwd / fa_bwd.
+ * Other arguments, ownership and errors as fa_fwd / fa_bwd, plus FA_ERR_ARG
+ * for a null block_mask.  The mask must stay valid until the call's work on
+ * the stream is done.
+ */
+int fa_fwd_blocksparse(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                       int H, int N, int d, int causal, float scale, const void* block_mask,
+                       void* stream);
+int fa_bwd_blocksparse(const void* q, const void* k, const void* v, const void* o,
+                       const void* dout, const float* lse, void* dq, void* dk, void* dv, int B,
+                       int H, int N, int d, int causal, float scale, const void* block_mask,
+                       void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Size of the scratch array fa_bwd_noalloc uses: 32 MiB of static device
  * data on every GPU that loads the library, held until the process exits.
  */

@@ -152,6 +152,102 @@ int make_tmap_bhnd(const void* base, int BH, int N, int d, CUtensorMap* out) {
   return r == CUDA_SUCCESS ? FA_OK : FA_ERR_ARG;
 }
 
+namespace {
+
+// The forward pass over a general shape; block_mask is null for dense attention.
+int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+             int Hkv, int Nq, int Nkv, int d, int causal, float scale, int num_splits,
+             void* workspace, size_t workspace_bytes, const uint8_t* block_mask, void* stream) {
+  if (!q || !k || !v || !o || !lse) return FA_ERR_ARG;
+  if (causal != 0 && causal != 1) return FA_ERR_ARG;
+  GqaShape g;
+  int rc = gqa_shape(B, Hq, Hkv, Nq, Nkv, d, num_splits, scale, &g);
+  if (rc != FA_OK) return rc;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+    return FA_ERR_ALIGN;
+  if (g.splits > 1 && (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
+                       workspace_bytes < g.ws.total))
+    return FA_ERR_WORKSPACE;
+  DeviceState* ds;
+  if ((rc = device_state(&ds)) != FA_OK) return rc;
+  CUtensorMap tq, tk, tv;
+  if ((rc = make_tmap_bhnd(q, g.BH, g.rows, d, &tq)) != FA_OK) return rc;
+  if ((rc = make_tmap_bhnd(k, g.BH, Nkv, d, &tk)) != FA_OK) return rc;
+  if ((rc = make_tmap_bhnd(v, g.BH, Nkv, d, &tv)) != FA_OK) return rc;
+  FwdParams p;
+  p.o = o;
+  p.lse = lse;
+  p.o_part = nullptr;
+  p.lse_part = nullptr;
+  p.block_mask = block_mask;
+  if (g.splits > 1) {
+    p.o_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + g.ws.o_part);
+    p.lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + g.ws.lse_part);
+  }
+  p.status = ds->status;
+  p.BH = g.BH;
+  p.rows = g.rows;
+  p.Nq = Nq;
+  p.Nkv = Nkv;
+  p.causal_off = Nkv - Nq;
+  p.n_kv = g.n_kv;
+  p.n_pairs = g.n_pairs;
+  p.splits = g.splits;
+  p.tiles_per_split = g.tiles_per_split;
+  p.causal = causal;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.grid = fwd_grid(g.BH, g.n_pairs * g.splits, causal, ds->sm_count);
+  return launch_fwd(tq, tk, tv, p, d, static_cast<cudaStream_t>(stream));
+}
+
+// The backward pass; block_mask is null for dense attention.
+int bwd_impl(const void* q, const void* k, const void* v, const void* o, const void* dout,
+             const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+             int causal, float scale, void* workspace, size_t workspace_bytes, void* stream,
+             int phase_mask, const uint8_t* block_mask) {
+  if (phase_mask < 1 || phase_mask > 7) return FA_ERR_ARG;
+  if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv) return FA_ERR_ARG;
+  if (causal != 0 && causal != 1) return FA_ERR_ARG;
+  int rc = check_shape(B, H, N, d, scale);
+  if (rc != FA_OK) return rc;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dout) ||
+      !aligned16(lse) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+    return FA_ERR_ALIGN;
+  const size_t need = fa_bwd_workspace_size(B, H, N, d);
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || workspace_bytes < need)
+    return FA_ERR_WORKSPACE;
+  DeviceState* ds;
+  if ((rc = device_state(&ds)) != FA_OK) return rc;
+  const int BH = B * H;
+  CUtensorMap tq, tk, tv, tdo;
+  if ((rc = make_tmap_bhnd(q, BH, N, d, &tq)) != FA_OK) return rc;
+  if ((rc = make_tmap_bhnd(k, BH, N, d, &tk)) != FA_OK) return rc;
+  if ((rc = make_tmap_bhnd(v, BH, N, d, &tv)) != FA_OK) return rc;
+  if ((rc = make_tmap_bhnd(dout, BH, N, d, &tdo)) != FA_OK) return rc;
+  const BwdWorkspace ws = bwd_workspace_layout(BH, N, d);
+  BwdParams p;
+  p.o = o;
+  p.dout = dout;
+  p.lse = lse;
+  p.dq = dq;
+  p.dk = dk;
+  p.dv = dv;
+  p.dq_acc = reinterpret_cast<float*>(static_cast<char*>(workspace) + ws.dq_acc);
+  p.delta = reinterpret_cast<float*>(static_cast<char*>(workspace) + ws.delta);
+  p.lse2 = reinterpret_cast<float*>(static_cast<char*>(workspace) + ws.lse2);
+  p.status = ds->status;
+  p.block_mask = block_mask;
+  p.BH = BH;
+  p.N = N;
+  p.n_kv = ceil_div(N, kTile);
+  p.causal = causal;
+  p.scale = scale;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  return launch_bwd(tq, tk, tv, tdo, p, d, static_cast<cudaStream_t>(stream), phase_mask);
+}
+
+}  // namespace
+
 }  // namespace fa
 
 using namespace fa;
@@ -212,45 +308,16 @@ int fa_fwd_gqa_splits(int B, int Hq, int Hkv, int Nq, int Nkv, int d, int causal
 int fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
                int Hkv, int Nq, int Nkv, int d, int causal, float scale, int num_splits,
                void* workspace, size_t workspace_bytes, void* stream) {
-  if (!q || !k || !v || !o || !lse) return FA_ERR_ARG;
-  if (causal != 0 && causal != 1) return FA_ERR_ARG;
-  GqaShape g;
-  int rc = gqa_shape(B, Hq, Hkv, Nq, Nkv, d, num_splits, scale, &g);
-  if (rc != FA_OK) return rc;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
-    return FA_ERR_ALIGN;
-  if (g.splits > 1 && (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
-                       workspace_bytes < g.ws.total))
-    return FA_ERR_WORKSPACE;
-  DeviceState* ds;
-  if ((rc = device_state(&ds)) != FA_OK) return rc;
-  CUtensorMap tq, tk, tv;
-  if ((rc = make_tmap_bhnd(q, g.BH, g.rows, d, &tq)) != FA_OK) return rc;
-  if ((rc = make_tmap_bhnd(k, g.BH, Nkv, d, &tk)) != FA_OK) return rc;
-  if ((rc = make_tmap_bhnd(v, g.BH, Nkv, d, &tv)) != FA_OK) return rc;
-  FwdParams p;
-  p.o = o;
-  p.lse = lse;
-  p.o_part = nullptr;
-  p.lse_part = nullptr;
-  if (g.splits > 1) {
-    p.o_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + g.ws.o_part);
-    p.lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + g.ws.lse_part);
-  }
-  p.status = ds->status;
-  p.BH = g.BH;
-  p.rows = g.rows;
-  p.Nq = Nq;
-  p.Nkv = Nkv;
-  p.causal_off = Nkv - Nq;
-  p.n_kv = g.n_kv;
-  p.n_pairs = g.n_pairs;
-  p.splits = g.splits;
-  p.tiles_per_split = g.tiles_per_split;
-  p.causal = causal;
-  p.scale_log2 = scale * 1.4426950408889634f;
-  p.grid = fwd_grid(g.BH, g.n_pairs * g.splits, causal, ds->sm_count);
-  return launch_fwd(tq, tk, tv, p, d, static_cast<cudaStream_t>(stream));
+  return fa::fwd_impl(q, k, v, o, lse, B, Hq, Hkv, Nq, Nkv, d, causal, scale, num_splits,
+                      workspace, workspace_bytes, nullptr, stream);
+}
+
+int fa_fwd_blocksparse(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                       int H, int N, int d, int causal, float scale, const void* block_mask,
+                       void* stream) {
+  if (!block_mask) return FA_ERR_ARG;
+  return fa::fwd_impl(q, k, v, o, lse, B, H, H, N, N, d, causal, scale, 1, nullptr, 0,
+                      static_cast<const uint8_t*>(block_mask), stream);
 }
 
 size_t fa_bwd_workspace_size(int B, int H, int N, int d) {
@@ -269,44 +336,17 @@ int fa_bwd_phases(const void* q, const void* k, const void* v, const void* o, co
                   const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d,
                   int causal, float scale, void* workspace, size_t workspace_bytes, void* stream,
                   int phase_mask) {
-  if (phase_mask < 1 || phase_mask > 7) return FA_ERR_ARG;
-  if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv) return FA_ERR_ARG;
-  if (causal != 0 && causal != 1) return FA_ERR_ARG;
-  int rc = check_shape(B, H, N, d, scale);
-  if (rc != FA_OK) return rc;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dout) ||
-      !aligned16(lse) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
-    return FA_ERR_ALIGN;
-  const size_t need = fa_bwd_workspace_size(B, H, N, d);
-  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || workspace_bytes < need)
-    return FA_ERR_WORKSPACE;
-  DeviceState* ds;
-  if ((rc = device_state(&ds)) != FA_OK) return rc;
-  const int BH = B * H;
-  CUtensorMap tq, tk, tv, tdo;
-  if ((rc = make_tmap_bhnd(q, BH, N, d, &tq)) != FA_OK) return rc;
-  if ((rc = make_tmap_bhnd(k, BH, N, d, &tk)) != FA_OK) return rc;
-  if ((rc = make_tmap_bhnd(v, BH, N, d, &tv)) != FA_OK) return rc;
-  if ((rc = make_tmap_bhnd(dout, BH, N, d, &tdo)) != FA_OK) return rc;
-  const BwdWorkspace ws = bwd_workspace_layout(BH, N, d);
-  BwdParams p;
-  p.o = o;
-  p.dout = dout;
-  p.lse = lse;
-  p.dq = dq;
-  p.dk = dk;
-  p.dv = dv;
-  p.dq_acc = reinterpret_cast<float*>(static_cast<char*>(workspace) + ws.dq_acc);
-  p.delta = reinterpret_cast<float*>(static_cast<char*>(workspace) + ws.delta);
-  p.lse2 = reinterpret_cast<float*>(static_cast<char*>(workspace) + ws.lse2);
-  p.status = ds->status;
-  p.BH = BH;
-  p.N = N;
-  p.n_kv = ceil_div(N, kTile);
-  p.causal = causal;
-  p.scale = scale;
-  p.scale_log2 = scale * 1.4426950408889634f;
-  return launch_bwd(tq, tk, tv, tdo, p, d, static_cast<cudaStream_t>(stream), phase_mask);
+  return fa::bwd_impl(q, k, v, o, dout, lse, dq, dk, dv, B, H, N, d, causal, scale, workspace,
+                      workspace_bytes, stream, phase_mask, nullptr);
+}
+
+int fa_bwd_blocksparse(const void* q, const void* k, const void* v, const void* o,
+                       const void* dout, const float* lse, void* dq, void* dk, void* dv, int B,
+                       int H, int N, int d, int causal, float scale, const void* block_mask,
+                       void* workspace, size_t workspace_bytes, void* stream) {
+  if (!block_mask) return FA_ERR_ARG;
+  return fa::bwd_impl(q, k, v, o, dout, lse, dq, dk, dv, B, H, N, d, causal, scale, workspace,
+                      workspace_bytes, stream, 7, static_cast<const uint8_t*>(block_mask));
 }
 
 int fa_device_status(void* stream, int* site) {

@@ -208,7 +208,9 @@ __global__ void __launch_bounds__(256) fa_bwd_convert_kernel(const BwdParams p) 
 
 // ------------------------------------------------------------------ main
 
-template <int D>
+// kSparse: a block mask over (128-query tile, 128-key tile) pairs; key tile
+// j visits only the query tiles i whose block (i, j) is active.
+template <int D, bool kSparse>
 __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                        const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
@@ -259,7 +261,19 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
   int bh, j;
   bwd_item(blockIdx.x, p.BH, p.n_kv, &bh, &j);
   const int i0 = p.causal ? j : 0;
-  const int n_iter = p.n_kv - i0;
+  auto active_i = [&](int i) -> bool {
+    return !kSparse || p.block_mask[(size_t)i * p.n_kv + j] != 0;
+  };
+  // The next query tile at or after c that this key tile visits.
+  auto next_i = [&](int c) -> int {
+    while (!active_i(c)) ++c;
+    return c;
+  };
+  int n_iter = p.n_kv - i0;
+  if (kSparse) {
+    n_iter = 0;
+    for (int i = i0; i < p.n_kv; ++i) n_iter += active_i(i) ? 1 : 0;
+  }
   const int npad = p.n_kv * kTile;
 
   if (warp == kWarpLoad) {
@@ -275,11 +289,13 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         tma_load_3d(sm.v + h * 16384, &tv, &sm.kv_full, h * 64, j * kTile, bh);
       }
       int it = 0;
+      int cur = i0;
       for (; it < n_iter; ++it) {
         const int s = it % NS, use = it / NS;
         if (use > 0 && !mbar_wait(&sm.q_empty[s], (use - 1) & 1, p.status, abortf, kSiteQEmpty))
           break;
-        const int i = i0 + it;
+        const int i = next_i(cur);
+        cur = i + 1;
         mbar_arrive_expect_tx(&sm.q_full[s], 2 * Cfg::kTileBytes + 2 * kTile * 4);
         for (int h = 0; h < D / 64; ++h) {
           tma_load_3d(sm.q[s] + h * 16384, &tq, &sm.q_full[s], h * 64, i * kTile, bh);
@@ -369,10 +385,12 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     uint32_t held[32];
     float* held_base = nullptr;  // dQ columns waiting to be added (see the drain)
     bool ok = true;
+    int cur = i0;
     for (int it = 0; it < n_iter; ++it) {
       const int s = it % NS;
       const uint32_t par = it & 1;
-      const int i = i0 + it;
+      const int i = next_i(cur);
+      cur = i + 1;
       ok = mbar_wait(&sm.q_full[s], (it / NS) & 1, p.status, abortf, kSiteQFull);
       if (ok) ok = mbar_wait(&sm.s_full, par, p.status, abortf, kSiteSFull);
       ok = __all_sync(0xffffffffu, ok);
@@ -502,8 +520,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
           uint4 v[4];
           uint32_t* w = reinterpret_cast<uint32_t*>(v);
 #pragma unroll
-          for (int e = 0; e < 16; ++e)
-            w[e] = pack_bf16x2(__uint_as_float(a[2 * e]) * mul, __uint_as_float(a[2 * e + 1]) * mul);
+          for (int e = 0; e < 16; ++e)  // no visited query tile: dK = dV = 0
+            w[e] = n_iter == 0 ? 0u
+                               : pack_bf16x2(__uint_as_float(a[2 * e]) * mul,
+                                             __uint_as_float(a[2 * e + 1]) * mul);
           uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
 #pragma unroll
           for (int e = 0; e < 4; ++e) d4[e] = v[e];
@@ -539,11 +559,12 @@ int launch_bwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap
   // 2. main
   if (mask & 2) {
     const size_t smem = sizeof(BwdSmem<D>);
-    if (cudaFuncSetAttribute(fa_bwd_main_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem) != cudaSuccess)
+    auto kern = p.block_mask ? fa_bwd_main_kernel<D, true> : fa_bwd_main_kernel<D, false>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+        cudaSuccess)
       return FA_ERR_LAUNCH;
     const unsigned grid = (unsigned)p.BH * (unsigned)p.n_kv;
-    fa_bwd_main_kernel<D><<<grid, BwdCfg<D>::kThreads, smem, stream>>>(tq, tk, tv, tdo, p);
+    kern<<<grid, BwdCfg<D>::kThreads, smem, stream>>>(tq, tk, tv, tdo, p);
     if (cudaGetLastError() != cudaSuccess) return FA_ERR_LAUNCH;
   }
   // 3. convert

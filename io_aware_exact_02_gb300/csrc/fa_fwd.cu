@@ -102,7 +102,10 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
 // scores (the exponent scale * s is largest where s is smallest).
 // kGeneral: grouped heads, N_q != N_kv or key splits; without it the kernel
 // is the square case (rows = N_q = N_kv, one split) in its simplest form.
-template <int D, bool kNeg, bool kGeneral>
+// kSparse (square case only): a block mask over (128-query tile, 128-key
+// tile) pairs; a pair of query tiles streams the union of their active key
+// tiles and each tile masks out the blocks active only for the other.
+template <int D, bool kNeg, bool kGeneral, bool kSparse>
 __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, const FwdParams p) {
@@ -155,7 +158,17 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
   // An item: K/V head bh, pair `pair` of its packed query rows, key split.
   // Q tile t's rows see key tiles [j0, j0 + n_t[t]) of the split.
   struct Item {
-    int bh, pair, split, row0, j0, n_t[2], nmax;
+    int bh, pair, split, row0, j0, n_t[2], nmax, hi[2];
+  };
+  // Block-sparse: is key tile jj active for query tile t of the item?
+  auto active = [&](const Item& it, int t, int jj) -> bool {
+    return jj < it.hi[t] && p.block_mask[(size_t)(it.row0 / kTile + t) * p.n_kv + jj] != 0;
+  };
+  // The next key tile at or after c that either query tile of the item uses.
+  auto next_tile = [&](const Item& it, int c) -> int {
+    if (!kSparse) return c;
+    while (!(active(it, 0, c) || active(it, 1, c))) ++c;
+    return c;
   };
   auto decode = [&](int idx) -> Item {
     Item it;
@@ -174,9 +187,26 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
       } else {  // rows = N_kv: the causal tile r0/128 ends on the diagonal
         hi = r0 >= p.rows ? 0 : (p.causal ? min(r0 / kTile + 1, p.n_kv) : p.n_kv);
       }
+      it.hi[t] = hi;
       const int n = min(hi, j1) - it.j0;
       it.n_t[t] = n > 0 ? n : 0;
       it.nmax = max(it.nmax, it.n_t[t]);
+    }
+    if (kSparse) {
+      // Both query tiles walk the union of their active key tiles; a tile
+      // with no active key tile at all takes no part.
+      int count = 0;
+      bool any[2] = {false, false};
+      const int top = max(it.hi[0], it.hi[1]);
+      for (int jj = 0; jj < top; ++jj) {
+        const bool a0 = active(it, 0, jj), a1 = active(it, 1, jj);
+        any[0] |= a0;
+        any[1] |= a1;
+        count += (a0 || a1) ? 1 : 0;
+      }
+      it.n_t[0] = any[0] ? count : 0;
+      it.n_t[1] = any[1] ? count : 0;
+      it.nmax = count;
     }
     return it;
   };
@@ -205,7 +235,10 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
           for (int h = 0; h < D / 64; ++h)
             tma_load_3d(sm.q[t] + h * 16384, &tq, &sm.q_full, h * 64, it.row0 + t * kTile, it.bh);
         ++q_issued;
+        int cur = it.j0;
         for (int j = 0; j < it.nmax && ok; ++j) {
+          const int jj = next_tile(it, cur);
+          cur = jj + 1;
           for (int w = 0; w < 2 && ok; ++w, ++c) {
             const int slot = c % S, use = c / S;
             if (use > 0 &&
@@ -216,7 +249,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
             mbar_arrive_expect_tx(&sm.kv_full[slot], Cfg::kTileBytes);
             for (int h = 0; h < D / 64; ++h)
               tma_load_3d(sm.kv[slot] + h * 16384, w == 0 ? &tk : &tv, &sm.kv_full[slot], h * 64,
-                          (it.j0 + j) * kTile, it.bh);
+                          jj * kTile, it.bh);
           }
         }
       }
@@ -366,8 +399,13 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
         lim = kGeneral ? min(max(R % p.Nq + p.causal_off + 1, 0), p.Nkv) : min(R + 1, p.Nkv);
       float m_ref = ninf;
       float l = 0.f;
+      int cur = item.j0;
       for (int j = 0; j < n_t; ++j) {
-        const int jj = item.j0 + j;  // key tile
+        const int jj = next_tile(item, cur);  // key tile
+        cur = jj + 1;
+        // Columns >= tlim of this key tile are masked for this row (all of
+        // them when the block is inactive for this query tile).
+        const int tlim = (kSparse && !active(item, t, jj)) ? 0 : lim - jj * kTile;
         ok = mbar_wait(&sm.s_full[t], s_par, p.status, abortf, kSiteSFull);
         ok = __all_sync(0xffffffffu, ok);  // keep the warp's collective TMEM ops converged
         s_par ^= 1;
@@ -379,9 +417,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
 #pragma unroll
         for (int c = 0; c < 4; ++c) tmem_wait_ld(sr[c]);
 
-        if ((jj + 1) * kTile > lim) {
-          // Keys at columns >= tlim of this tile are masked for this row.
-          const int tlim = lim - jj * kTile;
+        if (tlim < kTile) {
 #pragma unroll
           for (int c = 0; c < 4; ++c)
 #pragma unroll
@@ -579,14 +615,14 @@ __global__ void __launch_bounds__(256) fa_combine_kernel(const FwdParams p) {
   if (lane == 0) p.lse[row] = lse_row;
 }
 
-template <int D, bool kNeg, bool kGeneral>
+template <int D, bool kNeg, bool kGeneral, bool kSparse = false>
 int launch_fwd_dn(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                   const FwdParams& p, cudaStream_t stream) {
   const size_t smem = sizeof(FwdSmem<D>) + 1024;
-  if (cudaFuncSetAttribute(fa_fwd_kernel<D, kNeg, kGeneral>,
+  if (cudaFuncSetAttribute(fa_fwd_kernel<D, kNeg, kGeneral, kSparse>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return FA_ERR_LAUNCH;
-  fa_fwd_kernel<D, kNeg, kGeneral>
+  fa_fwd_kernel<D, kNeg, kGeneral, kSparse>
       <<<(unsigned)p.grid, FwdCfg<D>::kThreads, smem, stream>>>(tq, tk, tv, p);
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_LAUNCH;
   if (p.splits > 1) {
@@ -604,6 +640,10 @@ int launch_fwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap
   // smallest normal positive scale, whose exponents round to exactly 0.
   if (p.scale_log2 == 0.f) p.scale_log2 = 1.17549435e-38f;
   const bool general = p.splits > 1 || p.Nq != p.rows || p.Nkv != p.rows;
+  if (p.block_mask) {  // square case only (checked by the caller)
+    if (p.scale_log2 < 0.f) return launch_fwd_dn<D, true, false, true>(tq, tk, tv, p, stream);
+    return launch_fwd_dn<D, false, false, true>(tq, tk, tv, p, stream);
+  }
   if (general) {
     if (p.scale_log2 < 0.f) return launch_fwd_dn<D, true, true>(tq, tk, tv, p, stream);
     return launch_fwd_dn<D, false, true>(tq, tk, tv, p, stream);

@@ -47,6 +47,7 @@ struct FwdParams {
   float* lse;        // [BH][rows] fp32
   float* o_part;     // splits > 1: [splits][BH][rows][d] fp32, each split's O
   float* lse_part;   // splits > 1: [splits][BH][rows] fp32, each split's lse
+  const uint8_t* block_mask;  // optional [n_kv][n_kv] 0/1 over (query tile, key tile)
   int* status;       // device status word (2 ints: code, site)
   int BH;            // B * H_kv
   int rows;          // packed query rows per K/V head: G * N_q
@@ -108,6 +109,7 @@ struct BwdParams {
   float* delta;      // workspace: [BH][n_kv*128] fp32 (D_i)
   float* lse2;       // workspace: [BH][n_kv*128] fp32 (lse_i * log2 e, +inf past N)
   int* status;
+  const uint8_t* block_mask;  // optional [n_kv][n_kv] 0/1 over (query tile, key tile)
   int BH, N;
   int n_kv;
   int causal;

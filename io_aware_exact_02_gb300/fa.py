@@ -46,6 +46,9 @@ SIGNATURES = {
                            _vp, _sz, _vp, _i]),
     "fa_bwd_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f,
                             _vp]),
+    "fa_fwd_blocksparse": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp, _vp]),
+    "fa_bwd_blocksparse": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i,
+                                _f, _vp, _vp, _sz, _vp]),
     "fa_device_status": (_i, [_vp, _ip]),
     "fa_status_string": (ctypes.c_char_p, [_i]),
     "fa_fwd_schedule": (_i, [_i, _i, _i, _i, _i, _ip, _ip, _ip, _ip, _i]),
@@ -230,6 +233,64 @@ def bwd_noalloc(q, k, v, o, dout, lse, causal: bool = False, scale: float | None
                                dv.data_ptr(), B, H, N, d, int(bool(causal)),
                                ctypes.c_float(scale), _stream_of(q))
     _check("fa_bwd_noalloc", rc)
+    return dq, dk, dv
+
+
+def _check_block_mask(block_mask, N, device):
+    nt = (N + 127) // 128
+    if not isinstance(block_mask, torch.Tensor) or block_mask.device != device:
+        raise ValueError("block_mask must be a tensor on %s" % device)
+    if block_mask.dtype not in (torch.uint8, torch.bool) or tuple(block_mask.shape) != (nt, nt):
+        raise ValueError("block_mask must be uint8 or bool of shape (%d, %d)" % (nt, nt))
+    if not block_mask.is_contiguous():
+        raise ValueError("block_mask must be contiguous")
+
+
+def fwd_blocksparse(q, k, v, block_mask, causal: bool = False, scale: float | None = None,
+                    out=None, lse=None):
+    """Block-sparse forward: key block c is visible to query block r when
+    block_mask[r, c] is nonzero; blocks are 128 rows.  Returns (o, lse)."""
+    B, H, N, d = q.shape
+    scale = default_scale(d) if scale is None else float(scale)
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _check_qkv(name, t, (B, H, N, d))
+    _check_block_mask(block_mask, N, q.device)
+    out = torch.empty_like(q) if out is None else out
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    _check_qkv("out", out, (B, H, N, d))
+    _check_qkv("lse", lse, (B, H, N), torch.float32)
+    rc = load().fa_fwd_blocksparse(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                   lse.data_ptr(), B, H, N, d, int(bool(causal)),
+                                   ctypes.c_float(scale), block_mask.data_ptr(), _stream_of(q))
+    _check("fa_fwd_blocksparse", rc)
+    return out, lse
+
+
+def bwd_blocksparse(q, k, v, o, dout, lse, block_mask, causal: bool = False,
+                    scale: float | None = None, dq=None, dk=None, dv=None, workspace=None):
+    """dq, dk, dv of the block-sparse forward.  Returns (dq, dk, dv)."""
+    B, H, N, d = q.shape
+    scale = default_scale(d) if scale is None else float(scale)
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("dout", dout)):
+        _check_qkv(name, t, (B, H, N, d))
+    _check_qkv("lse", lse, (B, H, N), torch.float32)
+    _check_block_mask(block_mask, N, q.device)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(q) if dk is None else dk
+    dv = torch.empty_like(q) if dv is None else dv
+    for name, t in (("dq", dq), ("dk", dk), ("dv", dv)):
+        _check_qkv(name, t, (B, H, N, d))
+    if workspace is None:
+        workspace = torch.empty(bwd_workspace_size(B, H, N, d), dtype=torch.uint8,
+                                device=q.device)
+    nbytes = workspace.numel() * workspace.element_size()
+    rc = load().fa_bwd_blocksparse(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                   dout.data_ptr(), lse.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                                   dv.data_ptr(), B, H, N, d, int(bool(causal)),
+                                   ctypes.c_float(scale), block_mask.data_ptr(),
+                                   workspace.data_ptr(), nbytes, _stream_of(q))
+    _check("fa_bwd_blocksparse", rc)
     return dq, dk, dv
 
 

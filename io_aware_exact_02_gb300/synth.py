@@ -159,3 +159,51 @@ def draw_gqa(w: GqaWorkload, seed: int = 0, device="cpu"):
     k = torch.randn((w.B, w.Hkv, w.Nkv, w.d), generator=g, device=device).to(torch.bfloat16)
     v = torch.randn((w.B, w.Hkv, w.Nkv, w.d), generator=g, device=device).to(torch.bfloat16)
     return q, k, v
+
+
+@dataclass(frozen=True)
+class BlockSparseWorkload:
+    """Square attention with a 0/1 mask over (128-query block, 128-key block)
+    pairs shared by every head (the block-sparse extension of FlashAttention
+    in cs2680 Lecture 9's reading guide)."""
+    name: str
+    B: int
+    H: int
+    N: int
+    d: int
+    causal: bool
+    density: float
+
+    @property
+    def softmax_scale(self) -> float:
+        return 1.0 / math.sqrt(self.d)
+
+    @property
+    def n_blocks(self) -> int:
+        return -(-self.N // 128)
+
+
+# The headline square shape with a quarter of the blocks active.
+BLOCKSPARSE = BlockSparseWorkload("blocksparse_B8_H16_N8192_d128_density0.25", 8, 16, 8192, 128,
+                                  False, 0.25)
+BLOCKSPARSE_ALL = [BLOCKSPARSE]
+
+
+def blocksparse_by_name(name: str) -> BlockSparseWorkload:
+    for w in BLOCKSPARSE_ALL:
+        if w.name == name:
+            return w
+    raise KeyError(name)
+
+
+def draw_block_mask(n_blocks: int, density: float, seed: int = 0, diagonal: bool = True):
+    """(n_blocks, n_blocks) uint8 on the CPU: each block is 1 with probability
+    ``density`` (torch.rand < density from a CPU generator seeded with
+    ``seed``); with ``diagonal`` the diagonal blocks are 1 as well, so that
+    every query block sees keys under a causal mask."""
+    g = torch.Generator()
+    g.manual_seed(int(seed))
+    m = (torch.rand((n_blocks, n_blocks), generator=g) < density).to(torch.uint8)
+    if diagonal:
+        m.fill_diagonal_(1)
+    return m

@@ -201,3 +201,34 @@ def test_fwd_gqa_argument_errors_launch_nothing(lib):
     assert call(splits=0) == fa.FA_ERR_ARG
     assert call(d=80) == fa.FA_ERR_UNSUPPORTED_D
     assert call(splits=2, Nkv=1000) == fa.FA_ERR_WORKSPACE
+
+
+def test_blocksparse_argument_errors_launch_nothing(lib):
+    def fwd(mask=FAKE, **kw):
+        a = dict(B=1, H=2, N=300, d=64, causal=0)
+        a.update(kw)
+        return lib.fa_fwd_blocksparse(FAKE, FAKE, FAKE, FAKE, FAKE, a["B"], a["H"], a["N"], a["d"],
+                                      a["causal"], ctypes.c_float(0.1), mask, None)
+
+    def bwd(mask=FAKE, **kw):
+        a = dict(B=1, H=2, N=300, d=64, causal=0, ws=FAKE,
+                 wsb=lib.fa_bwd_workspace_size(1, 2, 300, 64))
+        a.update(kw)
+        return lib.fa_bwd_blocksparse(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, a["B"],
+                                      a["H"], a["N"], a["d"], a["causal"], ctypes.c_float(0.1),
+                                      mask, a["ws"], a["wsb"], None)
+
+    assert fwd(mask=None) == fa.FA_ERR_ARG
+    assert bwd(mask=None) == fa.FA_ERR_ARG
+    assert fwd(N=0) == fa.FA_ERR_ARG and bwd(N=0) == fa.FA_ERR_ARG
+    assert fwd(causal=3) == fa.FA_ERR_ARG and bwd(causal=3) == fa.FA_ERR_ARG
+    assert fwd(d=32) == fa.FA_ERR_UNSUPPORTED_D and bwd(d=32) == fa.FA_ERR_UNSUPPORTED_D
+    assert bwd(wsb=16) == fa.FA_ERR_WORKSPACE
+    # Valid arguments reach the device check (no GPU in a CPU-only run).
+    if not torch_cuda_available():
+        assert fwd() == fa.FA_ERR_DEVICE and bwd() == fa.FA_ERR_DEVICE
+
+
+def torch_cuda_available():
+    import torch
+    return torch.cuda.is_available()

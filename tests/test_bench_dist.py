@@ -75,3 +75,15 @@ def test_torchrun_reference_arm_two_ranks():
     assert line["impl"] == "reference" and line["n_gpus"] == 2
     assert line["cpu_baseline"]["kind"] == "oracle"
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["value"] == line["value"]
+
+
+@pytest.mark.parametrize("N,causal", [(1, False), (1, True), (200, False), (200, True),
+                                      (385, True), (385, False)])
+def test_visible_pairs_brute_force(N, causal):
+    import torch
+    from io_aware_exact_02_gb300 import synth
+    nb = -(-N // 128)
+    mask = synth.draw_block_mask(nb, 0.5, seed=N, diagonal=False).tolist()
+    want = sum(1 for i in range(N) for j in range(N)
+               if mask[i // 128][j // 128] and (not causal or j <= i))
+    assert bench.visible_pairs(mask, N, causal) == want
