@@ -12,7 +12,7 @@
  *   Three-step form of attention ("Reading CMU 11-868 LLM Systems:
  *   FlashAttention", section "The scenario", slide page 5):
  *       S = scale * Q K^T,  A = softmax(S) row-wise,  O = A V.
- *   FlashAttention's output is "identical to standard attention" (same
+ *   FlashAttention's output equals standard attention's exactly (same
  *   post, page 15 summary; quidproquo tag page "flashattention", Hung-yi
  *   Lee paragraph), so the oracle is that definition written out, with no
  *   tiling and no online rescaling.
