@@ -207,3 +207,23 @@ def draw_block_mask(n_blocks: int, density: float, seed: int = 0, diagonal: bool
     if diagonal:
         m.fill_diagonal_(1)
     return m
+
+
+def draw_outliers(B: int, H: int, N: int, d: int, seed: int = 0, frac: float = 0.001,
+                  magnitude: float = 10.0, device="cpu"):
+    """(q, k, v) bf16 with simulated outliers, the data on which incoherent
+    processing pays off (CMU 11-868 FlashAttention post, slide page 24; the
+    post gives no recipe, so this is the plainest one).  For each of Q, K, V
+    in turn: x = randn(B, H, N, d); m = rand(B, H, N, d) < frac; entries
+    where m holds are replaced by magnitude * randn(B, H, N, d); all from one
+    generator seeded with ``seed``, in that order, then rounded to bf16."""
+    device = torch.device(device)
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed))
+    out = []
+    for _ in range(3):
+        x = torch.randn((B, H, N, d), generator=g, device=device)
+        m = torch.rand((B, H, N, d), generator=g, device=device) < frac
+        big = torch.randn((B, H, N, d), generator=g, device=device) * magnitude
+        out.append(torch.where(m, big, x).to(torch.bfloat16))
+    return tuple(out)

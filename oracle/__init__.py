@@ -14,7 +14,11 @@ design notes):
   * ``scale`` multiplies Q K^T before the softmax, any finite value;
   * causal masking is square and top-left: row i sees keys j <= i;
   * the backward pass is the textbook softmax Jacobian (the pages print no
-    formula for it).
+    formula for it);
+  * FP8 form: Q and K rotated by the Sylvester Hadamard matrix, one E4M3
+    scale per head and tensor (amax / 448), codes rounded to nearest-even
+    and saturated, the rounding decision taken in fp32, then exact
+    attention over the dequantised tensors with scale / d.
 Parity of the backward pass against the pages themselves is unpinned: the
 pages print no worked gradient example.  It is pinned instead by finite
 differences of the forward pass and by an independent library routine.
@@ -68,6 +72,18 @@ def bind(path: str):
                                               dp, dp]
     lib.oracle_attn_bwd_blockmask.argtypes = [dp, dp, dp, dp, i64, i64, i64, cint, dbl, u8p,
                                               i64, dp, dp, dp]
+    lib.oracle_e4m3_decode.argtypes = [ctypes.c_ubyte]
+    lib.oracle_e4m3_decode.restype = dbl
+    lib.oracle_e4m3_encode.argtypes = [dbl]
+    lib.oracle_e4m3_encode.restype = ctypes.c_ubyte
+    lib.oracle_e4m3_encode_array.argtypes = [dp, i64, u8p]
+    lib.oracle_e4m3_decode_array.argtypes = [u8p, i64, dp]
+    lib.oracle_hadamard.argtypes = [dp, i64, i64, dp]
+    lib.oracle_quantize_e4m3.argtypes = [dp, i64, u8p]
+    lib.oracle_quantize_e4m3.restype = ctypes.c_float
+    fp = ctypes.POINTER(ctypes.c_float)
+    lib.oracle_attn_fwd_fp8.argtypes = [dp, dp, dp, i64, i64, i64, cint, dbl, cint, dp, dp,
+                                        u8p, u8p, u8p, fp]
     lib.oracle_fwd_flops.argtypes = [i64, i64, i64, cint]
     lib.oracle_fwd_flops.restype = dbl
     lib.oracle_recompute_flops.argtypes = [i64, i64]
@@ -78,7 +94,8 @@ def bind(path: str):
               lib.oracle_attn_probs, lib.oracle_attn_bwd,
               lib.oracle_attn_fwd_gqa, lib.oracle_combine_splits,
               lib.oracle_attn_fwd_blockmask, lib.oracle_attn_bwd_blockmask,
-              lib.oracle_set_num_threads):
+              lib.oracle_e4m3_encode_array, lib.oracle_e4m3_decode_array,
+              lib.oracle_hadamard, lib.oracle_attn_fwd_fp8, lib.oracle_set_num_threads):
         f.restype = None
     return lib
 
@@ -239,6 +256,62 @@ def attn_bwd_blockmask(q, k, v, dout, causal: bool, scale: float, block_mask, bl
                                                d, int(bool(causal)), float(scale), bmp, block,
                                                _ptr(dq), _ptr(dk), _ptr(dv))
     return dq, dk, dv
+
+
+def _u8p(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_ubyte))
+
+
+def e4m3_decode(codes, lib=None) -> np.ndarray:
+    """Values (float64) of E4M3 codes (uint8, any shape)."""
+    c = np.ascontiguousarray(codes, dtype=np.uint8)
+    out = np.zeros(c.shape)
+    (lib or _load()).oracle_e4m3_decode_array(_u8p(c), c.size, _ptr(out))
+    return out
+
+
+def e4m3_encode(x, lib=None) -> np.ndarray:
+    """Nearest E4M3 codes (ties to even, saturated to +-448) of float64 x."""
+    x = _f64(x)
+    out = np.zeros(x.shape, dtype=np.uint8)
+    (lib or _load()).oracle_e4m3_encode_array(_ptr(x), x.size, _u8p(out))
+    return out
+
+
+def hadamard(x, lib=None) -> np.ndarray:
+    """x H_d over the last axis (Sylvester Hadamard matrix, entries +-1)."""
+    x = _f64(x)
+    d = x.shape[-1]
+    y = np.zeros(x.shape)
+    (lib or _load()).oracle_hadamard(_ptr(x), x.size // d, d, _ptr(y))
+    return y
+
+
+def quantize_e4m3(x, lib=None):
+    """One-scale E4M3 quantisation of all of x: (codes, descale)."""
+    x = _f64(x)
+    codes = np.zeros(x.shape, dtype=np.uint8)
+    s = (lib or _load()).oracle_quantize_e4m3(_ptr(x), x.size, _u8p(codes))
+    return codes, float(s)
+
+
+def attn_fwd_fp8(q, k, v, causal: bool, scale: float, hadamard: bool, lib=None):
+    """FP8 forward with optional Hadamard rotation of Q and K.
+
+    Returns (o, lse, q8, k8, v8, descale): o (B,H,N,d) and lse (B,H,N) in
+    float64; the E4M3 codes of the (rotated) Q, K and of V as (B,H,N,d)
+    uint8; descale (3, B, H) float32, the per-head scales of Q, K, V."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, H, N, d = _shape4(q)
+    o = np.zeros((B, H, N, d))
+    lse = np.zeros((B, H, N))
+    q8, k8, v8 = (np.zeros((B, H, N, d), dtype=np.uint8) for _ in range(3))
+    ds = np.zeros((3, B, H), dtype=np.float32)
+    (lib or _load()).oracle_attn_fwd_fp8(
+        _ptr(q), _ptr(k), _ptr(v), B * H, N, d, int(bool(causal)), float(scale),
+        int(bool(hadamard)), _ptr(o), _ptr(lse), _u8p(q8), _u8p(k8), _u8p(v8),
+        ds.ctypes.data_as(ctypes.POINTER(ctypes.c_float)))
+    return o, lse, q8, k8, v8, ds
 
 
 def fwd_flops(B: int, H: int, N: int, d: int, causal: bool) -> float:

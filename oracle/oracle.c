@@ -59,6 +59,28 @@
  * scores at -inf, evaluated entry by entry; a row with no visible key has
  * O = 0, lse = -inf and takes no part in the gradients.
  *
+ * FP8 form with incoherent processing (CMU 11-868 FlashAttention post,
+ * FA3 section, slide page 24: quantisation outliers are spread by
+ * multiplying Q and K by the same orthogonal Hadamard matrix, which leaves
+ * Q K^T unchanged).  The steps, in order (oracle_attn_fwd_fp8):
+ *   1. with `hadamard`, every row of Q and of K is multiplied by the
+ *      Sylvester Hadamard matrix H_d (entries (-1)^popcount(i & j), so
+ *      H H^T = d I and (Q H)(K H)^T = d Q K^T); V is not transformed;
+ *   2. each head of each of Q, K, V is quantised to FP8 E4M3 with one
+ *      scale: amax = max |x| over the head, code = E4M3(x * (448 / amax)),
+ *      rounded to nearest-even and saturated to +-448; the dequantised
+ *      value is decode(code) * (amax / 448).  The rounding decision is made
+ *      in fp32 (x, amax, 448 / amax and the product each rounded to fp32),
+ *      the precision of the GPU kernel that takes the same decision;
+ *      amax = 0 gives code 0 and scale 1;
+ *   3. exact attention (the three-step definition above) over the
+ *      dequantised Q, K, V with scale / d under the rotation (scale
+ *      otherwise).
+ * Readings (the pages give none of these details): one scale per head and
+ * tensor; E4M3 in its OCP "fn" form (bias 7, no infinities, largest finite
+ * 448, S.1111.111 is NaN); the softmax probabilities are exact here (the GPU
+ * rounds them to E4M3 as tensor-core operands, which its tolerance covers).
+ *
  * Loops are parallelised with OpenMP over independent rows (forward, dQ) or
  * independent key rows (dK, dV); each output element is computed by one
  * thread with a plain sequential sum, so results do not depend on the thread
@@ -463,4 +485,131 @@ void oracle_attn_bwd_blockmask(const double* q, const double* k, const double* v
     free(lse);
     free(D);
     free(o);
+}
+
+/* ------------------------------------------------------------------ FP8 */
+
+/* Value of an E4M3 code: sign, 4 exponent bits with bias 7, 3 mantissa
+ * bits; exponent field 0 is subnormal (mantissa / 8 * 2^-6); exponent 15
+ * with mantissa 7 is NaN (there is no infinity). */
+double oracle_e4m3_decode(unsigned char c)
+{
+    const int sgn = (c >> 7) & 1, e = (c >> 3) & 15, m = c & 7;
+    double v;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0)
+        v = ldexp((double)m / 8.0, -6);
+    else
+        v = ldexp(1.0 + (double)m / 8.0, e - 7);
+    return sgn ? -v : v;
+}
+
+/* Nearest E4M3 code to x, ties to the even code (even mantissa), magnitudes
+ * above the largest finite value 448 saturated to 448: a plain search over
+ * the 127 non-negative finite codes. */
+unsigned char oracle_e4m3_encode(double x)
+{
+    const int neg = signbit(x) != 0;
+    const double a = fabs(x);
+    int best = 0;
+    double best_err = INFINITY;
+    for (int c = 0; c <= 0x7E; ++c) {
+        const double err = fabs(oracle_e4m3_decode((unsigned char)c) - a);
+        if (err < best_err || (err == best_err && (c & 1) == 0)) {
+            best = c;
+            best_err = err;
+        }
+    }
+    if (a >= 448.0) best = 0x7E;
+    return (unsigned char)(best | (neg ? 0x80 : 0));
+}
+
+/* y = x H_d row by row (rows x d), H_d[i][j] = (-1)^popcount(i & j). */
+void oracle_hadamard(const double* x, int64_t rows, int64_t d, double* y)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int64_t j = 0; j < d; ++j) {
+            double acc = 0.0;
+            for (int64_t i = 0; i < d; ++i) {
+                const int odd = __builtin_popcountll((unsigned long long)(i & j)) & 1;
+                acc += odd ? -x[r * d + i] : x[r * d + i];
+            }
+            y[r * d + j] = acc;
+        }
+    }
+}
+
+/* Quantise n values with one scale (step 2 of the FP8 form): codes[n] and
+ * the dequantisation scale amax / 448 (fp32), returned. */
+float oracle_quantize_e4m3(const double* x, int64_t n, unsigned char* codes)
+{
+    float amax = 0.0f;
+    for (int64_t i = 0; i < n; ++i) {
+        const float a = fabsf((float)x[i]);
+        if (a > amax) amax = a;
+    }
+    if (amax == 0.0f) {
+        for (int64_t i = 0; i < n; ++i) codes[i] = 0;
+        return 1.0f;
+    }
+    const float inv = 448.0f / amax;
+    for (int64_t i = 0; i < n; ++i) {
+        const float y = (float)x[i] * inv;
+        codes[i] = oracle_e4m3_encode((double)y);
+    }
+    return amax / 448.0f;
+}
+
+/* The FP8 forward pass (steps 1-3 of the FP8 form).  q, k, v, o are
+ * [BH][N][d]; q8, k8, v8 receive the codes ([BH][N][d]) and descale the
+ * scales, [3][BH] for Q, K, V. */
+void oracle_attn_fwd_fp8(const double* q, const double* k, const double* v, int64_t BH,
+                         int64_t N, int64_t d, int causal, double scale, int hadamard,
+                         double* o, double* lse, unsigned char* q8, unsigned char* k8,
+                         unsigned char* v8, float* descale)
+{
+    const int64_t n = BH * N * d, per = N * d;
+    double* qh = (double*)malloc(sizeof(double) * (size_t)n);
+    double* kh = (double*)malloc(sizeof(double) * (size_t)n);
+    double* qd = (double*)malloc(sizeof(double) * (size_t)n);
+    double* kd = (double*)malloc(sizeof(double) * (size_t)n);
+    double* vd = (double*)malloc(sizeof(double) * (size_t)n);
+    if (hadamard) {
+        oracle_hadamard(q, BH * N, d, qh);
+        oracle_hadamard(k, BH * N, d, kh);
+    } else {
+        for (int64_t i = 0; i < n; ++i) { qh[i] = q[i]; kh[i] = k[i]; }
+    }
+    for (int64_t h = 0; h < BH; ++h) {
+        const float sq = oracle_quantize_e4m3(qh + h * per, per, q8 + h * per);
+        const float sk = oracle_quantize_e4m3(kh + h * per, per, k8 + h * per);
+        const float sv = oracle_quantize_e4m3(v + h * per, per, v8 + h * per);
+        descale[h] = sq;
+        descale[BH + h] = sk;
+        descale[2 * BH + h] = sv;
+        for (int64_t i = h * per; i < (h + 1) * per; ++i) {
+            qd[i] = oracle_e4m3_decode(q8[i]) * (double)sq;
+            kd[i] = oracle_e4m3_decode(k8[i]) * (double)sk;
+            vd[i] = oracle_e4m3_decode(v8[i]) * (double)sv;
+        }
+    }
+    oracle_attn_fwd(qd, kd, vd, BH, N, d, causal, hadamard ? scale / (double)d : scale, o, lse);
+    free(qh);
+    free(kh);
+    free(qd);
+    free(kd);
+    free(vd);
+}
+
+/* Element-wise oracle_e4m3_encode / oracle_e4m3_decode over arrays. */
+void oracle_e4m3_encode_array(const double* x, int64_t n, unsigned char* out)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < n; ++i) out[i] = oracle_e4m3_encode(x[i]);
+}
+
+void oracle_e4m3_decode_array(const unsigned char* c, int64_t n, double* out)
+{
+    for (int64_t i = 0; i < n; ++i) out[i] = oracle_e4m3_decode(c[i]);
 }

@@ -44,6 +44,15 @@ MUTATIONS = {
     "dV_uses_dS": ("dvj[c] += a * doi[c];", "dvj[c] += ds * doi[c];"),
     "D_drops_probability": ("Di += exp(s[j] - l) * acc;", "Di += acc;"),
     "bwd_causal_start": ("int64_t i0 = causal ? j : 0;", "int64_t i0 = causal ? j + 1 : 0;"),
+    "e4m3_ties_to_odd": ("(err == best_err && (c & 1) == 0)", "(err == best_err && (c & 1) == 1)"),
+    "e4m3_subnormal_exponent": ("v = ldexp((double)m / 8.0, -6);", "v = ldexp((double)m / 8.0, -7);"),
+    "hadamard_no_sign": ("acc += odd ? -x[r * d + i] : x[r * d + i];", "acc += x[r * d + i];"),
+    "fp8_rotate_q_only": ("oracle_hadamard(k, BH * N, d, kh);",
+                          "for (int64_t i = 0; i < n; ++i) kh[i] = k[i];"),
+    "fp8_scale_not_divided_by_d": ("hadamard ? scale / (double)d : scale", "scale"),
+    "fp8_drop_descale": ("kd[i] = oracle_e4m3_decode(k8[i]) * (double)sk;",
+                         "kd[i] = oracle_e4m3_decode(k8[i]);"),
+    "fp8_inverse_scale": ("const float inv = 448.0f / amax;", "const float inv = amax / 448.0f;"),
 }
 
 
@@ -129,6 +138,51 @@ def battery(lib):
     o, lse = oracle.attn_fwd(q, k, v, False, 0.0, lib=lib)
     if np.abs(o - v.mean(2, keepdims=True)).max() > 1e-12 or np.abs(lse - math.log(N)).max() > 1e-12:
         failed.append("scale0")
+    failed += fp8_battery(lib)
+    return failed
+
+
+def fp8_battery(lib):
+    """FP8 pins: the codec against torch, exact quantisation against exact
+    attention with and without the rotation, and quantisation of a tensor
+    whose scale is not 1."""
+    failed = []
+    c = np.arange(256, dtype=np.uint8)
+    ref = torch.tensor(c).view(torch.float8_e4m3fn).double().numpy()
+    dec = oracle.e4m3_decode(c, lib=lib)
+    ok = ~np.isnan(ref)
+    if not np.array_equal(dec[ok], ref[ok]):
+        failed.append("e4m3_decode")
+    finite = ref[:0x7F]
+    mids = (finite[:-1] + finite[1:]) / 2
+    x = np.concatenate([mids, -mids, rnd(500, 40) * 30])
+    x = x.astype(np.float32).astype(np.float64)
+    tref = torch.tensor(x).float().to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    if not np.array_equal(oracle.e4m3_encode(x, lib=lib), tref):
+        failed.append("e4m3_encode")
+    d = 8
+    if not np.array_equal(oracle.hadamard(np.eye(d), lib=lib) @ oracle.hadamard(np.eye(d), lib=lib),
+                          d * np.eye(d)) or oracle.hadamard(np.eye(d), lib=lib)[1, 1] != -1:
+        failed.append("hadamard")
+    rng = np.random.default_rng(41)
+    N8 = 12
+    grid = finite[finite > 0]
+    tq, tk, tv = (rng.choice(grid, size=(1, 1, N8, d)) * rng.choice([-1.0, 1.0], size=(1, 1, N8, d))
+                  for _ in range(3))
+    for t in (tq, tk, tv):
+        t[0, 0, 0, 0] = 448.0
+    f = 2.0 ** -4
+    tq, tk, tv = tq * f, tk * f, tv * f
+    q, k = oracle.hadamard(tq, lib=lib) / d, oracle.hadamard(tk, lib=lib) / d
+    for had, (qq, kk) in ((True, (q, k)), (False, (tq, tk))):
+        o8 = oracle.attn_fwd_fp8(qq, kk, tv, True, 0.3, had, lib=lib)[0]
+        o, _ = oracle.attn_fwd(qq, kk, tv, True, 0.3, lib=lib)
+        if np.abs(o8 - o).max() > 1e-9:
+            failed.append("fp8_exact_%d" % had)
+    codes, s = oracle.quantize_e4m3(tv, lib=lib)
+    if s != np.float32(448.0 * f / 448.0) or not np.array_equal(
+            oracle.e4m3_decode(codes, lib=lib) * s, tv):
+        failed.append("quantize")
     return failed
 
 
