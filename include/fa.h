@@ -170,6 +170,49 @@ int fa_bwd_blocksparse(const void* q, const void* k, const void* v, const void* 
                        void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * FP8 forward pass with incoherent processing (CMU 11-868 FlashAttention
+ * post, FA3 section: FP8 as the low-precision direction, slide page 18, and
+ * the Hadamard rotation of Q and K that spreads outliers, slide page 24).
+ * Square shapes with d = 128 only (FA_ERR_UNSUPPORTED_D otherwise).
+ *
+ * Steps: with hadamard = 1 every row of Q and K is multiplied by the
+ * 128 x 128 Sylvester Hadamard matrix H (entries +-1; (QH)(KH)^T = 128 QK^T);
+ * each head of each of Q, K, V is quantised to E4M3 with one scale,
+ * code = E4M3(x * (448 / amax)) rounded to nearest-even and saturated, amax =
+ * max |x| over the head (amax = 0: codes 0, scale 1); then attention over the
+ * codes: S = scale * (amax_q / 448)(amax_k / 448) * codes_q codes_k^T (/ 128
+ * with the rotation), online softmax as in fa_fwd with P rounded to E4M3 as
+ * the tensor-core operand of O += P V, O scaled by amax_v / 448.  O is bf16,
+ * lse fp32 as in fa_fwd.
+ *
+ * Workspace (caller-owned, 256-byte aligned, fa_fwd_fp8_workspace_size
+ * bytes), in this order with 256-byte aligned parts (offsets from
+ * fa_fp8_workspace_offsets): q8 and k8, the codes of the (rotated) Q and K,
+ * [B][H][N][128] bytes; vt8, the codes of V transposed per head,
+ * [B][H][128][ceil(N/128)*128] bytes (keys past N hold code 0); amax,
+ * [3][B][H] fp32 (Q, K, V, after the rotation).
+ *
+ * fa_fp8_quantize writes the workspace from bf16 q, k, v ([B][H][N][128]);
+ * fa_fwd_fp8_quantized runs the attention kernel over a workspace written
+ * by fa_fp8_quantize with the same sizes and hadamard flag; fa_fwd_fp8 is
+ * the two in sequence on one stream.  Errors as fa_fwd, plus FA_ERR_ARG for
+ * hadamard outside {0, 1}, FA_ERR_WORKSPACE for a missing, misaligned or
+ * small workspace; fa_fp8_workspace_offsets fills offsets[4] (q8, k8, vt8,
+ * amax) or returns an error; fa_fwd_fp8_workspace_size returns 0 for
+ * invalid sizes.
+ */
+size_t fa_fwd_fp8_workspace_size(int B, int H, int N, int d);
+int fa_fp8_workspace_offsets(int B, int H, int N, int d, size_t* offsets);
+int fa_fp8_quantize(const void* q, const void* k, const void* v, int B, int H, int N, int d,
+                    int hadamard, void* workspace, size_t workspace_bytes, void* stream);
+int fa_fwd_fp8_quantized(void* o, float* lse, int B, int H, int N, int d, int causal, float scale,
+                         int hadamard, const void* workspace, size_t workspace_bytes,
+                         void* stream);
+int fa_fwd_fp8(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+               int N, int d, int causal, float scale, int hadamard, void* workspace,
+               size_t workspace_bytes, void* stream);
+
+/*
  * Size of the scratch array fa_bwd_noalloc uses: 32 MiB of static device
  * data on every GPU that loads the library, held until the process exits.
  */

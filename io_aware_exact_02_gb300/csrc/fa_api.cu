@@ -152,7 +152,96 @@ int make_tmap_bhnd(const void* base, int BH, int N, int d, CUtensorMap* out) {
   return r == CUDA_SUCCESS ? FA_OK : FA_ERR_ARG;
 }
 
+int make_tmap_u8(const void* base, int BH, int rows, int inner, CUtensorMap* out) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc;
+  int rc = get_encode(&enc);
+  if (rc != FA_OK) return rc;
+  cuuint64_t dims[3] = {(cuuint64_t)inner, (cuuint64_t)rows, (cuuint64_t)BH};
+  cuuint64_t strides[2] = {(cuuint64_t)inner, (cuuint64_t)rows * inner};
+  cuuint32_t box[3] = {128, kTile, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = enc(out, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides,
+                   box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FA_OK : FA_ERR_ARG;
+}
+
 namespace {
+
+// Shape checks of the FP8 forward pass: the square shape with d = 128.
+int fp8_shape(int B, int H, int N, int d, float scale) {
+  int rc = check_shape(B, H, N, d, scale);
+  if (rc != FA_OK) return rc;
+  if (d != 128) return FA_ERR_UNSUPPORTED_D;
+  if ((long long)B * H * ceil_div(N, kTile) > 0x7fffffffLL) return FA_ERR_ARG;
+  return FA_OK;
+}
+
+int fp8_workspace_ok(const void* workspace, size_t workspace_bytes, const Fp8Workspace& w) {
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
+      workspace_bytes < w.total)
+    return FA_ERR_WORKSPACE;
+  return FA_OK;
+}
+
+// The FP8 attention kernel over a quantised workspace.
+int fwd_fp8_quantized_impl(void* o, float* lse, int B, int H, int N, int d, int causal,
+                           float scale, int hadamard, const void* workspace,
+                           size_t workspace_bytes, void* stream) {
+  if (!o || !lse) return FA_ERR_ARG;
+  if ((causal != 0 && causal != 1) || (hadamard != 0 && hadamard != 1)) return FA_ERR_ARG;
+  int rc = fp8_shape(B, H, N, d, scale);
+  if (rc != FA_OK) return rc;
+  if (!aligned16(o) || !aligned16(lse)) return FA_ERR_ALIGN;
+  const int BH = B * H;
+  const Fp8Workspace w = fp8_workspace_layout(BH, N, d);
+  if ((rc = fp8_workspace_ok(workspace, workspace_bytes, w)) != FA_OK) return rc;
+  DeviceState* ds;
+  if ((rc = device_state(&ds)) != FA_OK) return rc;
+  const char* ws = static_cast<const char*>(workspace);
+  CUtensorMap tq, tk, tv;
+  if ((rc = make_tmap_u8(ws + w.q8, BH, N, d, &tq)) != FA_OK) return rc;
+  if ((rc = make_tmap_u8(ws + w.k8, BH, N, d, &tk)) != FA_OK) return rc;
+  if ((rc = make_tmap_u8(ws + w.vt8, BH, d, ceil_div(N, kTile) * kTile, &tv)) != FA_OK) return rc;
+  FwdParams p;
+  p.o = o;
+  p.lse = lse;
+  p.o_part = nullptr;
+  p.lse_part = nullptr;
+  p.block_mask = nullptr;
+  p.fp8_amax = reinterpret_cast<const float*>(ws + w.amax);
+  p.fp8_hadamard = hadamard;
+  p.status = ds->status;
+  p.BH = BH;
+  p.rows = N;
+  p.Nq = N;
+  p.Nkv = N;
+  p.causal_off = 0;
+  p.n_kv = ceil_div(N, kTile);
+  p.n_pairs = ceil_div(N, kPairRows);
+  p.splits = 1;
+  p.tiles_per_split = p.n_kv;
+  p.causal = causal;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.grid = fwd_grid(BH, p.n_pairs, causal, ds->sm_count);
+  return launch_fwd(tq, tk, tv, p, d, static_cast<cudaStream_t>(stream));
+}
+
+int fp8_quantize_impl(const void* q, const void* k, const void* v, int B, int H, int N, int d,
+                      int hadamard, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!q || !k || !v) return FA_ERR_ARG;
+  if (hadamard != 0 && hadamard != 1) return FA_ERR_ARG;
+  int rc = fp8_shape(B, H, N, d, 1.0f);
+  if (rc != FA_OK) return rc;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v)) return FA_ERR_ALIGN;
+  const int BH = B * H;
+  const Fp8Workspace w = fp8_workspace_layout(BH, N, d);
+  if ((rc = fp8_workspace_ok(workspace, workspace_bytes, w)) != FA_OK) return rc;
+  DeviceState* ds;
+  if ((rc = device_state(&ds)) != FA_OK) return rc;
+  return launch_fp8_quantize(q, k, v, BH, N, hadamard, static_cast<char*>(workspace), w,
+                             static_cast<cudaStream_t>(stream));
+}
 
 // The forward pass over a general shape; block_mask is null for dense attention.
 int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
@@ -180,6 +269,8 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
   p.o_part = nullptr;
   p.lse_part = nullptr;
   p.block_mask = block_mask;
+  p.fp8_amax = nullptr;
+  p.fp8_hadamard = 0;
   if (g.splits > 1) {
     p.o_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + g.ws.o_part);
     p.lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + g.ws.lse_part);
@@ -347,6 +438,49 @@ int fa_bwd_blocksparse(const void* q, const void* k, const void* v, const void* 
   if (!block_mask) return FA_ERR_ARG;
   return fa::bwd_impl(q, k, v, o, dout, lse, dq, dk, dv, B, H, N, d, causal, scale, workspace,
                       workspace_bytes, stream, 7, static_cast<const uint8_t*>(block_mask));
+}
+
+size_t fa_fwd_fp8_workspace_size(int B, int H, int N, int d) {
+  if (fp8_shape(B, H, N, d, 1.0f) != FA_OK) return 0;
+  return fp8_workspace_layout((long long)B * H, N, d).total;
+}
+
+int fa_fp8_workspace_offsets(int B, int H, int N, int d, size_t* offsets) {
+  if (!offsets) return FA_ERR_ARG;
+  int rc = fp8_shape(B, H, N, d, 1.0f);
+  if (rc != FA_OK) return rc;
+  const Fp8Workspace w = fp8_workspace_layout((long long)B * H, N, d);
+  offsets[0] = w.q8;
+  offsets[1] = w.k8;
+  offsets[2] = w.vt8;
+  offsets[3] = w.amax;
+  return FA_OK;
+}
+
+int fa_fp8_quantize(const void* q, const void* k, const void* v, int B, int H, int N, int d,
+                    int hadamard, void* workspace, size_t workspace_bytes, void* stream) {
+  return fp8_quantize_impl(q, k, v, B, H, N, d, hadamard, workspace, workspace_bytes, stream);
+}
+
+int fa_fwd_fp8_quantized(void* o, float* lse, int B, int H, int N, int d, int causal, float scale,
+                         int hadamard, const void* workspace, size_t workspace_bytes,
+                         void* stream) {
+  return fwd_fp8_quantized_impl(o, lse, B, H, N, d, causal, scale, hadamard, workspace,
+                                workspace_bytes, stream);
+}
+
+int fa_fwd_fp8(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+               int N, int d, int causal, float scale, int hadamard, void* workspace,
+               size_t workspace_bytes, void* stream) {
+  if (!o || !lse) return FA_ERR_ARG;
+  if (causal != 0 && causal != 1) return FA_ERR_ARG;
+  int rc = fp8_shape(B, H, N, d, scale);
+  if (rc != FA_OK) return rc;
+  if (!aligned16(o) || !aligned16(lse)) return FA_ERR_ALIGN;
+  rc = fp8_quantize_impl(q, k, v, B, H, N, d, hadamard, workspace, workspace_bytes, stream);
+  if (rc != FA_OK) return rc;
+  return fwd_fp8_quantized_impl(o, lse, B, H, N, d, causal, scale, hadamard, workspace,
+                                workspace_bytes, stream);
 }
 
 int fa_device_status(void* stream, int* site) {

@@ -42,26 +42,31 @@ namespace {
 constexpr float kRescaleSlack = 8.0f;  // log2 units
 constexpr float kLn2 = 0.69314718055994530942f;
 
-template <int D>
+template <int D, bool kFp8 = false>
 struct FwdCfg {
-  static constexpr int kTileBytes = kTile * D * 2;        // one 128 x d bf16 tile
-  static constexpr int kStages = (D == 128) ? 5 : 8;     // K/V ring slots
+  static constexpr int kTileBytes = kTile * D * (kFp8 ? 1 : 2);  // one 128 x d tile
+  static constexpr int kStages = kFp8 ? 10 : ((D == 128) ? 5 : 8);  // K/V ring slots
   static constexpr int kThreads = 320;
   static constexpr uint32_t kTmemCols = 512;
   // TMEM column of S/P and of O for Q tile t.
   static __device__ __forceinline__ uint32_t col_s(int t) { return (uint32_t)t * 128u; }
   static __device__ __forceinline__ uint32_t col_o(int t) { return 256u + (uint32_t)t * D; }
-  static constexpr int kKSteps = D / 16;                 // MMA K-steps of S = Q K^T
+  // MMA K-steps (32 bytes of each operand row per step) of S = Q K^T and
+  // of O += P V.
+  static constexpr int kKSteps = kFp8 ? D / 32 : D / 16;
+  static constexpr int kPvSteps = kFp8 ? kTile / 32 : kTile / 16;
+  // 128-byte TMA boxes per tile row (64 bf16 or 128 8-bit elements each).
+  static constexpr int kBoxes = kFp8 ? D / 128 : D / 64;
 };
 
-template <int D>
+template <int D, bool kFp8 = false>
 struct alignas(1024) FwdSmem {
-  uint8_t q[2][FwdCfg<D>::kTileBytes];
-  uint8_t kv[FwdCfg<D>::kStages][FwdCfg<D>::kTileBytes];
+  uint8_t q[2][FwdCfg<D, kFp8>::kTileBytes];
+  uint8_t kv[FwdCfg<D, kFp8>::kStages][FwdCfg<D, kFp8>::kTileBytes];
   uint64_t q_full;
   uint64_t q_empty;  // both Q tiles consumed by the item's last S product
-  uint64_t kv_full[FwdCfg<D>::kStages];
-  uint64_t kv_empty[FwdCfg<D>::kStages];
+  uint64_t kv_full[FwdCfg<D, kFp8>::kStages];
+  uint64_t kv_empty[FwdCfg<D, kFp8>::kStages];
   uint64_t s_full[2];
   uint64_t p_full[2];
   uint64_t o_full[2];
@@ -105,14 +110,19 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
 // kSparse (square case only): a block mask over (128-query tile, 128-key
 // tile) pairs; a pair of query tiles streams the union of their active key
 // tiles and each tile masks out the blocks active only for the other.
-template <int D, bool kNeg, bool kGeneral, bool kSparse>
-__global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
+// kFp8 (square case, d = 128): Q, K and V^T are E4M3 codes with one scale
+// per head (the FP8 forward pass of the CMU 11-868 FlashAttention post,
+// slide pages 18 and 24); S and O += P V run as kind::f8f6f4 products, P is
+// rounded to E4M3 in tensor memory, and V arrives transposed ([d][keys]) so
+// that both operands of O += P V are K-major.
+template <int D, bool kNeg, bool kGeneral, bool kSparse, bool kFp8>
+__global__ void __launch_bounds__(FwdCfg<D, kFp8>::kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, const FwdParams p) {
-  using Cfg = FwdCfg<D>;
+  using Cfg = FwdCfg<D, kFp8>;
   constexpr int S = Cfg::kStages;
   extern __shared__ uint8_t smem_raw[];
-  FwdSmem<D>& sm = *reinterpret_cast<FwdSmem<D>*>(
+  FwdSmem<D, kFp8>& sm = *reinterpret_cast<FwdSmem<D, kFp8>*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   volatile int* abortf = &sm.abort_flag;
   const int tid = threadIdx.x;
@@ -232,7 +242,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
         }
         mbar_arrive_expect_tx(&sm.q_full, 2 * Cfg::kTileBytes);
         for (int t = 0; t < 2; ++t)
-          for (int h = 0; h < D / 64; ++h)
+          for (int h = 0; h < Cfg::kBoxes; ++h)
             tma_load_3d(sm.q[t] + h * 16384, &tq, &sm.q_full, h * 64, it.row0 + t * kTile, it.bh);
         ++q_issued;
         int cur = it.j0;
@@ -247,9 +257,13 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
               break;
             }
             mbar_arrive_expect_tx(&sm.kv_full[slot], Cfg::kTileBytes);
-            for (int h = 0; h < D / 64; ++h)
-              tma_load_3d(sm.kv[slot] + h * 16384, w == 0 ? &tk : &tv, &sm.kv_full[slot], h * 64,
-                          jj * kTile, it.bh);
+            if (kFp8 && w == 1) {  // V^T tile: d rows of 128 keys
+              tma_load_3d(sm.kv[slot], &tv, &sm.kv_full[slot], jj * kTile, 0, it.bh);
+            } else {
+              for (int h = 0; h < Cfg::kBoxes; ++h)
+                tma_load_3d(sm.kv[slot] + h * 16384, w == 0 ? &tk : &tv, &sm.kv_full[slot],
+                            h * 64, jj * kTile, it.bh);
+            }
           }
         }
       }
@@ -263,8 +277,8 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
     if (lane_id() == 0) {
-      const uint32_t id_s = idesc_bf16(128, 128, false, false);
-      const uint32_t id_pv = idesc_bf16(128, D, false, true);
+      const uint32_t id_s = kFp8 ? idesc_e4m3(128, 128) : idesc_bf16(128, 128, false, false);
+      const uint32_t id_pv = kFp8 ? idesc_e4m3(128, D) : idesc_bf16(128, D, false, true);
       const uint32_t q_addr[2] = {smem_u32(sm.q[0]), smem_u32(sm.q[1])};
       uint32_t p_par[2] = {0, 0};
       int cb = 0;       // K/V loads consumed before the current item
@@ -275,9 +289,14 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
       auto issue_s = [&](int t, int kslot) {
         const uint32_t kb = smem_u32(sm.kv[kslot]);
 #pragma unroll 1
-        for (int kk = 0; kk < Cfg::kKSteps; ++kk)
-          mma_ss(tmem + Cfg::col_s(t), kmajor_desc(q_addr[t], kk), kmajor_desc(kb, kk), id_s,
-                 kk > 0);
+        for (int kk = 0; kk < Cfg::kKSteps; ++kk) {
+          if constexpr (kFp8)
+            mma_ss_f8(tmem + Cfg::col_s(t), kmajor_desc(q_addr[t], kk), kmajor_desc(kb, kk), id_s,
+                      kk > 0);
+          else
+            mma_ss(tmem + Cfg::col_s(t), kmajor_desc(q_addr[t], kk), kmajor_desc(kb, kk), id_s,
+                   kk > 0);
+        }
         tc_commit(&sm.s_full[t]);
       };
       // O_t += P_t V; the item's first product overwrites O_t, so it waits
@@ -290,9 +309,15 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
         }
         const uint32_t vb = smem_u32(sm.kv[vslot]);
 #pragma unroll 1
-        for (int kk = 0; kk < kTile / 16; ++kk)
-          mma_ts(tmem + Cfg::col_o(t), tmem + Cfg::col_s(t) + kk * 8, mnmajor_desc(vb, kk), id_pv,
-                 (accumulate || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < Cfg::kPvSteps; ++kk) {
+          // P occupies 8 TMEM columns per K-step: 16 bf16 or 32 E4M3 keys.
+          if constexpr (kFp8)
+            mma_ts_f8(tmem + Cfg::col_o(t), tmem + Cfg::col_s(t) + kk * 8, kmajor_desc(vb, kk),
+                      id_pv, (accumulate || kk > 0) ? 1u : 0u);
+          else
+            mma_ts(tmem + Cfg::col_o(t), tmem + Cfg::col_s(t) + kk * 8, mnmajor_desc(vb, kk),
+                   id_pv, (accumulate || kk > 0) ? 1u : 0u);
+        }
         return true;
       };
       auto wait_full = [&](int cnt) -> bool {
@@ -375,7 +400,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
     const int t = warp >> 2;             // which Q tile
     const int r = tid & 127;             // row within the tile
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-    const float c2 = p.scale_log2;  // nonzero: a zero scale arrives as a tiny positive one
+    float c2 = p.scale_log2;  // nonzero: a zero scale arrives as a tiny positive one
     // A masked score is replaced by the value that loses every max (min)
     // and whose exponent c2 * s is -inf, so its probability is exactly 0.
     const float neutral = kNeg ? __int_as_float(0x7f800000) : __int_as_float(0xff800000);
@@ -392,6 +417,19 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
       const Item item = decode(idx);
       const int bh = item.bh;
       const int n_t = item.n_t[t];
+      float o_mul = 1.f;  // FP8: the V scale, applied with 1 / l
+      if constexpr (kFp8) {
+        // Scores of codes carry the Q and K scales (and d, the squared norm
+        // of the Hadamard rotation's rows); fold them into the exponent.
+        auto descale = [&](int which) {
+          const float a = p.fp8_amax[which * p.BH + bh];
+          return a == 0.f ? 1.f : a / 448.f;
+        };
+        c2 = p.scale_log2 * descale(0) * descale(1);
+        if (p.fp8_hadamard) c2 *= 1.f / (float)D;
+        if (c2 == 0.f) c2 = kNeg ? -1.17549435e-38f : 1.17549435e-38f;
+        o_mul = descale(2);
+      }
       const int R = item.row0 + t * kTile + r;  // packed query row of this K/V head
       // Keys visible to this row: [0, lim) (bottom-right causal alignment).
       int lim = p.Nkv;
@@ -458,6 +496,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
         uint64_t ls4[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) ls4[u] = 0;
+        uint32_t pk8[kFp8 ? 32 : 1];  // FP8: all 128 probabilities, four per column
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           uint32_t pk[32];
@@ -473,11 +512,20 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
               const float p0 = ex2_approx(x0);
               const float p1 = ex2_approx(x1);
               ls4[(i >> 1) & 3] = f2_add(ls4[(i >> 1) & 3], f2_pack(p0, p1));
-              pk[c2i * 16 + i / 2] = pack_bf16x2(p0, p1);
+              if constexpr (kFp8) {
+                const uint32_t two = pack_e4m3x2(p0, p1);
+                if (((i >> 1) & 1) == 0)
+                  pk8[(c * 32 + i) >> 2] = two;
+                else
+                  pk8[(c * 32 + i) >> 2] |= two << 16;
+              } else {
+                pk[c2i * 16 + i / 2] = pack_bf16x2(p0, p1);
+              }
             }
           }
-          tmem_st32(colS + h * 32, pk);
+          if constexpr (!kFp8) tmem_st32(colS + h * 32, pk);
         }
+        if constexpr (kFp8) tmem_st32(colS, pk8);
         ls4[0] = f2_add(f2_add(ls4[0], ls4[1]), f2_add(ls4[2], ls4[3]));
         float lsa, lsb;
         f2_unpack(ls4[0], lsa, lsb);
@@ -507,7 +555,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
       // Epilogue: O / l (0 for a row that saw no key) and lse; with several
       // key splits, the split's normalised fp32 O and its lse, for the combine.
       const bool any = l > 0.f;
-      const float inv_l = any ? 1.f / l : 0.f;
+      const float inv_l = any ? o_mul / l : 0.f;
       const bool valid = R < p.rows;
       const size_t row_g = (size_t)bh * p.rows + R;
 #pragma unroll
@@ -615,15 +663,15 @@ __global__ void __launch_bounds__(256) fa_combine_kernel(const FwdParams p) {
   if (lane == 0) p.lse[row] = lse_row;
 }
 
-template <int D, bool kNeg, bool kGeneral, bool kSparse = false>
+template <int D, bool kNeg, bool kGeneral, bool kSparse = false, bool kFp8 = false>
 int launch_fwd_dn(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                   const FwdParams& p, cudaStream_t stream) {
-  const size_t smem = sizeof(FwdSmem<D>) + 1024;
-  if (cudaFuncSetAttribute(fa_fwd_kernel<D, kNeg, kGeneral, kSparse>,
+  const size_t smem = sizeof(FwdSmem<D, kFp8>) + 1024;
+  if (cudaFuncSetAttribute(fa_fwd_kernel<D, kNeg, kGeneral, kSparse, kFp8>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return FA_ERR_LAUNCH;
-  fa_fwd_kernel<D, kNeg, kGeneral, kSparse>
-      <<<(unsigned)p.grid, FwdCfg<D>::kThreads, smem, stream>>>(tq, tk, tv, p);
+  fa_fwd_kernel<D, kNeg, kGeneral, kSparse, kFp8>
+      <<<(unsigned)p.grid, FwdCfg<D, kFp8>::kThreads, smem, stream>>>(tq, tk, tv, p);
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_LAUNCH;
   if (p.splits > 1) {
     const long long threads = (long long)p.BH * p.rows * 32;
@@ -640,6 +688,13 @@ int launch_fwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap
   // smallest normal positive scale, whose exponents round to exactly 0.
   if (p.scale_log2 == 0.f) p.scale_log2 = 1.17549435e-38f;
   const bool general = p.splits > 1 || p.Nq != p.rows || p.Nkv != p.rows;
+  if (p.fp8_amax) {  // square case, d = 128 only (checked by the caller)
+    if constexpr (D == 128) {
+      if (p.scale_log2 < 0.f) return launch_fwd_dn<D, true, false, false, true>(tq, tk, tv, p, stream);
+      return launch_fwd_dn<D, false, false, false, true>(tq, tk, tv, p, stream);
+    }
+    return FA_ERR_UNSUPPORTED_D;
+  }
   if (p.block_mask) {  // square case only (checked by the caller)
     if (p.scale_log2 < 0.f) return launch_fwd_dn<D, true, false, true>(tq, tk, tv, p, stream);
     return launch_fwd_dn<D, false, false, true>(tq, tk, tv, p, stream);

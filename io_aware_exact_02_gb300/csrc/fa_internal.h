@@ -48,6 +48,8 @@ struct FwdParams {
   float* o_part;     // splits > 1: [splits][BH][rows][d] fp32, each split's O
   float* lse_part;   // splits > 1: [splits][BH][rows] fp32, each split's lse
   const uint8_t* block_mask;  // optional [n_kv][n_kv] 0/1 over (query tile, key tile)
+  const float* fp8_amax;      // FP8 forward: [3][BH] amax of the (rotated) Q, K and of V
+  int fp8_hadamard;           // FP8 forward: Q and K were rotated by H_d
   int* status;       // device status word (2 ints: code, site)
   int BH;            // B * H_kv
   int rows;          // packed query rows per K/V head: G * N_q
@@ -154,6 +156,36 @@ inline BwdWorkspace bwd_workspace_layout(long long BH, int N, int d) {
   w.total = w.lse2 + up(rows * sizeof(float));
   return w;
 }
+
+// Byte offsets of the FP8 forward pass's workspace (d = 128): the E4M3
+// codes of the (rotated) Q and K, [BH][N][d]; the codes of V transposed per
+// head, [BH][d][n_kv * 128] (keys past N are code 0); then the per-head
+// absolute maxima of Q, K and V, [3][BH] fp32.  Parts 256-byte aligned.
+struct Fp8Workspace {
+  size_t q8, k8, vt8, amax, total;
+};
+inline Fp8Workspace fp8_workspace_layout(long long BH, int N, int d) {
+  auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
+  const size_t qk = (size_t)BH * (size_t)N * (size_t)d;
+  const size_t vt = (size_t)BH * (size_t)d * (size_t)ceil_div(N, kTile) * kTile;
+  Fp8Workspace w;
+  w.q8 = 0;
+  w.k8 = up(qk);
+  w.vt8 = w.k8 + up(qk);
+  w.amax = w.vt8 + up(vt);
+  w.total = w.amax + up((size_t)3 * BH * sizeof(float));
+  return w;
+}
+
+// Quantise bf16 Q, K, V ([BH][N][128]) into the FP8 workspace `ws` laid out
+// by fp8_workspace_layout; with `hadamard` the rows of Q and K are first
+// multiplied by the 128 x 128 Sylvester Hadamard matrix.
+int launch_fp8_quantize(const void* q, const void* k, const void* v, int BH, int N, int hadamard,
+                        char* ws, const Fp8Workspace& layout, cudaStream_t stream);
+
+// A rank-3 tensor map over a [BH][rows][inner] array of bytes: box
+// (128, 128, 1), 128-byte swizzle, zero fill outside.
+int make_tmap_u8(const void* base, int BH, int rows, int inner, CUtensorMap* out);
 
 // phase_mask: bit 0 prep, bit 1 main, bit 2 convert.
 int launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,

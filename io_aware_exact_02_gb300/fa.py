@@ -49,6 +49,11 @@ SIGNATURES = {
     "fa_fwd_blocksparse": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp, _vp]),
     "fa_bwd_blocksparse": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i,
                                 _f, _vp, _vp, _sz, _vp]),
+    "fa_fwd_fp8_workspace_size": (_sz, [_i, _i, _i, _i]),
+    "fa_fp8_workspace_offsets": (_i, [_i, _i, _i, _i, ctypes.POINTER(ctypes.c_size_t)]),
+    "fa_fp8_quantize": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _sz, _vp]),
+    "fa_fwd_fp8_quantized": (_i, [_vp, _vp, _i, _i, _i, _i, _i, _f, _i, _vp, _sz, _vp]),
+    "fa_fwd_fp8": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _vp, _sz, _vp]),
     "fa_device_status": (_i, [_vp, _ip]),
     "fa_status_string": (ctypes.c_char_p, [_i]),
     "fa_fwd_schedule": (_i, [_i, _i, _i, _i, _i, _ip, _ip, _ip, _ip, _i]),
@@ -292,6 +297,76 @@ def bwd_blocksparse(q, k, v, o, dout, lse, block_mask, causal: bool = False,
                                    workspace.data_ptr(), nbytes, _stream_of(q))
     _check("fa_bwd_blocksparse", rc)
     return dq, dk, dv
+
+
+def fwd_fp8_workspace_size(B: int, H: int, N: int, d: int) -> int:
+    return int(load().fa_fwd_fp8_workspace_size(B, H, N, d))
+
+
+def fp8_workspace_offsets(B: int, H: int, N: int, d: int):
+    """Byte offsets of (q8, k8, vt8, amax) in the FP8 workspace."""
+    off = (ctypes.c_size_t * 4)()
+    _check("fa_fp8_workspace_offsets", load().fa_fp8_workspace_offsets(B, H, N, d, off))
+    return tuple(int(x) for x in off)
+
+
+def _fp8_workspace(workspace, B, H, N, d, device):
+    need = fwd_fp8_workspace_size(B, H, N, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=device)
+    return workspace, workspace.numel() * workspace.element_size()
+
+
+def fp8_quantize(q, k, v, hadamard: bool = True, workspace=None):
+    """Quantise bf16 q, k, v to the FP8 workspace (see fa_fp8_quantize).
+    Returns the workspace (uint8 tensor)."""
+    B, H, N, d = q.shape
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _check_qkv(name, t, (B, H, N, d))
+    workspace, nbytes = _fp8_workspace(workspace, B, H, N, d, q.device)
+    rc = load().fa_fp8_quantize(q.data_ptr(), k.data_ptr(), v.data_ptr(), B, H, N, d,
+                                int(bool(hadamard)), workspace.data_ptr(), nbytes, _stream_of(q))
+    _check("fa_fp8_quantize", rc)
+    return workspace
+
+
+def fwd_fp8_quantized(workspace, B, H, N, d, causal: bool = False, scale: float | None = None,
+                      hadamard: bool = True, out=None, lse=None):
+    """FP8 attention over a workspace written by fp8_quantize.  Returns (o, lse)."""
+    scale = default_scale(d) if scale is None else float(scale)
+    dev = workspace.device
+    out = torch.empty((B, H, N, d), dtype=torch.bfloat16, device=dev) if out is None else out
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    _check_qkv("out", out, (B, H, N, d))
+    _check_qkv("lse", lse, (B, H, N), torch.float32)
+    rc = load().fa_fwd_fp8_quantized(out.data_ptr(), lse.data_ptr(), B, H, N, d,
+                                     int(bool(causal)), ctypes.c_float(scale),
+                                     int(bool(hadamard)), workspace.data_ptr(),
+                                     workspace.numel() * workspace.element_size(),
+                                     _stream_of(out))
+    _check("fa_fwd_fp8_quantized", rc)
+    return out, lse
+
+
+def fwd_fp8(q, k, v, causal: bool = False, scale: float | None = None, hadamard: bool = True,
+            out=None, lse=None, workspace=None):
+    """FP8 forward pass (quantise, then attention).  Returns (o, lse)."""
+    B, H, N, d = q.shape
+    scale = default_scale(d) if scale is None else float(scale)
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _check_qkv(name, t, (B, H, N, d))
+    out = torch.empty_like(q) if out is None else out
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    _check_qkv("out", out, (B, H, N, d))
+    _check_qkv("lse", lse, (B, H, N), torch.float32)
+    workspace, nbytes = _fp8_workspace(workspace, B, H, N, d, q.device)
+    rc = load().fa_fwd_fp8(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                           lse.data_ptr(), B, H, N, d, int(bool(causal)), ctypes.c_float(scale),
+                           int(bool(hadamard)), workspace.data_ptr(), nbytes, _stream_of(q))
+    _check("fa_fwd_fp8", rc)
+    return out, lse
 
 
 def device_status(stream=None):

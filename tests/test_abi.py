@@ -232,3 +232,34 @@ def test_blocksparse_argument_errors_launch_nothing(lib):
 def torch_cuda_available():
     import torch
     return torch.cuda.is_available()
+
+
+def test_fp8_sizes_and_argument_errors(lib):
+    size = lib.fa_fwd_fp8_workspace_size(2, 3, 300, 128)
+    off = (ctypes.c_size_t * 4)()
+    assert lib.fa_fp8_workspace_offsets(2, 3, 300, 128, off) == fa.FA_OK
+    qk = 2 * 3 * 300 * 128
+    up = lambda x: (x + 255) // 256 * 256  # noqa: E731
+    assert list(off) == [0, up(qk), 2 * up(qk), 2 * up(qk) + up(2 * 3 * 128 * 384)]
+    assert size == off[3] + up(3 * 6 * 4)
+    assert lib.fa_fwd_fp8_workspace_size(1, 1, 128, 64) == 0
+    assert lib.fa_fp8_workspace_offsets(1, 1, 128, 64, off) == fa.FA_ERR_UNSUPPORTED_D
+    assert lib.fa_fp8_workspace_offsets(1, 1, 128, 128, None) == fa.FA_ERR_ARG
+
+    def call(**kw):
+        a = dict(B=1, H=1, N=128, d=128, causal=0, had=1, ws=FAKE,
+                 wsb=lib.fa_fwd_fp8_workspace_size(1, 1, 128, 128))
+        a.update(kw)
+        return lib.fa_fwd_fp8(FAKE, FAKE, FAKE, FAKE, FAKE, a["B"], a["H"], a["N"], a["d"],
+                              a["causal"], ctypes.c_float(0.1), a["had"], a["ws"], a["wsb"], None)
+
+    assert call(d=64) == fa.FA_ERR_UNSUPPORTED_D
+    assert call(had=2) == fa.FA_ERR_ARG
+    assert call(causal=5) == fa.FA_ERR_ARG
+    assert call(ws=None) == fa.FA_ERR_WORKSPACE
+    assert call(ws=FAKE + 128) == fa.FA_ERR_WORKSPACE
+    assert call(wsb=100) == fa.FA_ERR_WORKSPACE
+    assert lib.fa_fwd_fp8_quantized(FAKE, FAKE, 1, 1, 128, 128, 0, ctypes.c_float(0.1), 1, None,
+                                    0, None) == fa.FA_ERR_WORKSPACE
+    assert lib.fa_fp8_quantize(None, FAKE, FAKE, 1, 1, 128, 128, 1, FAKE, 1 << 20,
+                               None) == fa.FA_ERR_ARG
