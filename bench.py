@@ -576,6 +576,95 @@ def run_blocksparse(args, wl, rank, world, local_rank):
     return 0
 
 
+FP8_WORKLOAD = dict(name="fp8_hadamard_B8_H16_N8192_d128", B=8, H=16, N=8192, d=128,
+                    causal=False)
+
+
+def run_fp8(args, w, rank, world, local_rank):
+    """FP8 forward step: quantisation (with the Hadamard rotation) + FP8
+    attention, TFLOPS by the forward FLOP count."""
+    import torch
+    from io_aware_exact_02_gb300 import fa, synth
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    fa.load()
+    B, H, N, d, causal = w["B"], w["H"], w["N"], w["d"], w["causal"]
+    wl = synth.Workload(w["name"], B, H, N, d, causal)
+    q, k, v, _ = synth.draw_workload(wl, seed=rank_seed(args.seed, rank), device=dev,
+                                     with_dout=False)
+    ws = torch.empty(fa.fwd_fp8_workspace_size(B, H, N, d), dtype=torch.uint8, device=dev)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+    q_ms, a_ms = [], []
+
+    def step(record=False):
+        if record:
+            ev[0].record(stream)
+        fa.fp8_quantize(q, k, v, hadamard=True, workspace=ws)
+        if record:
+            ev[1].record(stream)
+        fa.fwd_fp8_quantized(ws, B, H, N, d, causal=causal, scale=wl.softmax_scale,
+                             hadamard=True, out=o, lse=lse)
+        if record:
+            ev[2].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    fa.check_device_status()
+    sampler = ClockSampler(gpu_selector(local_rank))
+    sampler.start()
+    time.sleep(0.3)
+    barrier()
+    torch.cuda.synchronize(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    clocks = sampler.stop()
+    for _ in range(3):
+        step(record=True)
+        torch.cuda.synchronize(dev)
+        q_ms.append(ev[0].elapsed_time(ev[1]))
+        a_ms.append(ev[1].elapsed_time(ev[2]))
+    fa.check_device_status()
+    sec = reduce_max(e0.elapsed_time(e1) / 1e3)
+    per_step = sec / args.steps
+    flops = fwd_flops(B, H, N, d, causal)
+    value = world * flops / per_step / 1e12
+    peaks, peak_kind = load_peaks()
+    # FP8 dense tensor rate = 2x bf16 (nominal 4.5 vs 2.25 PFLOP/s) applied
+    # to the measured bf16 burst figure.
+    peak = 2.0 * float(peaks["bf16_tflops"])
+    t_q, t_a = statistics.median(q_ms) / 1e3, statistics.median(a_ms) / 1e3
+    in_bytes = 3.0 * B * H * N * d * 2
+    if rank == 0:
+        print(json.dumps({
+            "metric": "FP8 attention forward TFLOPS (E4M3, Hadamard rotation, quantisation "
+                      "included)",
+            "value": value, "unit": "TFLOPS", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": per_step * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "e4m3", "data": "synthetic",
+            "config": {"workload": w["name"], "B": B, "H": H, "N": N, "d": d, "causal": causal,
+                       "step": "fa_fp8_quantize + fa_fwd_fp8_quantized",
+                       "l2": "inputs larger than L2"},
+            "clocks": clocks, "gpu_launches": args.steps * 3,
+            "roofline": {"bound": "tensor", "kernel": "fa_fwd_kernel (FP8)",
+                         "achieved": flops / t_a / 1e12, "peak": peak, "unit": "TFLOP/s",
+                         "frac": flops / t_a / 1e12 / peak,
+                         "peak_kind": "%s burst bf16 x 2 (nominal fp8/bf16 ratio)" % peak_kind,
+                         "traffic": profiled_traffic("fa_fwd_kernel_fp8_" + w["name"])},
+            "attention_ms": t_a * 1e3, "quantize_ms": t_q * 1e3,
+            "quantize_gbs_inputs_read": in_bytes / t_q / 1e9}), flush=True)
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -616,6 +705,12 @@ def main(argv=None):
                                   "the reference arm times the square workloads only"}))
                 return 0
             return run_gqa(args, synth.gqa_by_name(args.workload), rank, world, local_rank)
+        if args.workload == FP8_WORKLOAD["name"]:
+            if args.impl == "reference":
+                print(json.dumps({"impl": "reference", "unavailable":
+                                  "the reference arm times the square workloads only"}))
+                return 0
+            return run_fp8(args, FP8_WORKLOAD, rank, world, local_rank)
         if args.workload in [b.name for b in synth.BLOCKSPARSE_ALL]:
             if args.impl == "reference":
                 print(json.dumps({"impl": "reference", "unavailable":
