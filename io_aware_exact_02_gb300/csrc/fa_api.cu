@@ -287,7 +287,8 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
   p.tiles_per_split = g.tiles_per_split;
   p.causal = causal;
   p.scale_log2 = scale * 1.4426950408889634f;
-  p.grid = fwd_grid(g.BH, g.n_pairs * g.splits, causal, ds->sm_count);
+  // Block-sparse items differ in cost like causal ones: one CTA per item.
+  p.grid = fwd_grid(g.BH, g.n_pairs * g.splits, causal || block_mask != nullptr, ds->sm_count);
   return launch_fwd(tq, tk, tv, p, d, static_cast<cudaStream_t>(stream));
 }
 

@@ -264,9 +264,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
   auto active_i = [&](int i) -> bool {
     return !kSparse || p.block_mask[(size_t)i * p.n_kv + j] != 0;
   };
-  // The next query tile at or after c that this key tile visits.
+  // The next query tile at or after c that this key tile visits (callers
+  // ask only for tiles that exist; the scan stops at the last tile anyway).
   auto next_i = [&](int c) -> int {
-    while (!active_i(c)) ++c;
+    while (c < p.n_kv && !active_i(c)) ++c;
     return c;
   };
   int n_iter = p.n_kv - i0;

@@ -109,7 +109,8 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
 // is the square case (rows = N_q = N_kv, one split) in its simplest form.
 // kSparse (square case only): a block mask over (128-query tile, 128-key
 // tile) pairs; a pair of query tiles streams the union of their active key
-// tiles and each tile masks out the blocks active only for the other.
+// tiles once, and each tile takes S and P V products only on its own active
+// tiles.
 // kFp8 (square case, d = 128): Q, K and V^T are E4M3 codes with one scale
 // per head (the FP8 forward pass of the CMU 11-868 FlashAttention post,
 // slide pages 18 and 24); S and O += P V run as kind::f8f6f4 products, P is
@@ -166,7 +167,9 @@ __global__ void __launch_bounds__(FwdCfg<D, kFp8>::kThreads, 1)
     return (k & 1) ? base + (G - 1 - (int)blockIdx.x) : base + (int)blockIdx.x;
   };
   // An item: K/V head bh, pair `pair` of its packed query rows, key split.
-  // Q tile t's rows see key tiles [j0, j0 + n_t[t]) of the split.
+  // Q tile t's rows see key tiles [j0, j0 + n_t[t]) of the split.  Block-
+  // sparse: the item streams nmax key tiles (the union of both Q tiles'
+  // active tiles, in key order), of which Q tile t is active on n_t[t].
   struct Item {
     int bh, pair, split, row0, j0, n_t[2], nmax, hi[2];
   };
@@ -174,10 +177,18 @@ __global__ void __launch_bounds__(FwdCfg<D, kFp8>::kThreads, 1)
   auto active = [&](const Item& it, int t, int jj) -> bool {
     return jj < it.hi[t] && p.block_mask[(size_t)(it.row0 / kTile + t) * p.n_kv + jj] != 0;
   };
-  // The next key tile at or after c that either query tile of the item uses.
+  // The next key tile at or after c that either query tile of the item uses
+  // (that query tile t uses, for next_tile_t); callers ask only for tiles
+  // that exist, and the scan stops at the item's last visible tile anyway.
   auto next_tile = [&](const Item& it, int c) -> int {
     if (!kSparse) return c;
-    while (!(active(it, 0, c) || active(it, 1, c))) ++c;
+    const int top = max(it.hi[0], it.hi[1]);
+    while (c < top && !(active(it, 0, c) || active(it, 1, c))) ++c;
+    return c;
+  };
+  auto next_tile_t = [&](const Item& it, int t, int c) -> int {
+    if (!kSparse) return c;
+    while (c < it.hi[t] && !active(it, t, c)) ++c;
     return c;
   };
   auto decode = [&](int idx) -> Item {
@@ -203,19 +214,16 @@ __global__ void __launch_bounds__(FwdCfg<D, kFp8>::kThreads, 1)
       it.nmax = max(it.nmax, it.n_t[t]);
     }
     if (kSparse) {
-      // Both query tiles walk the union of their active key tiles; a tile
-      // with no active key tile at all takes no part.
+      // The union stream's length and each query tile's share of it.
       int count = 0;
-      bool any[2] = {false, false};
       const int top = max(it.hi[0], it.hi[1]);
+      it.n_t[0] = it.n_t[1] = 0;
       for (int jj = 0; jj < top; ++jj) {
         const bool a0 = active(it, 0, jj), a1 = active(it, 1, jj);
-        any[0] |= a0;
-        any[1] |= a1;
+        it.n_t[0] += a0 ? 1 : 0;
+        it.n_t[1] += a1 ? 1 : 0;
         count += (a0 || a1) ? 1 : 0;
       }
-      it.n_t[0] = any[0] ? count : 0;
-      it.n_t[1] = any[1] ? count : 0;
       it.nmax = count;
     }
     return it;
@@ -334,57 +342,128 @@ __global__ void __launch_bounds__(FwdCfg<D, kFp8>::kThreads, 1)
         if (idx >= num_items) continue;
         const Item it = decode(idx);
         const int nmax = it.nmax;
-        // A Q tile without keys is final at once (its rows get O = 0).
-        for (int t = 0; t < 2; ++t)
-          if (it.n_t[t] == 0) tc_commit(&sm.o_full[t]);
-        if (nmax == 0) {
-          ++n_done;
-          continue;
-        }
-        ok = mbar_wait(&sm.q_full, q_used & 1, p.status, abortf, kSiteQFull);
-        if (ok) ok = wait_full(cb);
-        if (ok) {
-          tc_fence_after();
+        if constexpr (!kSparse) {
+          // A Q tile without keys is final at once (its rows get O = 0).
           for (int t = 0; t < 2; ++t)
-            if (it.n_t[t] > 0) issue_s(t, cb % S);
-          tc_commit(&sm.kv_empty[cb % S]);
-          if (nmax == 1) tc_commit(&sm.q_empty);
-        }
-        // Key tile j: PV_t(j-1) then S_t(j) for each Q tile that has them.
-        for (int j = 1; j < nmax && ok; ++j) {
-          const int kc = cb + 2 * j, vc = cb + 2 * j - 1;
-          ok = wait_full(kc) && wait_full(vc);
-          if (!ok) break;
-          for (int t = 0; t < 2 && ok; ++t) {
-            if (j - 1 >= it.n_t[t]) continue;
-            ok = wait_p(t);
-            if (!ok) break;
+            if (it.n_t[t] == 0) tc_commit(&sm.o_full[t]);
+          if (nmax == 0) {
+            ++n_done;
+            continue;
+          }
+          ok = mbar_wait(&sm.q_full, q_used & 1, p.status, abortf, kSiteQFull);
+          if (ok) ok = wait_full(cb);
+          if (ok) {
             tc_fence_after();
-            ok = issue_pv(t, vc % S, j - 1 > 0);
+            for (int t = 0; t < 2; ++t)
+              if (it.n_t[t] > 0) issue_s(t, cb % S);
+            tc_commit(&sm.kv_empty[cb % S]);
+            if (nmax == 1) tc_commit(&sm.q_empty);
+          }
+          // Key tile j: PV_t(j-1) then S_t(j) for each Q tile that has them.
+          for (int j = 1; j < nmax && ok; ++j) {
+            const int kc = cb + 2 * j, vc = cb + 2 * j - 1;
+            ok = wait_full(kc) && wait_full(vc);
             if (!ok) break;
-            if (j < it.n_t[t]) {
-              issue_s(t, kc % S);
-            } else {
-              tc_commit(&sm.o_full[t]);  // tile t has no more keys
+            for (int t = 0; t < 2 && ok; ++t) {
+              if (j - 1 >= it.n_t[t]) continue;
+              ok = wait_p(t);
+              if (!ok) break;
+              tc_fence_after();
+              ok = issue_pv(t, vc % S, j - 1 > 0);
+              if (!ok) break;
+              if (j < it.n_t[t]) {
+                issue_s(t, kc % S);
+              } else {
+                tc_commit(&sm.o_full[t]);  // tile t has no more keys
+              }
             }
-          }
-          if (!ok) break;
-          tc_commit(&sm.kv_empty[vc % S]);
-          tc_commit(&sm.kv_empty[kc % S]);
-          if (j == nmax - 1) tc_commit(&sm.q_empty);  // last product reading Q
-        }
-        if (ok) {
-          const int vc = cb + 2 * nmax - 1;
-          ok = wait_full(vc);
-          for (int t = 0; t < 2 && ok; ++t) {
-            if (it.n_t[t] != nmax) continue;
-            ok = wait_p(t);
             if (!ok) break;
-            tc_fence_after();
-            ok = issue_pv(t, vc % S, nmax - 1 > 0);
-            if (ok) tc_commit(&sm.o_full[t]);
+            tc_commit(&sm.kv_empty[vc % S]);
+            tc_commit(&sm.kv_empty[kc % S]);
+            if (j == nmax - 1) tc_commit(&sm.q_empty);  // last product reading Q
           }
-          if (ok) tc_commit(&sm.kv_empty[vc % S]);
+          if (ok) {
+            const int vc = cb + 2 * nmax - 1;
+            ok = wait_full(vc);
+            for (int t = 0; t < 2 && ok; ++t) {
+              if (it.n_t[t] != nmax) continue;
+              ok = wait_p(t);
+              if (!ok) break;
+              tc_fence_after();
+              ok = issue_pv(t, vc % S, nmax - 1 > 0);
+              if (ok) tc_commit(&sm.o_full[t]);
+            }
+            if (ok) tc_commit(&sm.kv_empty[vc % S]);
+          }
+        } else {
+          // Block-sparse: the stream is the union of both Q tiles' active key
+          // tiles; Q tile t takes S and P V products only on its own.  Bit t
+          // of act_next(u) says whether it does at stream position u (called
+          // once for each u = 0 .. nmax-1, in order).
+          int scan = it.j0;
+          auto act_next = [&]() -> int {
+            const int key = next_tile(it, scan);
+            scan = key + 1;
+            return (active(it, 0, key) ? 1 : 0) | (active(it, 1, key) ? 2 : 0);
+          };
+          auto takes = [](int t, int a) -> bool { return ((a >> t) & 1) != 0; };
+          int a_prev = 0, a_cur = 0;
+          int pv_done[2] = {0, 0};  // P V products issued per Q tile
+          // A Q tile without keys is final at once (its rows get O = 0).
+          for (int t = 0; t < 2; ++t)
+            if (it.n_t[t] == 0) tc_commit(&sm.o_full[t]);
+          if (nmax == 0) {
+            ++n_done;
+            continue;
+          }
+          ok = mbar_wait(&sm.q_full, q_used & 1, p.status, abortf, kSiteQFull);
+          if (ok) ok = wait_full(cb);
+          if (ok) {
+            tc_fence_after();
+            a_cur = act_next();
+            for (int t = 0; t < 2; ++t)
+              if (takes(t, a_cur)) issue_s(t, cb % S);
+            tc_commit(&sm.kv_empty[cb % S]);
+            if (nmax == 1) tc_commit(&sm.q_empty);
+          }
+          // Key tile j: PV_t(j-1) then S_t(j) for each Q tile that has them.
+          for (int j = 1; j < nmax && ok; ++j) {
+            const int kc = cb + 2 * j, vc = cb + 2 * j - 1;
+            ok = wait_full(kc) && wait_full(vc);
+            if (!ok) break;
+            a_prev = a_cur;
+            a_cur = act_next();
+            for (int t = 0; t < 2 && ok; ++t) {
+              // P V for the tile at position j-1 if Q tile t took its S, then
+              // S at position j if Q tile t is active there.
+              if (takes(t, a_prev)) {
+                ok = wait_p(t);
+                if (!ok) break;
+                tc_fence_after();
+                ok = issue_pv(t, vc % S, pv_done[t] > 0);
+                if (!ok) break;
+                if (++pv_done[t] == it.n_t[t]) tc_commit(&sm.o_full[t]);  // no more keys
+              }
+              if (takes(t, a_cur)) issue_s(t, kc % S);
+            }
+            if (!ok) break;
+            tc_commit(&sm.kv_empty[vc % S]);
+            tc_commit(&sm.kv_empty[kc % S]);
+            if (j == nmax - 1) tc_commit(&sm.q_empty);  // last product reading Q
+          }
+          if (ok) {
+            const int vc = cb + 2 * nmax - 1;
+            ok = wait_full(vc);
+            for (int t = 0; t < 2 && ok; ++t) {
+              if (!takes(t, a_cur)) continue;  // a_cur: position nmax-1
+              ok = wait_p(t);
+              if (!ok) break;
+              tc_fence_after();
+              ok = issue_pv(t, vc % S, pv_done[t] > 0);
+              if (ok) tc_commit(&sm.o_full[t]);
+            }
+            if (ok) tc_commit(&sm.kv_empty[vc % S]);
+          }
         }
         cb += 2 * nmax;
         ++q_used;
@@ -439,11 +518,10 @@ __global__ void __launch_bounds__(FwdCfg<D, kFp8>::kThreads, 1)
       float l = 0.f;
       int cur = item.j0;
       for (int j = 0; j < n_t; ++j) {
-        const int jj = next_tile(item, cur);  // key tile
+        const int jj = next_tile_t(item, t, cur);  // key tile
         cur = jj + 1;
-        // Columns >= tlim of this key tile are masked for this row (all of
-        // them when the block is inactive for this query tile).
-        const int tlim = (kSparse && !active(item, t, jj)) ? 0 : lim - jj * kTile;
+        // Columns >= tlim of this key tile are masked for this row.
+        const int tlim = lim - jj * kTile;
         ok = mbar_wait(&sm.s_full[t], s_par, p.status, abortf, kSiteSFull);
         ok = __all_sync(0xffffffffu, ok);  // keep the warp's collective TMEM ops converged
         s_par ^= 1;
