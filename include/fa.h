@@ -249,6 +249,18 @@ int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, c
  */
 int fa_device_status(void* stream, int* site);
 
+/*
+ * Failure-detection self test (no counterpart on the pages): launches one
+ * CTA whose thread waits, through the same bounded-wait path the kernels
+ * use, on a shared-memory barrier that nothing completes.  After
+ * timeout_us microseconds (1 .. 1000000) the wait gives up, records
+ * FA_ERR_TIMEOUT with site FA_SITE_SELFTEST in the status word and the
+ * kernel returns; the context stays usable.  Returns FA_ERR_ARG for a
+ * timeout outside the range, else as a launch.
+ */
+#define FA_SITE_SELFTEST 901
+int fa_selftest_timeout(int timeout_us, void* stream);
+
 /* A static, human-readable description of a status code. */
 const char* fa_status_string(int status);
 

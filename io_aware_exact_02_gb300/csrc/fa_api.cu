@@ -10,6 +10,7 @@
 #include <mutex>
 
 #include "fa_internal.h"
+#include "sm100_ptx.cuh"
 
 namespace fa {
 
@@ -150,6 +151,25 @@ int make_tmap_bhnd(const void* base, int BH, int N, int d, CUtensorMap* out) {
                    strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? FA_OK : FA_ERR_ARG;
+}
+
+// The self test's kernel: one thread waits on a barrier nothing arrives on
+// until the limit passes, then records the timeout like any kernel wait.
+__global__ void fa_selftest_timeout_kernel(int* status, unsigned long long limit_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x != 0) return;
+  mbar_init(&bar, 1);
+  fence_mbar_init();
+  abort_flag = 0;
+  const uint32_t a = smem_u32(&bar);
+  const unsigned long long t0 = globaltimer_ns();
+  while (!mbar_try_wait(a, 0)) {
+    if (globaltimer_ns() - t0 > limit_ns) {
+      report_timeout(status, &abort_flag, FA_SITE_SELFTEST);
+      return;
+    }
+  }
 }
 
 int make_tmap_u8(const void* base, int BH, int rows, int inner, CUtensorMap* out) {
@@ -502,6 +522,16 @@ int fa_device_status(void* stream, int* site) {
   }
   if (site) *site = h[1];
   return h[0];
+}
+
+int fa_selftest_timeout(int timeout_us, void* stream) {
+  if (timeout_us < 1 || timeout_us > 1000000) return FA_ERR_ARG;
+  DeviceState* ds;
+  int rc = device_state(&ds);
+  if (rc != FA_OK) return rc;
+  fa_selftest_timeout_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
+      ds->status, (unsigned long long)timeout_us * 1000ull);
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
 int fa_fwd_schedule(int B, int H, int N, int causal, int num_ctas, int* item_bh, int* item_pair,

@@ -55,6 +55,7 @@ SIGNATURES = {
     "fa_fwd_fp8_quantized": (_i, [_vp, _vp, _i, _i, _i, _i, _i, _f, _i, _vp, _sz, _vp]),
     "fa_fwd_fp8": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _vp, _sz, _vp]),
     "fa_device_status": (_i, [_vp, _ip]),
+    "fa_selftest_timeout": (_i, [_i, _vp]),
     "fa_status_string": (ctypes.c_char_p, [_i]),
     "fa_fwd_schedule": (_i, [_i, _i, _i, _i, _i, _ip, _ip, _ip, _ip, _i]),
     "fa_snake_assign": (_i, [_i, _i, _ip]),
@@ -375,6 +376,16 @@ def device_status(stream=None):
     site = ctypes.c_int(0)
     code = load().fa_device_status(s, ctypes.byref(site))
     return int(code), int(site.value)
+
+
+FA_SITE_SELFTEST = 901
+
+
+def selftest_timeout(timeout_us: int = 20000):
+    """Launch the failure-detection self test on the current stream (see
+    fa_selftest_timeout); read the result with device_status()."""
+    s = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    _check("fa_selftest_timeout", load().fa_selftest_timeout(int(timeout_us), s))
 
 
 def check_device_status(stream=None):

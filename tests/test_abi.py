@@ -263,3 +263,10 @@ def test_fp8_sizes_and_argument_errors(lib):
                                     0, None) == fa.FA_ERR_WORKSPACE
     assert lib.fa_fp8_quantize(None, FAKE, FAKE, 1, 1, 128, 128, 1, FAKE, 1 << 20,
                                None) == fa.FA_ERR_ARG
+
+
+def test_selftest_timeout_arguments(lib):
+    assert lib.fa_selftest_timeout(0, None) == fa.FA_ERR_ARG
+    assert lib.fa_selftest_timeout(1000001, None) == fa.FA_ERR_ARG
+    if not torch_cuda_available():
+        assert lib.fa_selftest_timeout(1000, None) == fa.FA_ERR_DEVICE
