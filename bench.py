@@ -7,9 +7,10 @@ d = 128 (B=8, H=16, N=8192, non-causal, scale 1/sqrt(d)).
 Prints one JSON line (rank 0).  FLOPs follow the pages' count: forward
 4*B*H*N^2*d (two S x S x d matmuls per head, cs2680 Lecture 9 sec. 9.2),
 halved when causal; backward 2.5x the forward.  ``value`` is whole-job
-TFLOPS with the inputs resident in HBM; ``e2e`` is the same metric with the
-step's inputs copied from pinned host memory and its outputs copied back
-inside the timed region.  Every rank (one per GPU, launched by torchrun)
+TFLOPS with the inputs resident in HBM; ``e2e`` is the same metric with each
+step's inputs copied from pinned host memory and all its outputs copied back
+inside the timed region, pipelined as a user streaming batches would run it
+(step k+1's upload and step k-1's download overlap step k's kernels).  Every rank (one per GPU, launched by torchrun)
 runs its own independent batch (weak scaling, no data-path collective);
 timing is the max over ranks, exchanged over gloo.
 
@@ -317,32 +318,60 @@ def run_gpu(args, w, rank, world, local_rank):
         hlse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
         hdq, hdk, hdv = (torch.empty(q.shape, dtype=q.dtype).pin_memory() for _ in range(3))
 
-        def e2e_step():
-            for dst, src in ((q, hq), (k, hk), (v, hv), (do, hdo)):
-                dst.copy_(src, non_blocking=True)
-            fa.fwd(q, k, v, causal=causal, scale=scale, out=o, lse=lse)
-            fa.bwd(q, k, v, o, do, lse, causal=causal, scale=scale, dq=dq, dk=dk, dv=dv,
-                   workspace=ws)
-            for dst, src in ((ho, o), (hlse, lse), (hdq, dq), (hdk, dk), (hdv, dv)):
-                dst.copy_(src, non_blocking=True)
+        # Pipelined like a user streaming batches: two sets of device
+        # buffers; step k's inputs go up on one stream and its results come
+        # back on another while the compute stream runs step k-1 / k+1.  Every
+        # step still copies its own inputs in and all of its outputs out
+        # inside the timed region.
+        sets = [(q, k, v, do, o, lse, dq, dk, dv, ws)]
+        sets.append(tuple(torch.empty_like(t) for t in sets[0]))
+        up, comp, down = (torch.cuda.Stream(dev) for _ in range(3))
 
-        e2e_step()
+        def e2e_run(n):
+            done_down = [None, None]  # set b's last D2H (its buffers are free after it)
+            start = torch.cuda.Event(enable_timing=True)
+            end = torch.cuda.Event(enable_timing=True)
+            start.record(up)
+            for step in range(n):
+                b = step % 2
+                bq, bk, bv, bdo, bo, blse, bdq, bdk, bdv, bws = sets[b]
+                if done_down[b] is not None:
+                    up.wait_event(done_down[b])
+                with torch.cuda.stream(up):
+                    for dst, src in ((bq, hq), (bk, hk), (bv, hv), (bdo, hdo)):
+                        dst.copy_(src, non_blocking=True)
+                    loaded = torch.cuda.Event()
+                    loaded.record(up)
+                comp.wait_event(loaded)
+                with torch.cuda.stream(comp):
+                    fa.fwd(bq, bk, bv, causal=causal, scale=scale, out=bo, lse=blse)
+                    fa.bwd(bq, bk, bv, bo, bdo, blse, causal=causal, scale=scale, dq=bdq, dk=bdk,
+                           dv=bdv, workspace=bws)
+                    computed = torch.cuda.Event()
+                    computed.record(comp)
+                down.wait_event(computed)
+                with torch.cuda.stream(down):
+                    for dst, src in ((ho, bo), (hlse, blse), (hdq, bdq), (hdk, bdk), (hdv, bdv)):
+                        dst.copy_(src, non_blocking=True)
+                    done_down[b] = torch.cuda.Event()
+                    done_down[b].record(down)
+            end.record(down)
+            return start, end
+
+        e2e_run(2)
         torch.cuda.synchronize(dev)
         barrier()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(e2e_steps):
-            e2e_step()
-        e1.record(stream)
+        e0, e1 = e2e_run(e2e_steps)
         torch.cuda.synchronize(dev)
         barrier()
-        fa.check_device_status()
+        fa.check_device_status(stream=comp.cuda_stream)
         e2e_sec = reduce_max(e0.elapsed_time(e1) / 1e3)
         h2d = 4 * in_bytes
         d2h = 4 * in_bytes + lse.numel() * 4
         e2e = {"value": aggregate((ff + bf) * e2e_steps, world, e2e_sec), "unit": UNIT,
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps}
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+               "pipelined": "H2D of step k+1 and D2H of step k-1 overlap step k's kernels "
+                            "(two device buffer sets, three streams)"}
 
     # ------------------------------------------------------------ roofline
     peaks, peak_kind = load_peaks()
@@ -680,7 +709,7 @@ def main(argv=None):
                     help="heads of the workload the cpu_baseline leg times (GPU arm)")
     ap.add_argument("--ref-heads", type=int, default=1,
                     help="heads of the workload per step of the reference arm")
-    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--e2e-steps", type=int, default=8)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
