@@ -10,9 +10,10 @@
 //     dQ = scale dS K,  dK = scale dS^T Q.
 //
 // Three kernels:
-//   1. prep: per row D_i, lse_i * log2(e) into the workspace (padded rows get
-//      D = 0, lse = +inf so that their probabilities are exactly 0), and the
-//      fp32 dQ accumulator zeroed.  HBM-bound.
+//   1. prep: per row -D_i and -lse_i * log2(e) into the workspace, negated
+//      so that the main kernel adds them (padded rows get 0 and -inf, which
+//      makes their probabilities exactly 0), and the fp32 dQ accumulator
+//      zeroed.  HBM-bound.
 //   2. main: one CTA per (head, 128-key tile j).  K_j, V_j stay in shared
 //      memory; dK_j, dV_j accumulate in tensor memory while the CTA walks the
 //      query tiles i (all of them, or i >= j under a causal mask).  Per step:
@@ -27,17 +28,19 @@
 //                          workspace, by the compute warpgroups
 //   3. convert: dQ = bf16(scale * accumulator).
 //
-// Warp roles of the main kernel (320 threads):
-//   warps 0-7  compute: two warpgroups, each owning 64 of the 128 query
-//              columns (thread r owns key row r of the tile): P, dS, then
-//              half of dQ_i's columns from TMEM to the fp32 accumulator with
-//              atomic adds; finally the dV (warpgroup 0) / dK (warpgroup 1)
-//              epilogue
-//   warp 8     TMA producer;  warp 9 MMA issuer and TMEM owner
-// Tensor memory: [0,128) S^T, with P^T (bf16 pairs) over columns 0-31
-// (queries 0-63) and 64-95 (queries 64-127) and dS^T over columns 32-63 and
-// 96-127, so that dV += P^T dO and dK += dS^T Q take their A operand from
-// tensor memory; [128,256) dP^T, then dQ; [256,256+d) dV; [256+d, 256+2d) dK.
+// Warp roles of the main kernel (576 threads):
+//   warps 0-15 compute: four warpgroups, warpgroup g owning query columns
+//              [32g, 32g+32) (thread r owns key row r of the tile): P, dS,
+//              then d/4 of dQ_i's columns from TMEM to the fp32 accumulator
+//              with atomic adds; finally the epilogue (warpgroups 0-1 store
+//              halves of dV, 2-3 halves of dK).  Four compute warps per SM
+//              sub-partition hide the latency of the exponent and dS phases
+//              better than two (measured +3% at d = 128, +7% at d = 64).
+//   warp 16    TMA producer;  warp 17 MMA issuer and TMEM owner
+// Tensor memory: [0,128) S^T; warpgroup g's 32 columns [32g, 32g+32) take
+// P^T (bf16 pairs) over their first 16 and dS^T over the last 16, so that
+// dV += P^T dO and dK += dS^T Q take their A operand from tensor memory;
+// [128,256) dP^T, then dQ; [256,256+d) dV; [256+d, 256+2d) dK.
 #include "fa_internal.h"
 #include "sm100_ptx.cuh"
 
@@ -50,7 +53,10 @@ template <int D>
 struct BwdCfg {
   static constexpr int kTileBytes = kTile * D * 2;  // one 128 x d bf16 tile
   static constexpr int kStages = 2;                  // Q/dO ring
-  static constexpr int kThreads = 320;  // 2 compute warpgroups, producer, MMA
+  static constexpr int kWG = 4;                      // compute warpgroups
+  static constexpr int kQ = kTile / kWG;             // query columns per warpgroup
+  static constexpr int kThreads = kWG * 128 + 64;    // compute, producer, MMA
+  static constexpr int kWarpLoad = kWG * 4, kWarpMma = kWG * 4 + 1;
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D;
 };
@@ -72,7 +78,6 @@ struct BwdSmem {
   int abort_flag;
 };
 
-constexpr int kWarpLoad = 8, kWarpMma = 9;
 
 enum : int {
   kSiteKvFull = 201, kSiteQFull, kSiteQEmpty, kSiteSFull, kSiteDpFull, kSitePReady,
@@ -174,8 +179,8 @@ __global__ void __launch_bounds__(256) fa_bwd_prep_kernel(const BwdParams p) {
   if (in_range) {
     if (sub == 0) {
       const size_t ri = (size_t)bh * npad + row;
-      p.delta[ri] = acc;
-      p.lse2[ri] = row < p.N ? p.lse[(size_t)bh * p.N + row] * kLog2e : __int_as_float(0x7f800000);
+      p.delta[ri] = -acc;
+      p.lse2[ri] = row < p.N ? -(p.lse[(size_t)bh * p.N + row] * kLog2e) : __int_as_float(0xff800000);
     }
     // Zero this row of the dQ accumulator: D floats, 4 per lane-slot.
     for (int c4 = sub; c4 < D / 4; c4 += kLanesPerRow)
@@ -217,6 +222,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
                        const BwdParams p) {
   using Cfg = BwdCfg<D>;
   constexpr int NS = Cfg::kStages;
+  constexpr int kWarpLoad = Cfg::kWarpLoad, kWarpMma = Cfg::kWarpMma;
+  constexpr int kWG = Cfg::kWG, kQ = Cfg::kQ;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // The swizzled tiles need 1024-byte alignment; the dynamic window starts
   // there on this architecture, and the size leaves no slack to realign.
@@ -240,10 +247,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     }
     mbar_init(&sm.s_full, 1);
     mbar_init(&sm.dp_full, 1);
-    mbar_init(&sm.p_ready, 256);
-    mbar_init(&sm.ds_ready, 256);
+    mbar_init(&sm.p_ready, kWG * 128);
+    mbar_init(&sm.ds_ready, kWG * 128);
     mbar_init(&sm.dq_full, 1);
-    mbar_init(&sm.dq_empty, 256);
+    mbar_init(&sm.dq_empty, kWG * 128);
     mbar_init(&sm.acc_full, 1);
     mbar_init(&sm.drain, 1);
     sm.abort_flag = 0;
@@ -348,7 +355,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         tc_fence_after();
 #pragma unroll 1
         for (int kk = 0; kk < kTile / 16; ++kk)
-          mma_ts(tmem + Cfg::kColDV, tmem + Cfg::kColS + (kk >> 2) * 64 + (kk & 3) * 8,
+          mma_ts(tmem + Cfg::kColDV, tmem + Cfg::kColS + (kk * 16 / kQ) * kQ + (kk * 16 % kQ) / 2,
                  mnmajor_desc(dob, kk), id_acc, (it > 0 || kk > 0) ? 1u : 0u);
         // dK += dS^T Q_i ; dQ_i = dS K_j
         ok = mbar_wait(&sm.ds_ready, par, p.status, abortf, kSiteDsReady);
@@ -356,7 +363,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         tc_fence_after();
 #pragma unroll 1
         for (int kk = 0; kk < kTile / 16; ++kk)
-          mma_ts(tmem + Cfg::kColDK, tmem + Cfg::kColS + 32 + (kk >> 2) * 64 + (kk & 3) * 8,
+          mma_ts(tmem + Cfg::kColDK,
+                 tmem + Cfg::kColS + kQ / 2 + (kk * 16 / kQ) * kQ + (kk * 16 % kQ) / 2,
                  mnmajor_desc(qb, kk), id_acc, (it > 0 || kk > 0) ? 1u : 0u);
         tc_commit(&sm.q_empty[s]);
 #pragma unroll 1
@@ -369,22 +377,19 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       drain_wait(&sm.drain, 0);
     }
     __syncwarp();
-  } else if (warp < 8) {
+  } else if (warp < kWG * 4) {
     // ------------------------------------------------------------ compute
-    // Warpgroup g handles query columns [64g, 64g + 64) of the tile; thread
-    // r of either warpgroup owns key row r (TMEM lane r).
+    // Warpgroup g handles query columns [kQ g, kQ g + kQ) of the tile;
+    // thread r of every warpgroup owns key row r (TMEM lane r).
     const int g = warp >> 2;
     const int r = tid & 127;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-    const uint32_t colS = tmem + lane_base + Cfg::kColS + g * 64;
-    const uint32_t colDP = tmem + lane_base + Cfg::kColDP + g * 64;
-    const uint32_t colDQ = tmem + lane_base + Cfg::kColDP + g * (D / 2);
-    const float c2 = p.scale_log2;  // nonzero: a zero scale arrives as a tiny positive one
-    // A masked score is replaced by the value whose exponent c2 * s is -inf.
+    const uint32_t colS = tmem + lane_base + Cfg::kColS + g * kQ;
+    const uint32_t colDP = tmem + lane_base + Cfg::kColDP + g * kQ;
+    const uint32_t colDQ = tmem + lane_base + Cfg::kColDP + g * (D / kWG);
+    const float c2 = p.scale_log2;
     const float neutral = c2 < 0.f ? __int_as_float(0x7f800000) : __int_as_float(0xff800000);
     const int kv_row = j * kTile + r;
-    uint32_t held[32];
-    float* held_base = nullptr;  // dQ columns waiting to be added (see the drain)
     bool ok = true;
     int cur = i0;
     for (int it = 0; it < n_iter; ++it) {
@@ -397,123 +402,112 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
-      uint32_t sr[2][32];
-      tmem_ld32(colS, sr[0]);
-      tmem_ld32(colS + 32, sr[1]);
-      tmem_wait_ld(sr[0]);
-      tmem_wait_ld(sr[1]);
-      if (p.causal && i == j) {
-        // Diagonal tile: key row r is masked for query columns < r.
-#pragma unroll
-        for (int c = 0; c < 2; ++c)
-#pragma unroll
-          for (int e = 0; e < 32; ++e)
-            if (r > g * 64 + c * 32 + e) sr[c][e] = __float_as_uint(neutral);
+      uint32_t sr[kQ];
+      {
+        uint32_t (&h)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[0]);
+        static_assert(kQ == 32, "the compute code is written for 32 query columns per warpgroup");
+        tmem_ld32(colS, h);
+        tmem_wait_ld(h);
       }
-      // lse2 pairs as packed f32x2 (8-byte aligned shared loads).
-      const uint64_t* lse2x2 = reinterpret_cast<const uint64_t*>(sm.lse2[s] + g * 64);
+      if (p.causal && i == j) {
+#pragma unroll
+        for (int e = 0; e < kQ; ++e)
+          if (r > g * kQ + e) sr[e] = __float_as_uint(neutral);
+      }
+      const uint64_t* lse2x2 = reinterpret_cast<const uint64_t*>(sm.lse2[s] + g * kQ);
       const uint64_t c2x2 = f2_pack(c2, c2);
-      const uint64_t minus1 = f2_pack(-1.f, -1.f);
-      uint32_t pk[32];  // P^T for this warpgroup's 64 query columns, bf16 pairs
+      uint32_t pk[kQ / 2];
 #pragma unroll
-      for (int c = 0; c < 2; ++c)
-#pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          // c2 * s - lse2 = fma(s, c2, -lse2), two columns per instruction.
-          float x0, x1;
-          f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1])), c2x2,
-                           f2_mul(lse2x2[(c * 32 + e) / 2], minus1)),
-                    x0, x1);
-          pk[c * 16 + e / 2] = pack_bf16x2(ex2_approx(x0), ex2_approx(x1));
-        }
-      // Over the first 32 of this warpgroup's own S columns (already read).
-      tmem_st32(colS, pk);
+      for (int e = 0; e < kQ; e += 2) {
+        float x0, x1;
+        f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), c2x2,
+                         lse2x2[e / 2]),
+                  x0, x1);
+        pk[e / 2] = pack_bf16x2(ex2_approx(x0), ex2_approx(x1));
+      }
+      tmem_st16(colS, pk);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&sm.p_ready);
-      if (held_base) {
-        add_dq_chunk(held_base, held);
-        held_base = nullptr;
-      }
 
       ok = mbar_wait(&sm.dp_full, par, p.status, abortf, kSiteDpFull);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
-      uint32_t dp[2][32];
-      tmem_ld32(colDP, dp[0]);
-      tmem_ld32(colDP + 32, dp[1]);
-      tmem_wait_ld(dp[0]);
-      tmem_wait_ld(dp[1]);
-      const uint64_t* dlx2 = reinterpret_cast<const uint64_t*>(sm.delta[s] + g * 64);
-      // dS^T row r, query columns [64g, 64g+64) = column block g of the
-      // 128B-swizzled [key][query] tile: eight 16-byte chunks.
-      uint8_t* ds_row = sm.ds + g * 16384 + r * 128;
-      uint32_t dsw[32];  // dS^T row, bf16 pairs: also the A operand of dK in TMEM
+      uint32_t dp[kQ];
+      {
+        uint32_t (&h)[32] = *reinterpret_cast<uint32_t(*)[32]>(&dp[0]);
+        tmem_ld32(colDP, h);
+        tmem_wait_ld(h);
+      }
+      const uint64_t* dlx2 = reinterpret_cast<const uint64_t*>(sm.delta[s] + g * kQ);
+      // dS^T row r, query columns [kQ g, kQ g + kQ): in the 128B-swizzled
+      // [key][query] tile, column block (kQ g) / 64, 16-byte chunks from
+      // ((kQ g) % 64) / 8.
+      uint8_t* ds_row = sm.ds + (g * kQ / 64) * 16384 + r * 128;
+      const int ch0 = (g * kQ % 64) / 8;
+      uint32_t dsw[kQ / 2];
 #pragma unroll
-      for (int ch = 0; ch < 8; ++ch) {
+      for (int ch = 0; ch < kQ / 8; ++ch) {
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const int col = ch * 8 + 2 * e;  // 0..63 within this warpgroup's columns
+          const int col = ch * 8 + 2 * e;
           const float2 pf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pk[col / 2]));
-          // dS = P * (dP - D), two columns per packed instruction.
-          const uint64_t dpd = f2_add(f2_pack(__uint_as_float(dp[col >> 5][col & 31]),
-                                              __uint_as_float(dp[col >> 5][(col & 31) + 1])),
-                                      f2_mul(dlx2[col / 2], f2_pack(-1.f, -1.f)));
+          const uint64_t dpd = f2_add(f2_pack(__uint_as_float(dp[col]), __uint_as_float(dp[col + 1])),
+                                      dlx2[col / 2]);
           float d0, d1;
           f2_unpack(f2_mul(f2_pack(pf.x, pf.y), dpd), d0, d1);
           dsw[ch * 4 + e] = pack_bf16x2(d0, d1);
         }
-        *reinterpret_cast<uint4*>(ds_row + ((ch ^ (r & 7)) << 4)) =
+        *reinterpret_cast<uint4*>(ds_row + (((ch0 + ch) ^ (r & 7)) << 4)) =
             make_uint4(dsw[ch * 4], dsw[ch * 4 + 1], dsw[ch * 4 + 2], dsw[ch * 4 + 3]);
       }
-      // Over S^T columns [64g + 32, 64g + 64), read in the P phase already.
-      tmem_st32(colS + 32, dsw);
+      tmem_st16(colS + kQ / 2, dsw);
       tmem_wait_st();
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(&sm.ds_ready);
 
-      // dQ_i drain: TMEM lane r is query row r of dQ_i; warpgroup g reads
-      // its D/2 columns, releases the TMEM (the next dP^T reuses it) and adds
-      // them to the fp32 accumulator while the tensor core computes the next
-      // S^T.
       ok = mbar_wait(&sm.dq_full, par, p.status, abortf, kSiteDqFull);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
-      {
-        uint32_t a[D / 64][32];
-#pragma unroll
-        for (int c = 0; c < D / 64; ++c) tmem_ld32(colDQ + c * 32, a[c]);
-#pragma unroll
-        for (int c = 0; c < D / 64; ++c) tmem_wait_ld(a[c]);
+      if constexpr (D / kWG == 32) {
+        uint32_t a[32];
+        tmem_ld32(colDQ, a);
+        tmem_wait_ld(a);
         tc_fence_before();
         mbar_arrive(&sm.dq_empty);
-        float* base = p.dq_acc + dqacc_index<D>(bh, p.n_kv, i * kTile + r, g * (D / 8));
-        add_dq_chunk(base, a[0]);
-        if (D == 128) {
-          // The second half waits in registers until after the next step's
-          // P phase, so that the reductions do not all compete with the
-          // next S^T and dP^T products for the shared-memory/L1 data path.
+        add_dq_chunk(p.dq_acc + dqacc_index<D>(bh, p.n_kv, i * kTile + r, g * (D / kWG) / 4), a);
+      } else {
+        uint32_t a[16];
+        tmem_ld16(colDQ, a);
+        tmem_wait_ld16(a);
+        tc_fence_before();
+        mbar_arrive(&sm.dq_empty);
+        float* base = p.dq_acc + dqacc_index<D>(bh, p.n_kv, i * kTile + r, g * (D / kWG) / 4);
 #pragma unroll
-          for (int e = 0; e < 32; ++e) held[e] = a[D / 64 - 1][e];
-          held_base = base + (size_t)8 * kTile * 4;
-        }
+        for (int e = 0; e < 4; ++e)
+          atomicAdd(reinterpret_cast<float4*>(base + (size_t)e * kTile * 4),
+                    make_float4(__uint_as_float(a[4 * e]), __uint_as_float(a[4 * e + 1]),
+                                __uint_as_float(a[4 * e + 2]), __uint_as_float(a[4 * e + 3])));
       }
     }
-    if (held_base) add_dq_chunk(held_base, held);
-    // Epilogue: warpgroup 0 stores dV, warpgroup 1 stores scale * dK.
+    // Epilogue: the first half of the warpgroups stores dV, the second half
+    // scale * dK, each a D / (kWG / 2)-column slice.
     if (ok) ok = mbar_wait(&sm.acc_full, 0, p.status, abortf, kSiteAccFull);
     ok = __all_sync(0xffffffffu, ok);
     if (ok) {
       tc_fence_after();
-      const uint32_t col = tmem + lane_base + (g == 0 ? Cfg::kColDV : Cfg::kColDK);
-      const float mul = g == 0 ? 1.f : p.scale;
-      __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(g == 0 ? p.dv : p.dk) +
-                           ((size_t)bh * p.N + kv_row) * D;
+      constexpr int kCols = D / (kWG / 2);
+      const bool is_dv = g < kWG / 2;
+      const int c0 = (g % (kWG / 2)) * kCols;
+      const uint32_t col = tmem + lane_base + (is_dv ? Cfg::kColDV : Cfg::kColDK) + c0;
+      const float mul = is_dv ? 1.f : p.scale;
+      __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(is_dv ? p.dv : p.dk) +
+                           ((size_t)bh * p.N + kv_row) * D + c0;
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
+      for (int c = 0; c < kCols / 32; ++c) {
         uint32_t a[32];
         tmem_ld32(col + c * 32, a);
         tmem_wait_ld(a);
@@ -521,7 +515,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
           uint4 v[4];
           uint32_t* w = reinterpret_cast<uint32_t*>(v);
 #pragma unroll
-          for (int e = 0; e < 16; ++e)  // no visited query tile: dK = dV = 0
+          for (int e = 0; e < 16; ++e)
             w[e] = n_iter == 0 ? 0u
                                : pack_bf16x2(__uint_as_float(a[2 * e]) * mul,
                                              __uint_as_float(a[2 * e + 1]) * mul);

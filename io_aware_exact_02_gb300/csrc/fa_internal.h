@@ -108,8 +108,8 @@ struct BwdParams {
   void* dk;
   void* dv;
   float* dq_acc;     // workspace: [BH][n_kv*128][d] fp32, tile-blocked
-  float* delta;      // workspace: [BH][n_kv*128] fp32 (D_i)
-  float* lse2;       // workspace: [BH][n_kv*128] fp32 (lse_i * log2 e, +inf past N)
+  float* delta;      // workspace: [BH][n_kv*128] fp32 (-D_i)
+  float* lse2;       // workspace: [BH][n_kv*128] fp32 (-lse_i * log2 e, -inf past N)
   int* status;
   const uint8_t* block_mask;  // optional [n_kv][n_kv] 0/1 over (query tile, key tile)
   int BH, N;
