@@ -476,7 +476,7 @@ def run_gqa(args, wl, rank, world, local_rank):
         roofline = {"bound": "hbm", "kernel": "fa_fwd_kernel (general) + fa_combine_kernel",
                     "achieved": value / world, "peak": peak, "unit": "GB/s",
                     "frac": value / world / peak, "peak_kind": "%s HBM copy" % peak_kind,
-                    "traffic": None}
+                    "traffic": profiled_traffic("fa_fwd_general_and_combine_" + wl.name)}
     else:
         value = world * flops / per_call / 1e12
         unit, metric = "TFLOPS", "GQA prefill attention TFLOPS (bf16)"
@@ -484,7 +484,7 @@ def run_gqa(args, wl, rank, world, local_rank):
         roofline = {"bound": "tensor", "kernel": "fa_fwd_kernel (general)",
                     "achieved": value / world, "peak": peak, "unit": "TFLOP/s",
                     "frac": value / world / peak, "peak_kind": "%s burst bf16" % peak_kind,
-                    "traffic": None}
+                    "traffic": profiled_traffic("fa_fwd_general_" + wl.name)}
     if rank == 0:
         print(json.dumps({
             "metric": metric, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
@@ -599,7 +599,8 @@ def run_blocksparse(args, wl, rank, world, local_rank):
             "roofline": {"bound": "tensor", "kernel": "fa_bwd_main_kernel (sparse)",
                          "achieved": f_bwd / t_bwd / 1e12, "peak": peak, "unit": "TFLOP/s",
                          "frac": f_bwd / t_bwd / 1e12 / peak,
-                         "peak_kind": "%s burst bf16" % peak_kind, "traffic": None},
+                         "peak_kind": "%s burst bf16" % peak_kind,
+                         "traffic": profiled_traffic("fa_bwd_main_kernel_sparse_" + wl.name)},
             "fwd_tflops": f_fwd / t_fwd / 1e12, "bwd_tflops": f_bwd / t_bwd / 1e12,
             "fwd_ms": t_fwd * 1e3, "bwd_ms": t_bwd * 1e3}), flush=True)
     return 0
