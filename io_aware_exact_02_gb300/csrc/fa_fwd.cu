@@ -181,14 +181,16 @@ __global__ void __launch_bounds__(FwdCfg<D, kFp8>::kThreads, 1)
   // (that query tile t uses, for next_tile_t); callers ask only for tiles
   // that exist, and the scan stops at the item's last visible tile anyway.
   auto next_tile = [&](const Item& it, int c) -> int {
-    if (!kSparse) return c;
-    const int top = max(it.hi[0], it.hi[1]);
-    while (c < top && !(active(it, 0, c) || active(it, 1, c))) ++c;
+    if constexpr (kSparse) {
+      const int top = max(it.hi[0], it.hi[1]);
+      while (c < top && !(active(it, 0, c) || active(it, 1, c))) ++c;
+    }
     return c;
   };
   auto next_tile_t = [&](const Item& it, int t, int c) -> int {
-    if (!kSparse) return c;
-    while (c < it.hi[t] && !active(it, t, c)) ++c;
+    if constexpr (kSparse) {
+      while (c < it.hi[t] && !active(it, t, c)) ++c;
+    }
     return c;
   };
   auto decode = [&](int idx) -> Item {
