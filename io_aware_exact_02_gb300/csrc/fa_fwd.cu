@@ -108,9 +108,9 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
 // kGeneral: grouped heads, N_q != N_kv or key splits; without it the kernel
 // is the square case (rows = N_q = N_kv, one split) in its simplest form.
 // kSparse (square case only): a block mask over (128-query tile, 128-key
-// tile) pairs; a pair of query tiles streams the union of their active key
-// tiles once, and each tile takes S and P V products only on its own active
-// tiles.
+// tile) pairs; each query tile of a pair walks its own active key tiles, and
+// step j of the item loads the j-th active tile of each, so that the two
+// tiles keep alternating on the tensor core as in the dense case.
 // kFp8 (square case, d = 128): Q, K and V^T are E4M3 codes with one scale
 // per head (the FP8 forward pass of the CMU 11-868 FlashAttention post,
 // slide pages 18 and 24); S and O += P V run as kind::f8f6f4 products, P is
@@ -168,8 +168,8 @@ __global__ void __launch_bounds__(FwdCfg<D, kFp8>::kThreads, 1)
   };
   // An item: K/V head bh, pair `pair` of its packed query rows, key split.
   // Q tile t's rows see key tiles [j0, j0 + n_t[t]) of the split.  Block-
-  // sparse: the item streams nmax key tiles (the union of both Q tiles'
-  // active tiles, in key order), of which Q tile t is active on n_t[t].
+  // sparse: Q tile t has n_t[t] active key tiles and the item takes
+  // nmax = max(n_t[0], n_t[1]) steps.
   struct Item {
     int bh, pair, split, row0, j0, n_t[2], nmax, hi[2];
   };
@@ -177,16 +177,9 @@ __global__ void __launch_bounds__(FwdCfg<D, kFp8>::kThreads, 1)
   auto active = [&](const Item& it, int t, int jj) -> bool {
     return jj < it.hi[t] && p.block_mask[(size_t)(it.row0 / kTile + t) * p.n_kv + jj] != 0;
   };
-  // The next key tile at or after c that either query tile of the item uses
-  // (that query tile t uses, for next_tile_t); callers ask only for tiles
-  // that exist, and the scan stops at the item's last visible tile anyway.
-  auto next_tile = [&](const Item& it, int c) -> int {
-    if constexpr (kSparse) {
-      const int top = max(it.hi[0], it.hi[1]);
-      while (c < top && !(active(it, 0, c) || active(it, 1, c))) ++c;
-    }
-    return c;
-  };
+  // The next key tile at or after c that query tile t uses; callers ask only
+  // for tiles that exist, and the scan stops at the tile's last visible key
+  // tile anyway.
   auto next_tile_t = [&](const Item& it, int t, int c) -> int {
     if constexpr (kSparse) {
       while (c < it.hi[t] && !active(it, t, c)) ++c;
@@ -216,17 +209,13 @@ __global__ void __launch_bounds__(FwdCfg<D, kFp8>::kThreads, 1)
       it.nmax = max(it.nmax, it.n_t[t]);
     }
     if (kSparse) {
-      // The union stream's length and each query tile's share of it.
-      int count = 0;
       const int top = max(it.hi[0], it.hi[1]);
       it.n_t[0] = it.n_t[1] = 0;
       for (int jj = 0; jj < top; ++jj) {
-        const bool a0 = active(it, 0, jj), a1 = active(it, 1, jj);
-        it.n_t[0] += a0 ? 1 : 0;
-        it.n_t[1] += a1 ? 1 : 0;
-        count += (a0 || a1) ? 1 : 0;
+        it.n_t[0] += active(it, 0, jj) ? 1 : 0;
+        it.n_t[1] += active(it, 1, jj) ? 1 : 0;
       }
-      it.nmax = count;
+      it.nmax = max(it.n_t[0], it.n_t[1]);
     }
     return it;
   };
@@ -255,25 +244,37 @@ __global__ void __launch_bounds__(FwdCfg<D, kFp8>::kThreads, 1)
           for (int h = 0; h < Cfg::kBoxes; ++h)
             tma_load_3d(sm.q[t] + h * 16384, &tq, &sm.q_full, h * 64, it.row0 + t * kTile, it.bh);
         ++q_issued;
-        int cur = it.j0;
-        for (int j = 0; j < it.nmax && ok; ++j) {
-          const int jj = next_tile(it, cur);
-          cur = jj + 1;
-          for (int w = 0; w < 2 && ok; ++w, ++c) {
-            const int slot = c % S, use = c / S;
-            if (use > 0 &&
-                !mbar_wait(&sm.kv_empty[slot], (use - 1) & 1, p.status, abortf, kSiteKvEmpty)) {
-              ok = false;
-              break;
+        // K (w = 0) or V (w = 1) of key tile jj into the next ring slot.
+        auto load_kv = [&](int w, int jj) -> bool {
+          const int slot = c % S, use = c / S;
+          if (use > 0 &&
+              !mbar_wait(&sm.kv_empty[slot], (use - 1) & 1, p.status, abortf, kSiteKvEmpty))
+            return false;
+          ++c;
+          mbar_arrive_expect_tx(&sm.kv_full[slot], Cfg::kTileBytes);
+          if (kFp8 && w == 1) {  // V^T tile: d rows of 128 keys
+            tma_load_3d(sm.kv[slot], &tv, &sm.kv_full[slot], jj * kTile, 0, it.bh);
+          } else {
+            for (int h = 0; h < Cfg::kBoxes; ++h)
+              tma_load_3d(sm.kv[slot] + h * 16384, w == 0 ? &tk : &tv, &sm.kv_full[slot], h * 64,
+                          jj * kTile, it.bh);
+          }
+          return true;
+        };
+        if constexpr (kSparse) {
+          // Step j: K, V of query tile 0's j-th active tile, then of tile 1's.
+          int cur_t[2] = {it.j0, it.j0};
+          for (int j = 0; j < it.nmax && ok; ++j)
+            for (int t = 0; t < 2 && ok; ++t) {
+              if (j >= it.n_t[t]) continue;
+              const int jj = next_tile_t(it, t, cur_t[t]);
+              cur_t[t] = jj + 1;
+              ok = load_kv(0, jj) && load_kv(1, jj);
             }
-            mbar_arrive_expect_tx(&sm.kv_full[slot], Cfg::kTileBytes);
-            if (kFp8 && w == 1) {  // V^T tile: d rows of 128 keys
-              tma_load_3d(sm.kv[slot], &tv, &sm.kv_full[slot], jj * kTile, 0, it.bh);
-            } else {
-              for (int h = 0; h < Cfg::kBoxes; ++h)
-                tma_load_3d(sm.kv[slot] + h * 16384, w == 0 ? &tk : &tv, &sm.kv_full[slot],
-                            h * 64, jj * kTile, it.bh);
-            }
+        } else {
+          for (int j = 0; j < it.nmax && ok; ++j) {
+            const int jj = it.j0 + j;
+            ok = load_kv(0, jj) && load_kv(1, jj);
           }
         }
       }
@@ -397,77 +398,76 @@ __global__ void __launch_bounds__(FwdCfg<D, kFp8>::kThreads, 1)
             }
             if (ok) tc_commit(&sm.kv_empty[vc % S]);
           }
+          cb += 2 * nmax;
         } else {
-          // Block-sparse: the stream is the union of both Q tiles' active key
-          // tiles; Q tile t takes S and P V products only on its own.  Bit t
-          // of act_next(u) says whether it does at stream position u (called
-          // once for each u = 0 .. nmax-1, in order).
-          int scan = it.j0;
-          auto act_next = [&]() -> int {
-            const int key = next_tile(it, scan);
-            scan = key + 1;
-            return (active(it, 0, key) ? 1 : 0) | (active(it, 1, key) ? 2 : 0);
-          };
-          auto takes = [](int t, int a) -> bool { return ((a >> t) & 1) != 0; };
-          int a_prev = 0, a_cur = 0;
-          int pv_done[2] = {0, 0};  // P V products issued per Q tile
-          // A Q tile without keys is final at once (its rows get O = 0).
+          // Block-sparse: Q tile t walks its own n_t[t] active key tiles.
+          // Step j's loads are K and V of tile 0's j-th tile, then of tile
+          // 1's (for the tiles that have one), so the load index of each
+          // product follows from the counts alone.
           for (int t = 0; t < 2; ++t)
             if (it.n_t[t] == 0) tc_commit(&sm.o_full[t]);
           if (nmax == 0) {
             ++n_done;
             continue;
           }
-          ok = mbar_wait(&sm.q_full, q_used & 1, p.status, abortf, kSiteQFull);
-          if (ok) ok = wait_full(cb);
-          if (ok) {
-            tc_fence_after();
-            a_cur = act_next();
+          int base = cb;                    // first load of the next step
+          int ks[2] = {0, 0}, vs[2] = {0, 0};  // this step's K and V loads per tile
+          int vp[2] = {0, 0};               // the previous step's V loads
+          auto step_loads = [&](int j) {
             for (int t = 0; t < 2; ++t)
-              if (takes(t, a_cur)) issue_s(t, cb % S);
-            tc_commit(&sm.kv_empty[cb % S]);
-            if (nmax == 1) tc_commit(&sm.q_empty);
-          }
-          // Key tile j: PV_t(j-1) then S_t(j) for each Q tile that has them.
-          for (int j = 1; j < nmax && ok; ++j) {
-            const int kc = cb + 2 * j, vc = cb + 2 * j - 1;
-            ok = wait_full(kc) && wait_full(vc);
+              if (j < it.n_t[t]) {
+                ks[t] = base;
+                vs[t] = base + 1;
+                base += 2;
+              }
+          };
+          ok = mbar_wait(&sm.q_full, q_used & 1, p.status, abortf, kSiteQFull);
+          step_loads(0);
+          for (int t = 0; t < 2 && ok; ++t) {
+            if (it.n_t[t] == 0) continue;
+            ok = wait_full(ks[t]);
             if (!ok) break;
-            a_prev = a_cur;
-            a_cur = act_next();
+            tc_fence_after();
+            issue_s(t, ks[t] % S);
+            tc_commit(&sm.kv_empty[ks[t] % S]);
+          }
+          if (ok && nmax == 1) tc_commit(&sm.q_empty);
+          for (int j = 1; j < nmax && ok; ++j) {
+            vp[0] = vs[0];
+            vp[1] = vs[1];
+            step_loads(j);
             for (int t = 0; t < 2 && ok; ++t) {
-              // P V for the tile at position j-1 if Q tile t took its S, then
-              // S at position j if Q tile t is active there.
-              if (takes(t, a_prev)) {
-                ok = wait_p(t);
+              if (j - 1 < it.n_t[t]) {  // P V of tile t's (j-1)-th key tile
+                ok = wait_p(t) && wait_full(vp[t]);
                 if (!ok) break;
                 tc_fence_after();
-                ok = issue_pv(t, vc % S, pv_done[t] > 0);
+                ok = issue_pv(t, vp[t] % S, j - 1 > 0);
                 if (!ok) break;
-                if (++pv_done[t] == it.n_t[t]) tc_commit(&sm.o_full[t]);  // no more keys
+                tc_commit(&sm.kv_empty[vp[t] % S]);
+                if (j - 1 == it.n_t[t] - 1) tc_commit(&sm.o_full[t]);  // no more keys
               }
-              if (takes(t, a_cur)) issue_s(t, kc % S);
+              if (j < it.n_t[t]) {  // S of tile t's j-th key tile
+                ok = wait_full(ks[t]);
+                if (!ok) break;
+                tc_fence_after();
+                issue_s(t, ks[t] % S);
+                tc_commit(&sm.kv_empty[ks[t] % S]);
+              }
             }
+            if (ok && j == nmax - 1) tc_commit(&sm.q_empty);  // last product reading Q
+          }
+          for (int t = 0; t < 2 && ok; ++t) {
+            if (nmax - 1 >= it.n_t[t]) continue;
+            ok = wait_p(t) && wait_full(vs[t]);
             if (!ok) break;
-            tc_commit(&sm.kv_empty[vc % S]);
-            tc_commit(&sm.kv_empty[kc % S]);
-            if (j == nmax - 1) tc_commit(&sm.q_empty);  // last product reading Q
+            tc_fence_after();
+            ok = issue_pv(t, vs[t] % S, nmax - 1 > 0);
+            if (!ok) break;
+            tc_commit(&sm.kv_empty[vs[t] % S]);
+            tc_commit(&sm.o_full[t]);
           }
-          if (ok) {
-            const int vc = cb + 2 * nmax - 1;
-            ok = wait_full(vc);
-            for (int t = 0; t < 2 && ok; ++t) {
-              if (!takes(t, a_cur)) continue;  // a_cur: position nmax-1
-              ok = wait_p(t);
-              if (!ok) break;
-              tc_fence_after();
-              ok = issue_pv(t, vc % S, pv_done[t] > 0);
-              if (ok) tc_commit(&sm.o_full[t]);
-            }
-            if (ok) tc_commit(&sm.kv_empty[vc % S]);
-          }
+          cb = base;
         }
-        cb += 2 * nmax;
         ++q_used;
         ++n_done;
       }
