@@ -244,24 +244,24 @@ __global__ void __launch_bounds__(FwdCfg<D, kFp8>::kThreads, 1)
           for (int h = 0; h < Cfg::kBoxes; ++h)
             tma_load_3d(sm.q[t] + h * 16384, &tq, &sm.q_full, h * 64, it.row0 + t * kTile, it.bh);
         ++q_issued;
-        // K (w = 0) or V (w = 1) of key tile jj into the next ring slot.
-        auto load_kv = [&](int w, int jj) -> bool {
-          const int slot = c % S, use = c / S;
-          if (use > 0 &&
-              !mbar_wait(&sm.kv_empty[slot], (use - 1) & 1, p.status, abortf, kSiteKvEmpty))
-            return false;
-          ++c;
-          mbar_arrive_expect_tx(&sm.kv_full[slot], Cfg::kTileBytes);
-          if (kFp8 && w == 1) {  // V^T tile: d rows of 128 keys
-            tma_load_3d(sm.kv[slot], &tv, &sm.kv_full[slot], jj * kTile, 0, it.bh);
-          } else {
-            for (int h = 0; h < Cfg::kBoxes; ++h)
-              tma_load_3d(sm.kv[slot] + h * 16384, w == 0 ? &tk : &tv, &sm.kv_full[slot], h * 64,
-                          jj * kTile, it.bh);
-          }
-          return true;
-        };
         if constexpr (kSparse) {
+          // K (w = 0) or V (w = 1) of key tile jj into the next ring slot.
+          auto load_kv = [&](int w, int jj) -> bool {
+            const int slot = c % S, use = c / S;
+            if (use > 0 &&
+                !mbar_wait(&sm.kv_empty[slot], (use - 1) & 1, p.status, abortf, kSiteKvEmpty))
+              return false;
+            ++c;
+            mbar_arrive_expect_tx(&sm.kv_full[slot], Cfg::kTileBytes);
+            if (kFp8 && w == 1) {  // V^T tile: d rows of 128 keys
+              tma_load_3d(sm.kv[slot], &tv, &sm.kv_full[slot], jj * kTile, 0, it.bh);
+            } else {
+              for (int h = 0; h < Cfg::kBoxes; ++h)
+                tma_load_3d(sm.kv[slot] + h * 16384, w == 0 ? &tk : &tv, &sm.kv_full[slot], h * 64,
+                            jj * kTile, it.bh);
+            }
+            return true;
+          };
           // Step j: K, V of query tile 0's j-th active tile, then of tile 1's.
           int cur_t[2] = {it.j0, it.j0};
           for (int j = 0; j < it.nmax && ok; ++j)
@@ -274,7 +274,22 @@ __global__ void __launch_bounds__(FwdCfg<D, kFp8>::kThreads, 1)
         } else {
           for (int j = 0; j < it.nmax && ok; ++j) {
             const int jj = it.j0 + j;
-            ok = load_kv(0, jj) && load_kv(1, jj);
+            for (int w = 0; w < 2 && ok; ++w, ++c) {
+              const int slot = c % S, use = c / S;
+              if (use > 0 &&
+                  !mbar_wait(&sm.kv_empty[slot], (use - 1) & 1, p.status, abortf, kSiteKvEmpty)) {
+                ok = false;
+                break;
+              }
+              mbar_arrive_expect_tx(&sm.kv_full[slot], Cfg::kTileBytes);
+              if (kFp8 && w == 1) {  // V^T tile: d rows of 128 keys
+                tma_load_3d(sm.kv[slot], &tv, &sm.kv_full[slot], jj * kTile, 0, it.bh);
+              } else {
+                for (int h = 0; h < Cfg::kBoxes; ++h)
+                  tma_load_3d(sm.kv[slot] + h * 16384, w == 0 ? &tk : &tv, &sm.kv_full[slot],
+                              h * 64, jj * kTile, it.bh);
+              }
+            }
           }
         }
       }
