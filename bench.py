@@ -206,6 +206,28 @@ def cpu_sample(w, heads: int, seed: int = 0):
     return (ff + bf) / dt / 1e12, dt, oracle.num_threads()
 
 
+def cpu_single_thread_rows(w, rows: int = 256, seed: int = 0):
+    """The oracle's forward on `rows` query rows of one head with one thread:
+    (TFLOPS, seconds).  A single-thread reference point beside the all-core
+    figure."""
+    import oracle
+    from io_aware_exact_02_gb300 import synth
+    import numpy as np
+    q, k, v, _ = synth.draw(1, 1, w["N"], w["d"], seed=seed, with_dout=False)
+    sel = np.linspace(0, w["N"] - 1, rows).astype(np.int64)
+    heads = np.zeros(rows, dtype=np.int64)
+    before = oracle.num_threads()
+    oracle.set_num_threads(1)
+    try:
+        t0 = time.perf_counter()
+        oracle.attn_fwd_rows(q, k, v, w["causal"], 1.0 / math.sqrt(w["d"]), heads, sel)
+        dt = time.perf_counter() - t0
+    finally:
+        oracle.set_num_threads(before)
+    keys = sum(min(int(i) + 1, w["N"]) if w["causal"] else w["N"] for i in sel)
+    return 4.0 * keys * w["d"] / dt / 1e12, dt
+
+
 def run_reference(args, w, rank, world):
     if rank != 0:
         return 0
@@ -390,6 +412,13 @@ def run_gpu(args, w, rank, world, local_rank):
     kernels["fwd"]["frac_of_peak"] = ff / fwd_avg / 1e12 / peak
     kernels["bwd_main"]["tflops"] = achieved
     bwd_total = (per_kernel["bwd_prep"] + per_kernel["bwd_main"] + per_kernel["bwd_convert"]) / args.steps
+    # The trade the backward pass makes (cs2680 Lecture 9 sec. 9.6): recompute
+    # S and P instead of writing the N x N probabilities in the forward pass
+    # and reading them back, 2 * B*H*N^2 bf16 bytes at the HBM copy rate.
+    p_bytes = 2.0 * 2.0 * B * H * N * N
+    kernels["stored_p_equivalent"] = {
+        "bytes": p_bytes,
+        "ms_at_hbm_peak": p_bytes / (float(load_peaks()[0]["hbm_gbs"]) * 1e9) * 1e3}
     kernels["bwd_total"] = {"ms_per_call": bwd_total * 1e3, "tflops": bf / bwd_total / 1e12,
                             "frac_of_peak": bf / bwd_total / 1e12 / peak}
     hbm_bytes = 8.0 * B * H * N * d + 4.0 * B * H * N  # fwd: Q, K, V read, O written, lse
@@ -399,9 +428,13 @@ def run_gpu(args, w, rank, world, local_rank):
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         val, dt, threads = cpu_sample(w, args.cpu_heads)
+        st_val, st_dt = cpu_single_thread_rows(w)
         cpu = {"value": val, "unit": UNIT, "cores": threads, "kind": "oracle",
                "sample": "fwd+bwd of %d of %d heads (N=%d, d=%d), fp64 oracle, %.1f s"
-                         % (args.cpu_heads, B * H, N, d, dt)}
+                         % (args.cpu_heads, B * H, N, d, dt),
+               "single_thread": {"value": st_val, "unit": UNIT,
+                                 "sample": "forward of 256 query rows of one head, 1 thread, "
+                                           "%.2f s" % st_dt}}
 
     if rank == 0:
         line = {
