@@ -161,3 +161,16 @@ def test_fwd_full_size_sampled(name):
     fa.check_device_status()
     assert torch.isfinite(lse).all()
     sampled_check(w, o, lse, q, k, v)
+
+
+def test_fwd_long_sequence_sampled_rows():
+    # N = 65536 (512 key tiles per head) causal and not: sampled rows against
+    # the oracle's row-wise definition.
+    from io_aware_exact_02_gb300.synth import Workload
+    for causal in (False, True):
+        w = Workload("n64k_%d" % causal, 1, 2, 65536, 128, causal)
+        q, k, v, _ = synth.draw_workload(w, seed=3, with_dout=False)
+        dev = torch.device("cuda")
+        o, lse = fa.fwd(q.to(dev), k.to(dev), v.to(dev), causal=causal, scale=w.softmax_scale)
+        fa.check_device_status()
+        sampled_check(w, o, lse, q, k, v, n_heads=2, n_rows=24, seed=causal)
