@@ -743,7 +743,7 @@ def main(argv=None):
                     help="heads of the workload the cpu_baseline leg times (GPU arm)")
     ap.add_argument("--ref-heads", type=int, default=1,
                     help="heads of the workload per step of the reference arm")
-    ap.add_argument("--e2e-steps", type=int, default=8)
+    ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
