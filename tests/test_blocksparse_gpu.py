@@ -190,3 +190,21 @@ def test_blocksparse_full_size_sampled_head():
     refs = oracle.attn_bwd_blockmask(sel(q), sel(k), sel(v), sel(do), w.causal, w.softmax_scale,
                                      mask.numpy())
     check_bwd((sel(dq), sel(dk), sel(dv)), refs, w.name, mask, w.causal)
+
+
+def test_blocksparse_causal_large_sampled_head():
+    B, H, N, d = 2, 8, 4096, 128
+    q, k, v, do = synth.draw(B, H, N, d, seed=77)
+    mask = synth.draw_block_mask(32, 0.4, seed=5)
+    o, lse, dq, dk, dv = run(q, k, v, do, mask, True, 1 / math.sqrt(d))
+    head = 11
+
+    def sel(t):
+        return t.reshape(B * H, *t.shape[2:])[head][None, None]
+
+    o_ref, lse_ref = oracle.attn_fwd_blockmask(sel(q), sel(k), sel(v), True, 1 / math.sqrt(d),
+                                               mask.numpy())
+    check_fwd(sel(o), sel(lse), o_ref, lse_ref, "causal N4096")
+    refs = oracle.attn_bwd_blockmask(sel(q), sel(k), sel(v), sel(do), True, 1 / math.sqrt(d),
+                                     mask.numpy())
+    check_bwd((sel(dq), sel(dk), sel(dv)), refs, "causal N4096", mask, True)

@@ -182,3 +182,17 @@ def test_fp8_full_size_sampled_head():
 
     ref = oracle.attn_fwd_fp8(sel(q), sel(k), sel(v), False, 1 / math.sqrt(d), True)
     check_attention(sel(o), sel(lse), ref, True, "B8 H16 N8192")
+
+
+def test_fp8_causal_large_sampled_head():
+    B, H, N, d = 2, 8, 8192, 128
+    q, k, v = synth.draw_outliers(B, H, N, d, seed=21)
+    o, lse = run_fp8(q, k, v, True, 1 / math.sqrt(d), True)
+    head = 5
+
+    def sel(t):
+        return t.reshape(B * H, N, *t.shape[3:])[head][None, None]
+
+    # Per-head scales: the oracle on one head sees the same amax as the GPU.
+    ref = oracle.attn_fwd_fp8(sel(q), sel(k), sel(v), True, 1 / math.sqrt(d), True)
+    check_attention(sel(o), sel(lse), ref, True, "causal B2 H8 N8192")
