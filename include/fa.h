@@ -106,8 +106,9 @@ int fa_fwd_gqa_splits(int B, int Hq, int Hkv, int Nq, int Nkv, int d, int causal
  * Bytes of device workspace fa_bwd needs for these sizes: an fp32 dQ
  * accumulator of B*H*ceil(N/128)*128*d floats, then two per-row fp32
  * terms of B*H*ceil(N/128)*128 floats each (-D_i with D_i = sum_k dO_ik
- * O_ik, and -lse_i * log2 e), each part rounded up to 256 bytes.  Returns 0
- * when the sizes are invalid.
+ * O_ik, and -lse_i * log2 e), each part rounded up to 256 bytes, then 256
+ * bytes holding the main kernel's work-item counter.  Returns 0 when the
+ * sizes are invalid.
  */
 size_t fa_bwd_workspace_size(int B, int H, int N, int d);
 
@@ -135,10 +136,11 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
 /*
  * fa_bwd split into its three kernels, for callers that want to time or
  * overlap them: bit 0 of phase_mask runs the preparation (-D_i and
- * -lse_i * log2 e, zeroing of the dQ accumulator), bit 1 the main kernel
- * (dK, dV and the dQ accumulation), bit 2 the dQ conversion to bf16.
- * fa_bwd(...) is fa_bwd_phases(..., 7).  Phases must run in order on one
- * stream with the same workspace; arguments and errors as fa_bwd, plus
+ * -lse_i * log2 e, zeroing of the dQ accumulator and of the work-item
+ * counter), bit 1 the main kernel (dK, dV and the dQ accumulation), bit 2
+ * the dQ conversion to bf16.  fa_bwd(...) is fa_bwd_phases(..., 7).  Phases
+ * must run in order on one stream with the same workspace, each main
+ * kernel after its own preparation; arguments and errors as fa_bwd, plus
  * FA_ERR_ARG for a mask outside 1..7.
  */
 int fa_bwd_phases(const void* q, const void* k, const void* v, const void* o, const void* dout,

@@ -355,6 +355,8 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const v
   p.causal = causal;
   p.scale = scale;
   p.scale_log2 = scale * 1.4426950408889634f;
+  p.sm_count = ds->sm_count;
+  p.sched = reinterpret_cast<int*>(static_cast<char*>(workspace) + ws.sched);
   return launch_bwd(tq, tk, tv, tdo, p, d, static_cast<cudaStream_t>(stream), phase_mask);
 }
 

@@ -12,11 +12,16 @@
 // Three kernels:
 //   1. prep: per row -D_i and -lse_i * log2(e) into the workspace, negated
 //      so that the main kernel adds them (padded rows get 0 and -inf, which
-//      makes their probabilities exactly 0), and the fp32 dQ accumulator
-//      zeroed.  HBM-bound.
-//   2. main: one CTA per (head, 128-key tile j).  K_j, V_j stay in shared
-//      memory; dK_j, dV_j accumulate in tensor memory while the CTA walks the
-//      query tiles i (all of them, or i >= j under a causal mask).  Per step:
+//      makes their probabilities exactly 0), the fp32 dQ accumulator zeroed
+//      and the main kernel's work-item counter reset.  HBM-bound.
+//   2. main: one persistent CTA per SM; a work item is (head, 128-key tile
+//      j), claimed from the counter in longest-first list order when the CTA
+//      is ready for one.  K_j, V_j stay in shared memory; dK_j, dV_j
+//      accumulate in tensor memory while the CTA walks the query tiles i
+//      (all of them, or i >= j under a causal mask).  The next item's K and
+//      V load as soon as the last product has read the current ones, and
+//      its first products run while the compute warps store dK_j, dV_j.
+//      Per step:
 //        S^T  = K_j Q_i^T           (tcgen05, both operands in smem)
 //        dP^T = V_j dO_i^T
 //        P^T  = exp2(S^T c - lse_i log2 e)  -> bf16 in TMEM over S^T
@@ -70,7 +75,9 @@ struct BwdSmem {
   uint8_t ds[kTile * kTile * 2];  // dS^T [key][query] bf16, 128B swizzle
   float lse2[BwdCfg<D>::kStages][kTile];
   float delta[BwdCfg<D>::kStages][kTile];
-  uint64_t kv_full;
+  uint64_t kv_full, kv_empty;
+  uint64_t item_full[2], item_empty[2];  // work-item handoff from the producer
+  int item_idx[2];
   uint64_t q_full[BwdCfg<D>::kStages];
   uint64_t q_empty[BwdCfg<D>::kStages];
   uint64_t s_full, dp_full, p_ready, ds_ready, dq_full, dq_empty, acc_full, drain;
@@ -81,7 +88,8 @@ struct BwdSmem {
 
 enum : int {
   kSiteKvFull = 201, kSiteQFull, kSiteQEmpty, kSiteSFull, kSiteDpFull, kSitePReady,
-  kSiteDsReady, kSiteDqFull, kSiteDqEmpty, kSiteAccFull, kSiteAlign
+  kSiteDsReady, kSiteDqFull, kSiteDqEmpty, kSiteAccFull, kSiteAlign, kSiteKvEmpty,
+  kSiteItemFull, kSiteItemEmpty
 };
 
 __device__ __forceinline__ uint64_t kmajor_desc(uint32_t base, int kk) {
@@ -149,6 +157,7 @@ __global__ void __launch_bounds__(256) fa_bwd_prep_kernel(const BwdParams p) {
   constexpr int kRowsPerWarp = 32 / kLanesPerRow;
   const int lane = threadIdx.x & 31;
   const int warp_global = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  if (blockIdx.x == 0 && threadIdx.x == 0) *p.sched = 0;
   const int npad = p.n_kv * kTile;
   const long long total_rows = (long long)p.BH * npad;
   const long long row_g = (long long)warp_global * kRowsPerWarp + lane / kLanesPerRow;
@@ -241,6 +250,11 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
 
   if (tid == 0) {
     mbar_init(&sm.kv_full, 1);
+    mbar_init(&sm.kv_empty, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&sm.item_full[s], 1);
+      mbar_init(&sm.item_empty[s], 1 + kWG * 4);  // the MMA thread and every compute warp
+    }
     for (int s = 0; s < NS; ++s) {
       mbar_init(&sm.q_full[s], 1);
       mbar_init(&sm.q_empty[s], 1);
@@ -265,24 +279,42 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
 
-  int bh, j;
-  bwd_item(blockIdx.x, p.BH, p.n_kv, &bh, &j);
-  const int i0 = p.causal ? j : 0;
-  auto active_i = [&](int i) -> bool {
-    return !kSparse || p.block_mask[(size_t)i * p.n_kv + j] != 0;
+  // Work items t = (head, key tile j) in the order of bwd_item.  The
+  // producer claims them one at a time from the workspace counter and hands
+  // each to the MMA thread and the compute warps through a two-slot ring in
+  // shared memory (a claimed index >= total ends the CTA).  Every role walks
+  // the same item sequence, so the barrier phases carry over from one item
+  // to the next: gstep counts the query-tile steps of all items so far, kvc
+  // the K/V loads, m the items.
+  const int total = p.BH * p.n_kv;
+  const int npad = p.n_kv * kTile;
+  struct ItemInfo {
+    int bh, j, i0, n_iter;
   };
-  // The next query tile at or after c that this key tile visits (callers
-  // ask only for tiles that exist; the scan stops at the last tile anyway).
-  auto next_i = [&](int c) -> int {
-    while (c < p.n_kv && !active_i(c)) ++c;
+  auto item_info = [&](int t) -> ItemInfo {
+    ItemInfo w;
+    bwd_item(t, p.BH, p.n_kv, &w.bh, &w.j);
+    w.i0 = p.causal ? w.j : 0;
+    w.n_iter = p.n_kv - w.i0;
+    if (kSparse) {
+      w.n_iter = 0;
+      for (int i = w.i0; i < p.n_kv; ++i) w.n_iter += p.block_mask[(size_t)i * p.n_kv + w.j] != 0;
+    }
+    return w;
+  };
+  // The next query tile at or after c that key tile j visits (callers ask
+  // only for tiles that exist; the scan stops at the last tile anyway).
+  auto next_i = [&](int c, int j) -> int {
+    if (kSparse)
+      while (c < p.n_kv && p.block_mask[(size_t)c * p.n_kv + j] == 0) ++c;
     return c;
   };
-  int n_iter = p.n_kv - i0;
-  if (kSparse) {
-    n_iter = 0;
-    for (int i = i0; i < p.n_kv; ++i) n_iter += active_i(i) ? 1 : 0;
-  }
-  const int npad = p.n_kv * kTile;
+  // Consumers: the index of the m-th item (waits for the producer's handoff).
+  auto take_item = [&](int m, bool* ok) -> int {
+    const int slot = m & 1;
+    *ok = mbar_wait(&sm.item_full[slot], (m >> 1) & 1, p.status, abortf, kSiteItemFull);
+    return *ok ? *reinterpret_cast<volatile int*>(&sm.item_idx[slot]) : total;
+  };
 
   if (warp == kWarpLoad) {
     // ------------------------------------------------------------ producer
@@ -291,30 +323,60 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       prefetch_tmap(&tk);
       prefetch_tmap(&tv);
       prefetch_tmap(&tdo);
-      mbar_arrive_expect_tx(&sm.kv_full, 2 * Cfg::kTileBytes);
-      for (int h = 0; h < D / 64; ++h) {
-        tma_load_3d(sm.k + h * 16384, &tk, &sm.kv_full, h * 64, j * kTile, bh);
-        tma_load_3d(sm.v + h * 16384, &tv, &sm.kv_full, h * 64, j * kTile, bh);
-      }
-      int it = 0;
-      int cur = i0;
-      for (; it < n_iter; ++it) {
-        const int s = it % NS, use = it / NS;
-        if (use > 0 && !mbar_wait(&sm.q_empty[s], (use - 1) & 1, p.status, abortf, kSiteQEmpty))
+      int gstep = 0, kvc = 0;
+      bool ok = true;
+      for (int m = 0; ok; ++m) {
+        const int slot = m & 1;
+        if (m >= 2 &&
+            !mbar_wait(&sm.item_empty[slot], ((m - 2) >> 1) & 1, p.status, abortf, kSiteItemEmpty)) {
+          ok = false;
           break;
-        const int i = next_i(cur);
-        cur = i + 1;
-        mbar_arrive_expect_tx(&sm.q_full[s], 2 * Cfg::kTileBytes + 2 * kTile * 4);
-        for (int h = 0; h < D / 64; ++h) {
-          tma_load_3d(sm.q[s] + h * 16384, &tq, &sm.q_full[s], h * 64, i * kTile, bh);
-          tma_load_3d(sm.dO[s] + h * 16384, &tdo, &sm.q_full[s], h * 64, i * kTile, bh);
         }
-        bulk_load(sm.lse2[s], p.lse2 + (size_t)bh * npad + i * kTile, kTile * 4, &sm.q_full[s]);
-        bulk_load(sm.delta[s], p.delta + (size_t)bh * npad + i * kTile, kTile * 4, &sm.q_full[s]);
+        const int t = atomicAdd(p.sched, 1);
+        *reinterpret_cast<volatile int*>(&sm.item_idx[slot]) = t;
+        mbar_arrive(&sm.item_full[slot]);
+        if (t >= total) break;
+        const ItemInfo w = item_info(t);
+        int cur = w.i0;
+        for (int it = 0; it < w.n_iter; ++it) {
+          const int s = gstep % NS, use = gstep / NS;
+          if (use > 0 && !mbar_wait(&sm.q_empty[s], (use - 1) & 1, p.status, abortf, kSiteQEmpty)) {
+            ok = false;
+            break;
+          }
+          const int i = next_i(cur, w.j);
+          cur = i + 1;
+          mbar_arrive_expect_tx(&sm.q_full[s], 2 * Cfg::kTileBytes + 2 * kTile * 4);
+          for (int h = 0; h < D / 64; ++h) {
+            tma_load_3d(sm.q[s] + h * 16384, &tq, &sm.q_full[s], h * 64, i * kTile, w.bh);
+            tma_load_3d(sm.dO[s] + h * 16384, &tdo, &sm.q_full[s], h * 64, i * kTile, w.bh);
+          }
+          bulk_load(sm.lse2[s], p.lse2 + (size_t)w.bh * npad + i * kTile, kTile * 4, &sm.q_full[s]);
+          bulk_load(sm.delta[s], p.delta + (size_t)w.bh * npad + i * kTile, kTile * 4, &sm.q_full[s]);
+          ++gstep;
+          if (it == 0) {
+            // K_j, V_j replace the previous item's once its last product
+            // has read them (kv_empty).
+            if (kvc > 0 &&
+                !mbar_wait(&sm.kv_empty, (kvc - 1) & 1, p.status, abortf, kSiteKvEmpty)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(&sm.kv_full, 2 * Cfg::kTileBytes);
+            for (int h = 0; h < D / 64; ++h) {
+              tma_load_3d(sm.k + h * 16384, &tk, &sm.kv_full, h * 64, w.j * kTile, w.bh);
+              tma_load_3d(sm.v + h * 16384, &tv, &sm.kv_full, h * 64, w.j * kTile, w.bh);
+            }
+            ++kvc;
+          }
+        }
       }
-      if (it < n_iter) {
-        drain_wait(&sm.kv_full, 0);
-        for (int c = it - 1; c >= 0 && c >= it - NS; --c) drain_wait(&sm.q_full[c % NS], (c / NS) & 1);
+      if (!ok) {
+        // Aborting: wait (bounded) for the copies in flight before the CTA
+        // releases its shared memory.
+        if (kvc > 0) drain_wait(&sm.kv_full, (kvc - 1) & 1);
+        for (int c = gstep - 1; c >= 0 && c >= gstep - NS; --c)
+          drain_wait(&sm.q_full[c % NS], (c / NS) & 1);
       }
     }
     __syncwarp();
@@ -325,54 +387,71 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       const uint32_t id_acc = idesc_bf16(128, D, false, true);    // dV, dK
       const uint32_t id_dq = idesc_bf16(128, D, true, true);      // dQ
       const uint32_t kb = smem_u32(sm.k), vb = smem_u32(sm.v), dsb = smem_u32(sm.ds);
-      bool ok = mbar_wait(&sm.kv_full, 0, p.status, abortf, kSiteKvFull);
-      for (int it = 0; it < n_iter && ok; ++it) {
-        const int s = it % NS;
-        const uint32_t par = it & 1;
-        const uint32_t qb = smem_u32(sm.q[s]), dob = smem_u32(sm.dO[s]);
-        ok = mbar_wait(&sm.q_full[s], (it / NS) & 1, p.status, abortf, kSiteQFull);
+      int gstep = 0, kvc = 0;
+      bool ok = true;
+      for (int m = 0; ok; ++m) {
+        const int t = take_item(m, &ok);
         if (!ok) break;
-        tc_fence_after();
-        // S^T = K_j Q_i^T
-#pragma unroll 1
-        for (int kk = 0; kk < D / 16; ++kk)
-          mma_ss(tmem + Cfg::kColS, kmajor_desc(kb, kk), kmajor_desc(qb, kk), id_s, kk > 0);
-        tc_commit(&sm.s_full);
-        // dP^T = V_j dO_i^T, into the columns dQ_{i-1} occupied
-        if (it > 0) {
-          ok = mbar_wait(&sm.dq_empty, (it - 1) & 1, p.status, abortf, kSiteDqEmpty);
+        mbar_arrive(&sm.item_empty[m & 1]);
+        if (t >= total) break;
+        const ItemInfo w = item_info(t);
+        if (w.n_iter > 0) {
+          ok = mbar_wait(&sm.kv_full, kvc & 1, p.status, abortf, kSiteKvFull);
+          if (!ok) break;
+        }
+        for (int it = 0; it < w.n_iter; ++it, ++gstep) {
+          const int s = gstep % NS;
+          const uint32_t par = gstep & 1;
+          const uint32_t qb = smem_u32(sm.q[s]), dob = smem_u32(sm.dO[s]);
+          ok = mbar_wait(&sm.q_full[s], (gstep / NS) & 1, p.status, abortf, kSiteQFull);
           if (!ok) break;
           tc_fence_after();
+          // S^T = K_j Q_i^T
+#pragma unroll 1
+          for (int kk = 0; kk < D / 16; ++kk)
+            mma_ss(tmem + Cfg::kColS, kmajor_desc(kb, kk), kmajor_desc(qb, kk), id_s, kk > 0);
+          tc_commit(&sm.s_full);
+          // dP^T = V_j dO_i^T, into the columns the previous step's dQ occupied
+          if (gstep > 0) {
+            ok = mbar_wait(&sm.dq_empty, (gstep - 1) & 1, p.status, abortf, kSiteDqEmpty);
+            if (!ok) break;
+            tc_fence_after();
+          }
+#pragma unroll 1
+          for (int kk = 0; kk < D / 16; ++kk)
+            mma_ss(tmem + Cfg::kColDP, kmajor_desc(vb, kk), kmajor_desc(dob, kk), id_s, kk > 0);
+          tc_commit(&sm.dp_full);
+          // dV += P^T dO_i.  Warpgroup g's P^T sits in TMEM columns
+          // [kQ g, kQ g + kQ/2) as bf16 pairs.
+          ok = mbar_wait(&sm.p_ready, par, p.status, abortf, kSitePReady);
+          if (!ok) break;
+          tc_fence_after();
+#pragma unroll 1
+          for (int kk = 0; kk < kTile / 16; ++kk)
+            mma_ts(tmem + Cfg::kColDV, tmem + Cfg::kColS + (kk * 16 / kQ) * kQ + (kk * 16 % kQ) / 2,
+                   mnmajor_desc(dob, kk), id_acc, (it > 0 || kk > 0) ? 1u : 0u);
+          // dK += dS^T Q_i ; dQ_i = dS K_j
+          ok = mbar_wait(&sm.ds_ready, par, p.status, abortf, kSiteDsReady);
+          if (!ok) break;
+          tc_fence_after();
+#pragma unroll 1
+          for (int kk = 0; kk < kTile / 16; ++kk)
+            mma_ts(tmem + Cfg::kColDK,
+                   tmem + Cfg::kColS + kQ / 2 + (kk * 16 / kQ) * kQ + (kk * 16 % kQ) / 2,
+                   mnmajor_desc(qb, kk), id_acc, (it > 0 || kk > 0) ? 1u : 0u);
+          tc_commit(&sm.q_empty[s]);
+#pragma unroll 1
+          for (int kk = 0; kk < kTile / 16; ++kk)
+            mma_ss(tmem + Cfg::kColDP, mnmajor_desc(dsb, kk), mnmajor_desc(kb, kk), id_dq, kk > 0);
+          tc_commit(&sm.dq_full);
         }
-#pragma unroll 1
-        for (int kk = 0; kk < D / 16; ++kk)
-          mma_ss(tmem + Cfg::kColDP, kmajor_desc(vb, kk), kmajor_desc(dob, kk), id_s, kk > 0);
-        tc_commit(&sm.dp_full);
-        // dV += P^T dO_i.  P^T for query columns 0-63 sits in TMEM columns
-        // 0-31, for query columns 64-127 in columns 64-95 (bf16 pairs).
-        ok = mbar_wait(&sm.p_ready, par, p.status, abortf, kSitePReady);
         if (!ok) break;
-        tc_fence_after();
-#pragma unroll 1
-        for (int kk = 0; kk < kTile / 16; ++kk)
-          mma_ts(tmem + Cfg::kColDV, tmem + Cfg::kColS + (kk * 16 / kQ) * kQ + (kk * 16 % kQ) / 2,
-                 mnmajor_desc(dob, kk), id_acc, (it > 0 || kk > 0) ? 1u : 0u);
-        // dK += dS^T Q_i ; dQ_i = dS K_j
-        ok = mbar_wait(&sm.ds_ready, par, p.status, abortf, kSiteDsReady);
-        if (!ok) break;
-        tc_fence_after();
-#pragma unroll 1
-        for (int kk = 0; kk < kTile / 16; ++kk)
-          mma_ts(tmem + Cfg::kColDK,
-                 tmem + Cfg::kColS + kQ / 2 + (kk * 16 / kQ) * kQ + (kk * 16 % kQ) / 2,
-                 mnmajor_desc(qb, kk), id_acc, (it > 0 || kk > 0) ? 1u : 0u);
-        tc_commit(&sm.q_empty[s]);
-#pragma unroll 1
-        for (int kk = 0; kk < kTile / 16; ++kk)
-          mma_ss(tmem + Cfg::kColDP, mnmajor_desc(dsb, kk), mnmajor_desc(kb, kk), id_dq, kk > 0);
-        tc_commit(&sm.dq_full);
+        if (w.n_iter > 0) {
+          tc_commit(&sm.kv_empty);  // the item's last product has read K_j, V_j
+          ++kvc;
+        }
+        tc_commit(&sm.acc_full);    // dK_j, dV_j complete
       }
-      if (ok) tc_commit(&sm.acc_full);
       tc_commit(&sm.drain);
       drain_wait(&sm.drain, 0);
     }
@@ -389,115 +468,129 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     const uint32_t colDQ = tmem + lane_base + Cfg::kColDP + g * (D / kWG);
     const float c2 = p.scale_log2;
     const float neutral = c2 < 0.f ? __int_as_float(0x7f800000) : __int_as_float(0xff800000);
-    const int kv_row = j * kTile + r;
+    int gstep = 0;
     bool ok = true;
-    int cur = i0;
-    for (int it = 0; it < n_iter; ++it) {
-      const int s = it % NS;
-      const uint32_t par = it & 1;
-      const int i = next_i(cur);
-      cur = i + 1;
-      ok = mbar_wait(&sm.q_full[s], (it / NS) & 1, p.status, abortf, kSiteQFull);
-      if (ok) ok = mbar_wait(&sm.s_full, par, p.status, abortf, kSiteSFull);
+    for (int m = 0;; ++m) {
+      const int t = take_item(m, &ok);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
-      tc_fence_after();
-      uint32_t sr[kQ];
-      {
-        uint32_t (&h)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[0]);
-        static_assert(kQ == 32, "the compute code is written for 32 query columns per warpgroup");
-        tmem_ld32(colS, h);
-        tmem_wait_ld(h);
-      }
-      if (p.causal && i == j) {
-#pragma unroll
-        for (int e = 0; e < kQ; ++e)
-          if (r > g * kQ + e) sr[e] = __float_as_uint(neutral);
-      }
-      const uint64_t* lse2x2 = reinterpret_cast<const uint64_t*>(sm.lse2[s] + g * kQ);
-      const uint64_t c2x2 = f2_pack(c2, c2);
-      uint32_t pk[kQ / 2];
-#pragma unroll
-      for (int e = 0; e < kQ; e += 2) {
-        float x0, x1;
-        f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), c2x2,
-                         lse2x2[e / 2]),
-                  x0, x1);
-        pk[e / 2] = pack_bf16x2(ex2_approx(x0), ex2_approx(x1));
-      }
-      tmem_st16(colS, pk);
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(&sm.p_ready);
-
-      ok = mbar_wait(&sm.dp_full, par, p.status, abortf, kSiteDpFull);
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) break;
-      tc_fence_after();
-      uint32_t dp[kQ];
-      {
-        uint32_t (&h)[32] = *reinterpret_cast<uint32_t(*)[32]>(&dp[0]);
-        tmem_ld32(colDP, h);
-        tmem_wait_ld(h);
-      }
-      const uint64_t* dlx2 = reinterpret_cast<const uint64_t*>(sm.delta[s] + g * kQ);
-      // dS^T row r, query columns [kQ g, kQ g + kQ): in the 128B-swizzled
-      // [key][query] tile, column block (kQ g) / 64, 16-byte chunks from
-      // ((kQ g) % 64) / 8.
-      uint8_t* ds_row = sm.ds + (g * kQ / 64) * 16384 + r * 128;
-      const int ch0 = (g * kQ % 64) / 8;
-      uint32_t dsw[kQ / 2];
-#pragma unroll
-      for (int ch = 0; ch < kQ / 8; ++ch) {
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int col = ch * 8 + 2 * e;
-          const float2 pf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pk[col / 2]));
-          const uint64_t dpd = f2_add(f2_pack(__uint_as_float(dp[col]), __uint_as_float(dp[col + 1])),
-                                      dlx2[col / 2]);
-          float d0, d1;
-          f2_unpack(f2_mul(f2_pack(pf.x, pf.y), dpd), d0, d1);
-          dsw[ch * 4 + e] = pack_bf16x2(d0, d1);
+      __syncwarp();
+      if (lane_id() == 0) mbar_arrive(&sm.item_empty[m & 1]);
+      if (t >= total) break;
+      const ItemInfo w = item_info(t);
+      const int j = w.j, bh = w.bh;
+      const int kv_row = j * kTile + r;
+      int cur = w.i0;
+      for (int it = 0; it < w.n_iter; ++it, ++gstep) {
+        const int s = gstep % NS;
+        const uint32_t par = gstep & 1;
+        const int i = next_i(cur, j);
+        cur = i + 1;
+        ok = mbar_wait(&sm.q_full[s], (gstep / NS) & 1, p.status, abortf, kSiteQFull);
+        if (ok) ok = mbar_wait(&sm.s_full, par, p.status, abortf, kSiteSFull);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t sr[kQ];
+        {
+          uint32_t (&h)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[0]);
+          static_assert(kQ == 32, "the compute code is written for 32 query columns per warpgroup");
+          tmem_ld32(colS, h);
+          tmem_wait_ld(h);
         }
-        *reinterpret_cast<uint4*>(ds_row + (((ch0 + ch) ^ (r & 7)) << 4)) =
-            make_uint4(dsw[ch * 4], dsw[ch * 4 + 1], dsw[ch * 4 + 2], dsw[ch * 4 + 3]);
-      }
-      tmem_st16(colS + kQ / 2, dsw);
-      tmem_wait_st();
-      fence_proxy_async_smem();
-      tc_fence_before();
-      mbar_arrive(&sm.ds_ready);
+        if (p.causal && i == j) {
+  #pragma unroll
+          for (int e = 0; e < kQ; ++e)
+            if (r > g * kQ + e) sr[e] = __float_as_uint(neutral);
+        }
+        const uint64_t* lse2x2 = reinterpret_cast<const uint64_t*>(sm.lse2[s] + g * kQ);
+        const uint64_t c2x2 = f2_pack(c2, c2);
+        uint32_t pk[kQ / 2];
+  #pragma unroll
+        for (int e = 0; e < kQ; e += 2) {
+          float x0, x1;
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), c2x2,
+                           lse2x2[e / 2]),
+                    x0, x1);
+          pk[e / 2] = pack_bf16x2(ex2_approx(x0), ex2_approx(x1));
+        }
+        tmem_st16(colS, pk);
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&sm.p_ready);
 
-      ok = mbar_wait(&sm.dq_full, par, p.status, abortf, kSiteDqFull);
+        ok = mbar_wait(&sm.dp_full, par, p.status, abortf, kSiteDpFull);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t dp[kQ];
+        {
+          uint32_t (&h)[32] = *reinterpret_cast<uint32_t(*)[32]>(&dp[0]);
+          tmem_ld32(colDP, h);
+          tmem_wait_ld(h);
+        }
+        const uint64_t* dlx2 = reinterpret_cast<const uint64_t*>(sm.delta[s] + g * kQ);
+        // dS^T row r, query columns [kQ g, kQ g + kQ): in the 128B-swizzled
+        // [key][query] tile, column block (kQ g) / 64, 16-byte chunks from
+        // ((kQ g) % 64) / 8.
+        uint8_t* ds_row = sm.ds + (g * kQ / 64) * 16384 + r * 128;
+        const int ch0 = (g * kQ % 64) / 8;
+        uint32_t dsw[kQ / 2];
+  #pragma unroll
+        for (int ch = 0; ch < kQ / 8; ++ch) {
+  #pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int col = ch * 8 + 2 * e;
+            const float2 pf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pk[col / 2]));
+            const uint64_t dpd = f2_add(f2_pack(__uint_as_float(dp[col]), __uint_as_float(dp[col + 1])),
+                                        dlx2[col / 2]);
+            float d0, d1;
+            f2_unpack(f2_mul(f2_pack(pf.x, pf.y), dpd), d0, d1);
+            dsw[ch * 4 + e] = pack_bf16x2(d0, d1);
+          }
+          *reinterpret_cast<uint4*>(ds_row + (((ch0 + ch) ^ (r & 7)) << 4)) =
+              make_uint4(dsw[ch * 4], dsw[ch * 4 + 1], dsw[ch * 4 + 2], dsw[ch * 4 + 3]);
+        }
+        tmem_st16(colS + kQ / 2, dsw);
+        tmem_wait_st();
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(&sm.ds_ready);
+
+        ok = mbar_wait(&sm.dq_full, par, p.status, abortf, kSiteDqFull);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        tc_fence_after();
+        if constexpr (D / kWG == 32) {
+          uint32_t a[32];
+          tmem_ld32(colDQ, a);
+          tmem_wait_ld(a);
+          tc_fence_before();
+          mbar_arrive(&sm.dq_empty);
+          add_dq_chunk(p.dq_acc + dqacc_index<D>(bh, p.n_kv, i * kTile + r, g * (D / kWG) / 4), a);
+        } else {
+          uint32_t a[16];
+          tmem_ld16(colDQ, a);
+          tmem_wait_ld16(a);
+          tc_fence_before();
+          mbar_arrive(&sm.dq_empty);
+          float* base = p.dq_acc + dqacc_index<D>(bh, p.n_kv, i * kTile + r, g * (D / kWG) / 4);
+  #pragma unroll
+          for (int e = 0; e < 4; ++e)
+            atomicAdd(reinterpret_cast<float4*>(base + (size_t)e * kTile * 4),
+                      make_float4(__uint_as_float(a[4 * e]), __uint_as_float(a[4 * e + 1]),
+                                  __uint_as_float(a[4 * e + 2]), __uint_as_float(a[4 * e + 3])));
+        }
+      }
+      if (!ok) break;
+      // Epilogue: the first half of the warpgroups stores dV, the second half
+      // scale * dK, each a D / (kWG / 2)-column slice.  The next item's first
+      // dV and dK products overwrite these columns only after this warp's
+      // P-ready and dS-ready arrivals for that item, which come after the
+      // loads below.
+      ok = mbar_wait(&sm.acc_full, m & 1, p.status, abortf, kSiteAccFull);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
-      tc_fence_after();
-      if constexpr (D / kWG == 32) {
-        uint32_t a[32];
-        tmem_ld32(colDQ, a);
-        tmem_wait_ld(a);
-        tc_fence_before();
-        mbar_arrive(&sm.dq_empty);
-        add_dq_chunk(p.dq_acc + dqacc_index<D>(bh, p.n_kv, i * kTile + r, g * (D / kWG) / 4), a);
-      } else {
-        uint32_t a[16];
-        tmem_ld16(colDQ, a);
-        tmem_wait_ld16(a);
-        tc_fence_before();
-        mbar_arrive(&sm.dq_empty);
-        float* base = p.dq_acc + dqacc_index<D>(bh, p.n_kv, i * kTile + r, g * (D / kWG) / 4);
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-          atomicAdd(reinterpret_cast<float4*>(base + (size_t)e * kTile * 4),
-                    make_float4(__uint_as_float(a[4 * e]), __uint_as_float(a[4 * e + 1]),
-                                __uint_as_float(a[4 * e + 2]), __uint_as_float(a[4 * e + 3])));
-      }
-    }
-    // Epilogue: the first half of the warpgroups stores dV, the second half
-    // scale * dK, each a D / (kWG / 2)-column slice.
-    if (ok) ok = mbar_wait(&sm.acc_full, 0, p.status, abortf, kSiteAccFull);
-    ok = __all_sync(0xffffffffu, ok);
-    if (ok) {
       tc_fence_after();
       constexpr int kCols = D / (kWG / 2);
       const bool is_dv = g < kWG / 2;
@@ -513,17 +606,18 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         tmem_wait_ld(a);
         if (kv_row < p.N) {
           uint4 v[4];
-          uint32_t* w = reinterpret_cast<uint32_t*>(v);
+          uint32_t* wv = reinterpret_cast<uint32_t*>(v);
 #pragma unroll
           for (int e = 0; e < 16; ++e)
-            w[e] = n_iter == 0 ? 0u
-                               : pack_bf16x2(__uint_as_float(a[2 * e]) * mul,
-                                             __uint_as_float(a[2 * e + 1]) * mul);
+            wv[e] = w.n_iter == 0 ? 0u
+                                  : pack_bf16x2(__uint_as_float(a[2 * e]) * mul,
+                                                __uint_as_float(a[2 * e + 1]) * mul);
           uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
 #pragma unroll
           for (int e = 0; e < 4; ++e) d4[e] = v[e];
         }
       }
+      tc_fence_before();
     }
   }
 
@@ -558,7 +652,11 @@ int launch_bwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
         cudaSuccess)
       return FA_ERR_LAUNCH;
-    const unsigned grid = (unsigned)p.BH * (unsigned)p.n_kv;
+    // One persistent CTA per SM; each claims the next item of the list
+    // from the workspace counter when it is ready for one (greedy list
+    // scheduling, which under a causal or block mask is the LPT rule).
+    const long long items = (long long)p.BH * p.n_kv;
+    const unsigned grid = (unsigned)(p.sm_count < 1 || items <= p.sm_count ? items : p.sm_count);
     kern<<<grid, BwdCfg<D>::kThreads, smem, stream>>>(tq, tk, tv, tdo, p);
     if (cudaGetLastError() != cudaSuccess) return FA_ERR_LAUNCH;
   }

@@ -117,6 +117,8 @@ struct BwdParams {
   int causal;
   float scale;
   float scale_log2;
+  int* sched;    // workspace: the main kernel's work-item counter (zeroed by prep)
+  int sm_count;  // persistent grid size of the main kernel
 };
 
 // Build a rank-3 tensor map over a [BH][N][d] bf16 array: dims (d, N, BH),
@@ -142,9 +144,11 @@ inline FwdWorkspace fwd_workspace_layout(long long splits, long long BH, long lo
 }
 
 // Byte offsets of the backward workspace's parts for these sizes:
-// the fp32 dQ accumulator, then D, then lse * log2(e), each 256-byte aligned.
+// the fp32 dQ accumulator, then -D, then -lse * log2(e), then the main
+// kernel's work-item counter (one int in a 256-byte slot), each 256-byte
+// aligned.
 struct BwdWorkspace {
-  size_t dq_acc, delta, lse2, total;
+  size_t dq_acc, delta, lse2, sched, total;
 };
 inline BwdWorkspace bwd_workspace_layout(long long BH, int N, int d) {
   const size_t rows = (size_t)BH * (size_t)ceil_div(N, kTile) * kTile;
@@ -153,7 +157,8 @@ inline BwdWorkspace bwd_workspace_layout(long long BH, int N, int d) {
   w.dq_acc = 0;
   w.delta = up(rows * (size_t)d * sizeof(float));
   w.lse2 = w.delta + up(rows * sizeof(float));
-  w.total = w.lse2 + up(rows * sizeof(float));
+  w.sched = w.lse2 + up(rows * sizeof(float));
+  w.total = w.sched + 256;
   return w;
 }
 

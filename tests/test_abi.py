@@ -92,9 +92,10 @@ def test_workspace_size(lib):
     def up(x):
         return (x + 255) // 256 * 256
     rows = 2 * 3 * 384
-    assert lib.fa_bwd_workspace_size(2, 3, 300, 64) == up(rows * 64 * 4) + 2 * up(rows * 4)
-    assert lib.fa_bwd_workspace_size(1, 1, 128, 128) == 128 * 128 * 4 + 2 * 128 * 4
-    assert lib.fa_bwd_workspace_size(1, 1, 1, 64) == 128 * 64 * 4 + 2 * 512
+    # dQ accumulator, -D, -lse*log2(e), then a 256-byte slot for the counter
+    assert lib.fa_bwd_workspace_size(2, 3, 300, 64) == up(rows * 64 * 4) + 2 * up(rows * 4) + 256
+    assert lib.fa_bwd_workspace_size(1, 1, 128, 128) == 128 * 128 * 4 + 2 * 128 * 4 + 256
+    assert lib.fa_bwd_workspace_size(1, 1, 1, 64) == 128 * 64 * 4 + 2 * 512 + 256
     assert lib.fa_bwd_workspace_size(1, 1, 0, 64) == 0
     assert lib.fa_bwd_workspace_size(1, 1, 128, 72) == 0
 
