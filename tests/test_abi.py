@@ -86,6 +86,18 @@ def test_bwd_argument_errors_launch_nothing(lib):
     assert call(wsb=ws - 1) == fa.FA_ERR_WORKSPACE
     assert call(ws=FAKE + 16) == fa.FA_ERR_WORKSPACE
 
+    def phases(mask, **kw):
+        a = dict(q=FAKE, ws=FAKE, wsb=ws)
+        a.update(kw)
+        return lib.fa_bwd_phases(a["q"], FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 128,
+                                 64, 0, ctypes.c_float(0.125), a["ws"], a["wsb"], None, mask)
+
+    # The phase mask is checked first; then the arguments as for fa_bwd.
+    for mask in (0, 8, -1, 15):
+        assert phases(mask) == fa.FA_ERR_ARG
+    assert phases(2, q=None) == fa.FA_ERR_ARG
+    assert phases(4, wsb=ws - 1) == fa.FA_ERR_WORKSPACE
+
 
 def test_workspace_size(lib):
     # fp32 dQ accumulator over 128-row-padded rows plus two fp32 per row.
