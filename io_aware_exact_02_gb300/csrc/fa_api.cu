@@ -244,7 +244,7 @@ int fwd_fp8_quantized_impl(void* o, float* lse, int B, int H, int N, int d, int 
   p.causal = causal;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.grid = fwd_grid(BH, p.n_pairs, causal, ds->sm_count);
-  return launch_fwd(tq, tk, tv, p, d, static_cast<cudaStream_t>(stream));
+  return launch_fwd(tq, tk, tv, tq, p, d, static_cast<cudaStream_t>(stream));  // O stored directly
 }
 
 int fp8_quantize_impl(const void* q, const void* k, const void* v, int B, int H, int N, int d,
@@ -279,10 +279,11 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
     return FA_ERR_WORKSPACE;
   DeviceState* ds;
   if ((rc = device_state(&ds)) != FA_OK) return rc;
-  CUtensorMap tq, tk, tv;
+  CUtensorMap tq, tk, tv, to;
   if ((rc = make_tmap_bhnd(q, g.BH, g.rows, d, &tq)) != FA_OK) return rc;
   if ((rc = make_tmap_bhnd(k, g.BH, Nkv, d, &tk)) != FA_OK) return rc;
   if ((rc = make_tmap_bhnd(v, g.BH, Nkv, d, &tv)) != FA_OK) return rc;
+  if ((rc = make_tmap_bhnd(o, g.BH, g.rows, d, &to)) != FA_OK) return rc;
   FwdParams p;
   p.o = o;
   p.lse = lse;
@@ -309,7 +310,7 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
   p.scale_log2 = scale * 1.4426950408889634f;
   // Block-sparse items differ in cost like causal ones: one CTA per item.
   p.grid = fwd_grid(g.BH, g.n_pairs * g.splits, causal || block_mask != nullptr, ds->sm_count);
-  return launch_fwd(tq, tk, tv, p, d, static_cast<cudaStream_t>(stream));
+  return launch_fwd(tq, tk, tv, to, p, d, static_cast<cudaStream_t>(stream));
 }
 
 // The backward pass; block_mask is null for dense attention.

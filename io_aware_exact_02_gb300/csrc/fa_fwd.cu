@@ -12,11 +12,12 @@
 // per-row logsumexp are stored (cs2680 Lecture 9, sec. 9.2 and 9.4; CMU post,
 // slide pages 9-12).
 //
-// Warp roles (320 threads):
+// Warp roles (320 threads; 352 when O is staged):
 //   warps 0-3  softmax for Q tile 0 (thread r owns row r of the tile)
 //   warps 4-7  softmax for Q tile 1
 //   warp 8     TMA producer: Q tiles once, then K_0, V_0, K_1, V_1, ...
 //   warp 9     MMA issuer (one thread) and TMEM owner
+//   warp 10    (kStage) O store warp: TMA stores of the staged O tiles
 // The two softmax warpgroups ping-pong: while one exponentiates its tile
 // the tensor core computes the other tile's S and PV products (the overlap
 // the CMU post motivates on slide pages 20-22 and 51-52).
@@ -46,7 +47,8 @@ template <int D, bool kFp8 = false>
 struct FwdCfg {
   static constexpr int kTileBytes = kTile * D * (kFp8 ? 1 : 2);  // one 128 x d tile
   static constexpr int kStages = kFp8 ? 10 : ((D == 128) ? 5 : 8);  // K/V ring slots
-  static constexpr int kThreads = 320;
+  // 2 softmax warpgroups, producer, MMA (and the O store warp when staging).
+  static constexpr int threads(bool stage) { return stage ? 352 : 320; }
   static constexpr uint32_t kTmemCols = 512;
   // TMEM column of S/P and of O for Q tile t.
   static __device__ __forceinline__ uint32_t col_s(int t) { return (uint32_t)t * 128u; }
@@ -71,6 +73,9 @@ struct alignas(1024) FwdSmem {
   uint64_t p_full[2];
   uint64_t o_full[2];
   uint64_t o_empty[2];  // softmax t has read O_t of the item (epilogue done)
+  uint64_t staged[2];   // softmax t has written O_t into its ring slot for the store
+  uint64_t stored[2];   // the store warp has read softmax t's staged O_t
+  uint64_t stage_ready[2];  // softmax t's staging slot of the item is free
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
@@ -79,7 +84,7 @@ struct alignas(1024) FwdSmem {
 // Wait sites reported through the status word.
 enum : int {
   kSiteQFull = 101, kSiteKvEmpty, kSiteKvFull, kSitePFull, kSiteSFull, kSiteOFull, kSiteDrain,
-  kSiteQEmpty, kSiteOEmpty
+  kSiteQEmpty, kSiteOEmpty, kSiteStageSlot, kSiteStaged, kSiteStored
 };
 
 // Descriptor of the K-major, 128B-swizzled tile at `base` for MMA K-step kk:
@@ -116,10 +121,11 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
 // slide pages 18 and 24); S and O += P V run as kind::f8f6f4 products, P is
 // rounded to E4M3 in tensor memory, and V arrives transposed ([d][keys]) so
 // that both operands of O += P V are K-major.
-template <int D, bool kNeg, bool kGeneral, bool kSparse, bool kFp8>
-__global__ void __launch_bounds__(FwdCfg<D, kFp8>::kThreads, 1)
+template <int D, bool kNeg, bool kGeneral, bool kSparse, bool kFp8, bool kStage>
+__global__ void __launch_bounds__(FwdCfg<D, kFp8>::threads(kStage), 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
-                  const __grid_constant__ CUtensorMap tv, const FwdParams p) {
+                  const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap to,
+                  const FwdParams p) {
   using Cfg = FwdCfg<D, kFp8>;
   constexpr int S = Cfg::kStages;
   extern __shared__ uint8_t smem_raw[];
@@ -141,6 +147,9 @@ __global__ void __launch_bounds__(FwdCfg<D, kFp8>::kThreads, 1)
       mbar_init(&sm.p_full[t], 128);
       mbar_init(&sm.o_full[t], 1);
       mbar_init(&sm.o_empty[t], 128);
+      mbar_init(&sm.staged[t], 128);
+      mbar_init(&sm.stored[t], 1);
+      mbar_init(&sm.stage_ready[t], 1);
     }
     mbar_init(&sm.drain, 1);
     sm.abort_flag = 0;
@@ -162,6 +171,15 @@ __global__ void __launch_bounds__(FwdCfg<D, kFp8>::kThreads, 1)
   const int splits = kGeneral ? p.splits : 1;
   const int num_items = p.BH * p.n_pairs * splits;
   const int G = gridDim.x;
+  // kStage (square bf16 kernels on persistent CTAs): O leaves through the
+  // K/V ring.  After an item's last K/V tiles the ring takes two more uses,
+  // one per Q tile, in which the producer loads nothing; softmax warpgroup
+  // t writes its O tile into that slot (128B-swizzled, as the TMA boxes)
+  // and the store warp sends it out with TMA stores and then releases the
+  // slot, so the softmax warps go on to the next item without waiting for
+  // the stores.
+  constexpr bool stage_epi = kStage;
+  constexpr int ring_per_item_extra = stage_epi ? 2 : 0;
   auto item_of_round = [&](int k) -> int {
     const int base = k * G;
     return (k & 1) ? base + (G - 1 - (int)blockIdx.x) : base + (int)blockIdx.x;
@@ -228,6 +246,7 @@ __global__ void __launch_bounds__(FwdCfg<D, kFp8>::kThreads, 1)
       prefetch_tmap(&tv);
       int c = 0;         // K/V loads issued, over all items
       int q_issued = 0;  // Q pairs issued
+      int n_staged = 0;  // items whose O staging uses were handed over
       bool ok = true;
       for (int k = 0; ok && k * G < num_items; ++k) {
         const int idx = item_of_round(k);
@@ -291,6 +310,25 @@ __global__ void __launch_bounds__(FwdCfg<D, kFp8>::kThreads, 1)
               }
             }
           }
+          // The item's two O staging uses: hand the slots over empty, each
+          // once the store warp has read the warpgroup's previous staged tile
+          // (so that a warpgroup is never two staged tiles ahead of it).
+          for (int t = 0; t < ring_per_item_extra && ok; ++t, ++c) {
+            const int slot = c % S, use = c / S;
+            if (use > 0 &&
+                !mbar_wait(&sm.kv_empty[slot], (use - 1) & 1, p.status, abortf, kSiteKvEmpty)) {
+              ok = false;
+              break;
+            }
+            if (n_staged > 0 &&
+                !mbar_wait(&sm.stored[t], (n_staged - 1) & 1, p.status, abortf, kSiteStored)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive(&sm.kv_full[slot]);
+            mbar_arrive(&sm.stage_ready[t]);
+          }
+          if (stage_epi) ++n_staged;
         }
       }
       if (!ok) {
@@ -413,7 +451,7 @@ __global__ void __launch_bounds__(FwdCfg<D, kFp8>::kThreads, 1)
             }
             if (ok) tc_commit(&sm.kv_empty[vc % S]);
           }
-          cb += 2 * nmax;
+          cb += 2 * nmax + ring_per_item_extra;
         } else {
           // Block-sparse: Q tile t walks its own n_t[t] active key tiles.
           // Step j's loads are K and V of tile 0's j-th tile, then of tile
@@ -491,6 +529,40 @@ __global__ void __launch_bounds__(FwdCfg<D, kFp8>::kThreads, 1)
       drain_wait(&sm.drain, 0);
     }
     __syncwarp();
+  } else if (warp == 10) {
+    // ------------------------------------------------------------ O store warp
+    // Sends each staged O tile out with TMA stores (rows past the tensor's
+    // end are not written) and releases its ring slot once the stores have
+    // read it.
+    if (lane_id() == 0 && stage_epi) {
+      int cb = 0, n_staged = 0;
+      bool ok = true;
+      for (int k = 0; ok && k * G < num_items; ++k) {
+        const int idx = item_of_round(k);
+        if (idx >= num_items) continue;
+        const Item it = decode(idx);
+        if (it.nmax == 0) continue;
+        for (int t = 0; t < 2 && ok; ++t) {
+          const int use = cb + 2 * it.nmax + t;
+          const int slot = use % S;
+          if (!mbar_wait_sleep(&sm.staged[t], n_staged & 1, p.status, abortf, kSiteStaged)) {
+            ok = false;
+            break;
+          }
+          for (int h = 0; h < Cfg::kBoxes; ++h)
+            tma_store_3d(&to, sm.kv[slot] + h * 16384, h * 64, it.row0 + t * kTile, it.bh);
+          bulk_commit_group();
+          bulk_wait_group_read0();
+          mbar_arrive(&sm.stored[t]);
+          mbar_arrive(&sm.kv_empty[slot]);
+        }
+        ++n_staged;
+        cb += 2 * it.nmax + ring_per_item_extra;
+      }
+      // The stores must be complete before the CTA exits.
+      bulk_wait_group0();
+    }
+    __syncwarp();
   } else if (warp < 8) {
     // ------------------------------------------------------------ softmax
     const int t = warp >> 2;             // which Q tile
@@ -505,6 +577,8 @@ __global__ void __launch_bounds__(FwdCfg<D, kFp8>::kThreads, 1)
     const uint32_t colO = tmem + lane_base + Cfg::col_o(t);
     uint32_t s_par = 0;
     int n_done = 0;
+    int cb = 0;        // ring uses before the current item (as the MMA thread counts them)
+    int n_staged = 0;  // this warpgroup's O tiles handed to the store warp
     bool ok = true;
 
     for (int k = 0; ok && k * G < num_items; ++k) {
@@ -513,6 +587,10 @@ __global__ void __launch_bounds__(FwdCfg<D, kFp8>::kThreads, 1)
       const Item item = decode(idx);
       const int bh = item.bh;
       const int n_t = item.n_t[t];
+      // This tile's O staging use of the ring, when the item has one.
+      const bool staged = stage_epi && item.nmax > 0;
+      const int stage_use = cb + 2 * item.nmax + t;
+      if (item.nmax > 0) cb += 2 * item.nmax + ring_per_item_extra;
       float o_mul = 1.f;  // FP8: the V scale, applied with 1 / l
       if constexpr (kFp8) {
         // Scores of codes carry the Q and K scales (and d, the squared norm
@@ -653,6 +731,41 @@ __global__ void __launch_bounds__(FwdCfg<D, kFp8>::kThreads, 1)
       const float inv_l = any ? o_mul / l : 0.f;
       const bool valid = R < p.rows;
       const size_t row_g = (size_t)bh * p.rows + R;
+      if (staged) {
+        const int slot = stage_use % S;
+        ok = mbar_wait(&sm.stage_ready[t], n_staged & 1, p.status, abortf, kSiteStageSlot);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        // Row r of the tile in the 128B-swizzled layout of the TMA boxes
+        // (64 columns each): 16-byte chunk ch of the row at ch ^ (r % 8).
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t orow[32];
+          tmem_ld32(colO + c * 32, orow);
+          tmem_wait_ld(orow);
+          uint8_t* rowp = sm.kv[slot] + (c / 2) * 16384 + r * 128;
+          uint32_t w[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            w[i] = any ? pack_bf16x2(__uint_as_float(orow[2 * i]) * inv_l,
+                                     __uint_as_float(orow[2 * i + 1]) * inv_l)
+                       : 0u;
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            *reinterpret_cast<uint4*>(rowp + ((((c % 2) * 4 + e) ^ (r & 7)) << 4)) =
+                make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+        }
+        fence_proxy_async_smem();
+        // O_t may now be overwritten by the next item's first product, and
+        // the staged tile stored.
+        tc_fence_before();
+        mbar_arrive(&sm.o_empty[t]);
+        mbar_arrive(&sm.staged[t]);
+        if (valid) p.lse[row_g] = any ? (m_ref + __log2f(l)) * kLn2 : ninf;
+        ++n_staged;
+        ++n_done;
+        continue;
+      }
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t orow[32];
@@ -758,15 +871,16 @@ __global__ void __launch_bounds__(256) fa_combine_kernel(const FwdParams p) {
   if (lane == 0) p.lse[row] = lse_row;
 }
 
-template <int D, bool kNeg, bool kGeneral, bool kSparse = false, bool kFp8 = false>
+template <int D, bool kNeg, bool kGeneral, bool kSparse = false, bool kFp8 = false,
+          bool kStage = false>
 int launch_fwd_dn(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                  const FwdParams& p, cudaStream_t stream) {
+                  const CUtensorMap& to, const FwdParams& p, cudaStream_t stream) {
   const size_t smem = sizeof(FwdSmem<D, kFp8>) + 1024;
-  if (cudaFuncSetAttribute(fa_fwd_kernel<D, kNeg, kGeneral, kSparse, kFp8>,
+  if (cudaFuncSetAttribute(fa_fwd_kernel<D, kNeg, kGeneral, kSparse, kFp8, kStage>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return FA_ERR_LAUNCH;
-  fa_fwd_kernel<D, kNeg, kGeneral, kSparse, kFp8>
-      <<<(unsigned)p.grid, FwdCfg<D, kFp8>::kThreads, smem, stream>>>(tq, tk, tv, p);
+  fa_fwd_kernel<D, kNeg, kGeneral, kSparse, kFp8, kStage>
+      <<<(unsigned)p.grid, FwdCfg<D, kFp8>::threads(kStage), smem, stream>>>(tq, tk, tv, to, p);
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_LAUNCH;
   if (p.splits > 1) {
     const long long threads = (long long)p.BH * p.rows * 32;
@@ -778,36 +892,44 @@ int launch_fwd_dn(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMa
 
 template <int D>
 int launch_fwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                 FwdParams p, cudaStream_t stream) {
+                 const CUtensorMap& to, FwdParams p, cudaStream_t stream) {
   // A zero scale makes every unmasked probability equal; it runs as the
   // smallest normal positive scale, whose exponents round to exactly 0.
   if (p.scale_log2 == 0.f) p.scale_log2 = 1.17549435e-38f;
   const bool general = p.splits > 1 || p.Nq != p.rows || p.Nkv != p.rows;
   if (p.fp8_amax) {  // square case, d = 128 only (checked by the caller)
     if constexpr (D == 128) {
-      if (p.scale_log2 < 0.f) return launch_fwd_dn<D, true, false, false, true>(tq, tk, tv, p, stream);
-      return launch_fwd_dn<D, false, false, false, true>(tq, tk, tv, p, stream);
+      if (p.scale_log2 < 0.f) return launch_fwd_dn<D, true, false, false, true>(tq, tk, tv, to, p, stream);
+      return launch_fwd_dn<D, false, false, false, true>(tq, tk, tv, to, p, stream);
     }
     return FA_ERR_UNSUPPORTED_D;
   }
   if (p.block_mask) {  // square case only (checked by the caller)
-    if (p.scale_log2 < 0.f) return launch_fwd_dn<D, true, false, true>(tq, tk, tv, p, stream);
-    return launch_fwd_dn<D, false, false, true>(tq, tk, tv, p, stream);
+    if (p.scale_log2 < 0.f) return launch_fwd_dn<D, true, false, true>(tq, tk, tv, to, p, stream);
+    return launch_fwd_dn<D, false, false, true>(tq, tk, tv, to, p, stream);
   }
   if (general) {
-    if (p.scale_log2 < 0.f) return launch_fwd_dn<D, true, true>(tq, tk, tv, p, stream);
-    return launch_fwd_dn<D, false, true>(tq, tk, tv, p, stream);
+    if (p.scale_log2 < 0.f) return launch_fwd_dn<D, true, true>(tq, tk, tv, to, p, stream);
+    return launch_fwd_dn<D, false, true>(tq, tk, tv, to, p, stream);
   }
-  if (p.scale_log2 < 0.f) return launch_fwd_dn<D, true, false>(tq, tk, tv, p, stream);
-  return launch_fwd_dn<D, false, false>(tq, tk, tv, p, stream);
+  // Staged O stores pay where items are short (N <= 2K at d = 128) and, at
+  // d = 64, at every length; they need persistent CTAs (no mask).
+  const long long items = (long long)p.BH * p.n_pairs;
+  if (p.grid < items && (D == 64 || p.n_kv <= 16)) {
+    if (p.scale_log2 < 0.f)
+      return launch_fwd_dn<D, true, false, false, false, true>(tq, tk, tv, to, p, stream);
+    return launch_fwd_dn<D, false, false, false, false, true>(tq, tk, tv, to, p, stream);
+  }
+  if (p.scale_log2 < 0.f) return launch_fwd_dn<D, true, false>(tq, tk, tv, to, p, stream);
+  return launch_fwd_dn<D, false, false>(tq, tk, tv, to, p, stream);
 }
 
 }  // namespace
 
 int launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-               const FwdParams& p, int d, cudaStream_t stream) {
-  if (d == 128) return launch_fwd_d<128>(tq, tk, tv, p, stream);
-  if (d == 64) return launch_fwd_d<64>(tq, tk, tv, p, stream);
+               const CUtensorMap& to, const FwdParams& p, int d, cudaStream_t stream) {
+  if (d == 128) return launch_fwd_d<128>(tq, tk, tv, to, p, stream);
+  if (d == 64) return launch_fwd_d<64>(tq, tk, tv, to, p, stream);
   return FA_ERR_UNSUPPORTED_D;
 }
 

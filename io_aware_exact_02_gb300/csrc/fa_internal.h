@@ -126,8 +126,10 @@ struct BwdParams {
 // FA_ERR_* code.
 int make_tmap_bhnd(const void* base, int BH, int N, int d, CUtensorMap* out);
 
+// `to` is a tensor map over O with the shape of tq's; only the square bf16
+// kernels that stage O for TMA stores use it.
 int launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-               const FwdParams& p, int d, cudaStream_t stream);
+               const CUtensorMap& to, const FwdParams& p, int d, cudaStream_t stream);
 
 // Byte offsets of the general forward pass's split workspace: each split's
 // fp32 O, then each split's lse, 256-byte aligned.

@@ -163,6 +163,27 @@ def test_fwd_full_size_sampled(name):
     sampled_check(w, o, lse, q, k, v)
 
 
+@pytest.mark.parametrize("N,d", [(1000, 128), (1920, 128), (3000, 64), (257, 64)])
+def test_fwd_staged_stores_ragged(N, d):
+    # Non-causal grids with more items than SMs, at d = 64 or N <= 2K, store
+    # O through the staging ring slots with TMA; the tail tile of every head
+    # is partly past N (rows there must not be written).  Sampled rows of the
+    # first, last and random heads, including each head's last rows.
+    from io_aware_exact_02_gb300.synth import Workload
+    w = Workload("staged_N%d_d%d" % (N, d), 8, 24, N, d, False)
+    q, k, v, _ = synth.draw_workload(w, seed=N + d, with_dout=False)
+    dev = torch.device("cuda")
+    # A guard band after O catches a store past the end of the tensor.
+    o_buf = torch.full((w.B * w.H * N * d + 4096,), 7.0, dtype=torch.bfloat16, device=dev)
+    o = o_buf[: w.B * w.H * N * d].view(w.B, w.H, N, d)
+    lse = torch.empty((w.B, w.H, N), dtype=torch.float32, device=dev)
+    fa.fwd(q.to(dev), k.to(dev), v.to(dev), causal=False, scale=w.softmax_scale, out=o, lse=lse)
+    fa.check_device_status()
+    assert torch.all(o_buf[w.B * w.H * N * d:] == 7.0)
+    assert torch.isfinite(o).all() and torch.isfinite(lse).all()
+    sampled_check(w, o, lse, q, k, v, n_heads=4, n_rows=40, seed=N)
+
+
 def test_fwd_long_sequence_sampled_rows():
     # N = 65536 (512 key tiles per head) causal and not: sampled rows against
     # the oracle's row-wise definition.
