@@ -247,7 +247,8 @@ int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, c
  * current device: FA_OK, FA_ERR_TIMEOUT if a kernel gave up on a pipeline
  * wait since the last call, or FA_ERR_LAUNCH if the stream holds a CUDA
  * error.  If `site` is not NULL it receives the identifier of the first wait
- * that timed out (0 if none).
+ * that timed out (0 if none): 101-199 a wait of the forward kernel, 201-299
+ * one of the backward main kernel, FA_SITE_SELFTEST the self test's.
  */
 int fa_device_status(void* stream, int* site);
 
