@@ -361,43 +361,60 @@ def run_gpu(args, w, rank, world, local_rank):
         hdq, hdk, hdv = (torch.empty(q.shape, dtype=q.dtype).pin_memory() for _ in range(3))
 
         # Pipelined like a user streaming batches: two sets of device
-        # buffers; step k's inputs go up on one stream and its results come
-        # back on another while the compute stream runs step k-1 / k+1.  Every
+        # buffers; step k's inputs go up while the compute stream runs step
+        # k-1 and its results come back while it runs step k+1.  Each copy
+        # direction is spread over several streams (one tensor per stream),
+        # so that more than one copy engine moves the step's gigabyte.  Every
         # step still copies its own inputs in and all of its outputs out
         # inside the timed region.
         sets = [(q, k, v, do, o, lse, dq, dk, dv, ws)]
         sets.append(tuple(torch.empty_like(t) for t in sets[0]))
-        up, comp, down = (torch.cuda.Stream(dev) for _ in range(3))
+        nc = max(1, args.e2e_copy_streams)
+        ups = [torch.cuda.Stream(dev) for _ in range(nc)]
+        downs = [torch.cuda.Stream(dev) for _ in range(nc)]
+        comp = torch.cuda.Stream(dev)
 
         def e2e_run(n):
-            done_down = [None, None]  # set b's last D2H (its buffers are free after it)
+            done_down = [[], []]  # set b's last D2H events (its buffers are free after them)
             start = torch.cuda.Event(enable_timing=True)
             end = torch.cuda.Event(enable_timing=True)
-            start.record(up)
+            start.record(ups[0])
+            for u in ups[1:]:
+                u.wait_event(start)
             for step in range(n):
                 b = step % 2
                 bq, bk, bv, bdo, bo, blse, bdq, bdk, bdv, bws = sets[b]
-                if done_down[b] is not None:
-                    up.wait_event(done_down[b])
-                with torch.cuda.stream(up):
-                    for dst, src in ((bq, hq), (bk, hk), (bv, hv), (bdo, hdo)):
+                loaded = []
+                for i, (dst, src) in enumerate(((bq, hq), (bk, hk), (bv, hv), (bdo, hdo))):
+                    u = ups[i % nc]
+                    for ev in done_down[b]:
+                        u.wait_event(ev)
+                    with torch.cuda.stream(u):
                         dst.copy_(src, non_blocking=True)
-                    loaded = torch.cuda.Event()
-                    loaded.record(up)
-                comp.wait_event(loaded)
+                        ev = torch.cuda.Event()
+                        ev.record(u)
+                    loaded.append(ev)
+                for ev in loaded:
+                    comp.wait_event(ev)
                 with torch.cuda.stream(comp):
                     fa.fwd(bq, bk, bv, causal=causal, scale=scale, out=bo, lse=blse)
                     fa.bwd(bq, bk, bv, bo, bdo, blse, causal=causal, scale=scale, dq=bdq, dk=bdk,
                            dv=bdv, workspace=bws)
                     computed = torch.cuda.Event()
                     computed.record(comp)
-                down.wait_event(computed)
-                with torch.cuda.stream(down):
-                    for dst, src in ((ho, bo), (hlse, blse), (hdq, bdq), (hdk, bdk), (hdv, bdv)):
+                done_down[b] = []
+                for j, (dst, src) in enumerate(((hdq, bdq), (hdk, bdk), (hdv, bdv), (ho, bo),
+                                                (hlse, blse))):
+                    dn = downs[j % nc]
+                    dn.wait_event(computed)
+                    with torch.cuda.stream(dn):
                         dst.copy_(src, non_blocking=True)
-                    done_down[b] = torch.cuda.Event()
-                    done_down[b].record(down)
-            end.record(down)
+                        ev = torch.cuda.Event()
+                        ev.record(dn)
+                    done_down[b].append(ev)
+            for ev in done_down[0] + done_down[1]:
+                downs[0].wait_event(ev)
+            end.record(downs[0])
             return start, end
 
         e2e_run(2)
@@ -413,7 +430,7 @@ def run_gpu(args, w, rank, world, local_rank):
         e2e = {"value": aggregate((ff + bf) * e2e_steps, world, e2e_sec), "unit": UNIT,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
                "pipelined": "H2D of step k+1 and D2H of step k-1 overlap step k's kernels "
-                            "(two device buffer sets, three streams)"}
+                            "(two device buffer sets, %d copy streams per direction)" % nc}
 
     # ------------------------------------------------------------ roofline
     peaks, peak_kind = load_peaks()
@@ -776,6 +793,8 @@ def main(argv=None):
     ap.add_argument("--ref-heads", type=int, default=1,
                     help="heads of the workload per step of the reference arm")
     ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--e2e-copy-streams", type=int, default=1,
+                    help="streams per copy direction in the end-to-end run")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
