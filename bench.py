@@ -362,11 +362,11 @@ def run_gpu(args, w, rank, world, local_rank):
 
         # Pipelined like a user streaming batches: two sets of device
         # buffers; step k's inputs go up while the compute stream runs step
-        # k-1 and its results come back while it runs step k+1.  Each copy
-        # direction is spread over several streams (one tensor per stream),
-        # so that more than one copy engine moves the step's gigabyte.  Every
-        # step still copies its own inputs in and all of its outputs out
-        # inside the timed region.
+        # k-1 and its results come back while it runs step k+1.  With
+        # --e2e-copy-streams > 1 each copy direction is spread over that many
+        # streams (tensors round-robin), so that several copy engines can move
+        # the step's gigabyte.  Every step still copies its own inputs in and
+        # all of its outputs out inside the timed region.
         sets = [(q, k, v, do, o, lse, dq, dk, dv, ws)]
         sets.append(tuple(torch.empty_like(t) for t in sets[0]))
         nc = max(1, args.e2e_copy_streams)
