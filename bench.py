@@ -272,6 +272,56 @@ def run_reference(args, w, rank, world):
 
 # ------------------------------------------------------------------ GPU arm
 
+SWEEP_N = (1024, 2048, 4096, 16384)
+
+
+def n_sweep(dev, seed, steps=5, warmup=3):
+    """The metric's range at d = 128 (B=8, H=16, non-causal): forward and
+    backward TFLOPS per N, each kernel call timed with CUDA events on the
+    launching stream, L2 flushed before every call whose inputs fit in it."""
+    import torch
+    from io_aware_exact_02_gb300 import fa, synth
+    out = {}
+    flush = None
+    for N in SWEEP_N:
+        B, H, d = 8, 16, 128
+        q, k, v, do = synth.draw(B, H, N, d, seed=seed, device=dev)
+        o = torch.empty_like(q)
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+        ws = torch.empty(fa.bwd_workspace_size(B, H, N, d), dtype=torch.uint8, device=dev)
+        small = q.numel() * q.element_size() <= L2_BYTES
+        if small and flush is None:
+            flush = l2_flush_buffer(dev)
+        stream = torch.cuda.current_stream(dev)
+
+        def call(which):
+            if which == 0:
+                fa.fwd(q, k, v, out=o, lse=lse)
+            else:
+                fa.bwd(q, k, v, o, do, lse, dq=dq, dk=dk, dv=dv, workspace=ws)
+
+        times = [0.0, 0.0]
+        for it in range(warmup + steps):
+            for which in (0, 1):
+                if small:
+                    flush.zero_()
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                call(which)
+                e1.record(stream)
+                torch.cuda.synchronize(dev)
+                if it >= warmup:
+                    times[which] += e0.elapsed_time(e1) / 1e3
+        fa.check_device_status()
+        ff = fwd_flops(B, H, N, d, False)
+        out["N%d" % N] = {"fwd_tflops": ff * steps / times[0] / 1e12,
+                          "bwd_tflops": 2.5 * ff * steps / times[1] / 1e12}
+        del q, k, v, do, o, lse, dq, dk, dv, ws
+    return out
+
+
 def run_gpu(args, w, rank, world, local_rank):
     import torch
     from io_aware_exact_02_gb300 import fa, synth
@@ -473,6 +523,10 @@ def run_gpu(args, w, rank, world, local_rank):
                                  "sample": "forward of 256 query rows of one head, 1 thread, "
                                            "%.2f s" % st_dt}}
 
+    sweep = None
+    if world == 1 and not args.no_sweep and w["name"] == WORKLOAD["name"]:
+        sweep = n_sweep(dev, seed)
+
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
@@ -489,6 +543,10 @@ def run_gpu(args, w, rank, world, local_rank):
             "clocks": clocks, "e2e": e2e, "gpu_launches": launches_per_step * args.steps,
             "roofline": roofline, "cpu_baseline": cpu, "kernels": kernels,
         }
+        if sweep is not None:
+            line["n_sweep_d128"] = dict(sweep, note="B=8 H=16 d=128 non-causal, per kernel "
+                                        "call, L2 flushed when the inputs fit in it; outside "
+                                        "the timed region")
         print(json.dumps(line), flush=True)
     return 0
 
@@ -796,6 +854,8 @@ def main(argv=None):
     ap.add_argument("--e2e-copy-streams", type=int, default=1,
                     help="streams per copy direction in the end-to-end run")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-sweep", action="store_true",
+                    help="skip the d=128 N sweep (1K, 2K, 4K, 16K) reported beside the headline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
 
