@@ -19,6 +19,10 @@ before every timed step outside that step's CUDA events.
 
 ``--impl reference`` times the fp64 CPU oracle (the reference arm of this
 build) on a bounded sample of the same workload on the host cores.
+
+The default (N = 1) line also reports ``n_sweep_d128``: forward and backward
+TFLOPS at N = 1K, 2K, 4K and 16K (B=8, H=16, d=128), measured after the timed
+region (``--no-sweep`` skips it).
 """
 from __future__ import annotations
 
