@@ -45,7 +45,10 @@
 // Tensor memory: [0,128) S^T; warpgroup g's 32 columns [32g, 32g+32) take
 // P^T (bf16 pairs) over their first 16 and dS^T over the last 16, so that
 // dV += P^T dO and dK += dS^T Q take their A operand from tensor memory;
-// [128,256) dP^T, then dQ; [256,256+d) dV; [256+d, 256+2d) dK.
+// [128,256) dP^T, then dQ; [256,256+d) dV; [256+d, 256+2d) dK.  At d = 64
+// the free columns [384,512) are a second S^T region: step i+1's S^T is
+// issued right after step i's dP^T, the compute warps run P(i+1) while the
+// tensor core does dK(i) and dQ(i), and read dQ(i) out after P(i+1).
 #include "fa_internal.h"
 #include "sm100_ptx.cuh"
 
@@ -64,6 +67,10 @@ struct BwdCfg {
   static constexpr int kWarpLoad = kWG * 4, kWarpMma = kWG * 4 + 1;
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D;
+  // d = 64 leaves 128 columns free: a second S^T region, so that the next
+  // step's S^T and P phase overlap this step's dK and dQ products.
+  static constexpr bool kDbl = D == 64;
+  static constexpr uint32_t kColS2 = 256 + 2 * D;
 };
 
 template <int D>
@@ -80,7 +87,8 @@ struct BwdSmem {
   int item_idx[2];
   uint64_t q_full[BwdCfg<D>::kStages];
   uint64_t q_empty[BwdCfg<D>::kStages];
-  uint64_t s_full, dp_full, p_ready, ds_ready, dq_full, dq_empty, acc_full, drain;
+  uint64_t s_full[2];  // per S^T region (one region unless BwdCfg::kDbl)
+  uint64_t dp_full, p_ready, ds_ready, dq_full, dq_empty, acc_full, drain;
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -259,7 +267,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       mbar_init(&sm.q_full[s], 1);
       mbar_init(&sm.q_empty[s], 1);
     }
-    mbar_init(&sm.s_full, 1);
+    mbar_init(&sm.s_full[0], 1);
+    mbar_init(&sm.s_full[1], 1);
     mbar_init(&sm.dp_full, 1);
     mbar_init(&sm.p_ready, kWG * 128);
     mbar_init(&sm.ds_ready, kWG * 128);
@@ -399,6 +408,61 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
           ok = mbar_wait(&sm.kv_full, kvc & 1, p.status, abortf, kSiteKvFull);
           if (!ok) break;
         }
+        if constexpr (Cfg::kDbl) {
+          // S^T of global step gs into region gs & 1.
+          auto issue_st = [&](int gs) -> bool {
+            const int s2 = gs % NS;
+            if (!mbar_wait(&sm.q_full[s2], (gs / NS) & 1, p.status, abortf, kSiteQFull))
+              return false;
+            tc_fence_after();
+            const uint32_t qb2 = smem_u32(sm.q[s2]);
+            const uint32_t col = (gs & 1) ? Cfg::kColS2 : Cfg::kColS;
+#pragma unroll 1
+            for (int kk = 0; kk < D / 16; ++kk)
+              mma_ss(tmem + col, kmajor_desc(kb, kk), kmajor_desc(qb2, kk), id_s, kk > 0);
+            tc_commit(&sm.s_full[gs & 1]);
+            return true;
+          };
+          if (w.n_iter > 0 && !(ok = issue_st(gstep))) break;
+          for (int it = 0; it < w.n_iter; ++it, ++gstep) {
+            const int s = gstep % NS;
+            const uint32_t par = gstep & 1;
+            const uint32_t cs = par ? Cfg::kColS2 : Cfg::kColS;
+            const uint32_t qb = smem_u32(sm.q[s]), dob = smem_u32(sm.dO[s]);
+            // dP^T into the columns the previous step's dQ occupied
+            if (gstep > 0) {
+              ok = mbar_wait(&sm.dq_empty, (gstep - 1) & 1, p.status, abortf, kSiteDqEmpty);
+              if (!ok) break;
+              tc_fence_after();
+            }
+#pragma unroll 1
+            for (int kk = 0; kk < D / 16; ++kk)
+              mma_ss(tmem + Cfg::kColDP, kmajor_desc(vb, kk), kmajor_desc(dob, kk), id_s, kk > 0);
+            tc_commit(&sm.dp_full);
+            // The next step's S^T into the other region (its previous step's
+            // dV and dK, issued earlier, have read it).
+            if (it + 1 < w.n_iter && !(ok = issue_st(gstep + 1))) break;
+            ok = mbar_wait(&sm.p_ready, par, p.status, abortf, kSitePReady);
+            if (!ok) break;
+            tc_fence_after();
+#pragma unroll 1
+            for (int kk = 0; kk < kTile / 16; ++kk)
+              mma_ts(tmem + Cfg::kColDV, tmem + cs + (kk * 16 / kQ) * kQ + (kk * 16 % kQ) / 2,
+                     mnmajor_desc(dob, kk), id_acc, (it > 0 || kk > 0) ? 1u : 0u);
+            ok = mbar_wait(&sm.ds_ready, par, p.status, abortf, kSiteDsReady);
+            if (!ok) break;
+            tc_fence_after();
+#pragma unroll 1
+            for (int kk = 0; kk < kTile / 16; ++kk)
+              mma_ts(tmem + Cfg::kColDK, tmem + cs + kQ / 2 + (kk * 16 / kQ) * kQ + (kk * 16 % kQ) / 2,
+                     mnmajor_desc(qb, kk), id_acc, (it > 0 || kk > 0) ? 1u : 0u);
+            tc_commit(&sm.q_empty[s]);
+#pragma unroll 1
+            for (int kk = 0; kk < kTile / 16; ++kk)
+              mma_ss(tmem + Cfg::kColDP, mnmajor_desc(dsb, kk), mnmajor_desc(kb, kk), id_dq, kk > 0);
+            tc_commit(&sm.dq_full);
+          }
+        } else
         for (int it = 0; it < w.n_iter; ++it, ++gstep) {
           const int s = gstep % NS;
           const uint32_t par = gstep & 1;
@@ -410,7 +474,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
 #pragma unroll 1
           for (int kk = 0; kk < D / 16; ++kk)
             mma_ss(tmem + Cfg::kColS, kmajor_desc(kb, kk), kmajor_desc(qb, kk), id_s, kk > 0);
-          tc_commit(&sm.s_full);
+          tc_commit(&sm.s_full[0]);
           // dP^T = V_j dO_i^T, into the columns the previous step's dQ occupied
           if (gstep > 0) {
             ok = mbar_wait(&sm.dq_empty, (gstep - 1) & 1, p.status, abortf, kSiteDqEmpty);
@@ -466,7 +530,29 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     const uint32_t colS = tmem + lane_base + Cfg::kColS + g * kQ;
     const uint32_t colDP = tmem + lane_base + Cfg::kColDP + g * kQ;
     const uint32_t colDQ = tmem + lane_base + Cfg::kColDP + g * (D / kWG);
+    const uint32_t colS2 = tmem + lane_base + Cfg::kColS2 + g * kQ;
     const float c2 = p.scale_log2;
+    // Read dQ of global step gs (query tile qi) out of tensor memory and add
+    // it to the accumulator (BwdCfg::kDbl: done one step late, after the
+    // next step's P phase).
+    auto drain_dq = [&](int gs, int bh, int qi) -> bool {
+      bool okd = mbar_wait(&sm.dq_full, gs & 1, p.status, abortf, kSiteDqFull);
+      okd = __all_sync(0xffffffffu, okd);
+      if (!okd) return false;
+      tc_fence_after();
+      uint32_t a[16];
+      tmem_ld16(colDQ, a);
+      tmem_wait_ld16(a);
+      tc_fence_before();
+      mbar_arrive(&sm.dq_empty);
+      float* base = p.dq_acc + dqacc_index<D>(bh, p.n_kv, qi * kTile + r, g * (D / kWG) / 4);
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        atomicAdd(reinterpret_cast<float4*>(base + (size_t)e * kTile * 4),
+                  make_float4(__uint_as_float(a[4 * e]), __uint_as_float(a[4 * e + 1]),
+                              __uint_as_float(a[4 * e + 2]), __uint_as_float(a[4 * e + 3])));
+      return true;
+    };
     const float neutral = c2 < 0.f ? __int_as_float(0x7f800000) : __int_as_float(0xff800000);
     int gstep = 0;
     bool ok = true;
@@ -481,13 +567,17 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       const int j = w.j, bh = w.bh;
       const int kv_row = j * kTile + r;
       int cur = w.i0;
+      int i_prev = 0;
       for (int it = 0; it < w.n_iter; ++it, ++gstep) {
         const int s = gstep % NS;
         const uint32_t par = gstep & 1;
         const int i = next_i(cur, j);
         cur = i + 1;
+        const uint32_t cS = (Cfg::kDbl && par) ? colS2 : colS;
         ok = mbar_wait(&sm.q_full[s], (gstep / NS) & 1, p.status, abortf, kSiteQFull);
-        if (ok) ok = mbar_wait(&sm.s_full, par, p.status, abortf, kSiteSFull);
+        if (ok)
+          ok = mbar_wait(&sm.s_full[Cfg::kDbl ? par : 0], Cfg::kDbl ? (gstep >> 1) & 1 : par,
+                         p.status, abortf, kSiteSFull);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         tc_fence_after();
@@ -495,7 +585,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         {
           uint32_t (&h)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[0]);
           static_assert(kQ == 32, "the compute code is written for 32 query columns per warpgroup");
-          tmem_ld32(colS, h);
+          tmem_ld32(cS, h);
           tmem_wait_ld(h);
         }
         if (p.causal && i == j) {
@@ -514,10 +604,14 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
                     x0, x1);
           pk[e / 2] = pack_bf16x2(ex2_approx(x0), ex2_approx(x1));
         }
-        tmem_st16(colS, pk);
+        tmem_st16(cS, pk);
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(&sm.p_ready);
+        if constexpr (Cfg::kDbl) {
+          if (it > 0 && !(ok = drain_dq(gstep - 1, bh, i_prev))) break;
+          i_prev = i;
+        }
 
         ok = mbar_wait(&sm.dp_full, par, p.status, abortf, kSiteDpFull);
         ok = __all_sync(0xffffffffu, ok);
@@ -551,11 +645,12 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
           *reinterpret_cast<uint4*>(ds_row + (((ch0 + ch) ^ (r & 7)) << 4)) =
               make_uint4(dsw[ch * 4], dsw[ch * 4 + 1], dsw[ch * 4 + 2], dsw[ch * 4 + 3]);
         }
-        tmem_st16(colS + kQ / 2, dsw);
+        tmem_st16(cS + kQ / 2, dsw);
         tmem_wait_st();
         fence_proxy_async_smem();
         tc_fence_before();
         mbar_arrive(&sm.ds_ready);
+        if constexpr (Cfg::kDbl) continue;
 
         ok = mbar_wait(&sm.dq_full, par, p.status, abortf, kSiteDqFull);
         ok = __all_sync(0xffffffffu, ok);
@@ -583,6 +678,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         }
       }
       if (!ok) break;
+      if constexpr (Cfg::kDbl) {
+        if (w.n_iter > 0 && !(ok = drain_dq(gstep - 1, bh, i_prev))) break;
+      }
       // Epilogue: the first half of the warpgroups stores dV, the second half
       // scale * dK, each a D / (kWG / 2)-column slice.  The next item's first
       // dV and dK products overwrite these columns only after this warp's
