@@ -309,7 +309,11 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
   p.causal = causal;
   p.scale_log2 = scale * 1.4426950408889634f;
   // Block-sparse items differ in cost like causal ones: one CTA per item.
-  p.grid = fwd_grid(g.BH, g.n_pairs * g.splits, causal || block_mask != nullptr, ds->sm_count);
+  // Under the bottom-right causal mask, items cost the same when the query
+  // rows are few (decode, N_q <= 16: every row sees about all keys), and
+  // the persistent grid serves them.
+  const bool uneven = block_mask != nullptr || (causal && Nq > 16);
+  p.grid = fwd_grid(g.BH, g.n_pairs * g.splits, uneven, ds->sm_count);
   return launch_fwd(tq, tk, tv, to, p, d, static_cast<cudaStream_t>(stream));
 }
 
