@@ -24,7 +24,9 @@
  *
  * Pointers: every tensor pointer is a DEVICE pointer of the current CUDA
  * device, 16-byte aligned, owned by the caller; the library neither frees
- * nor retains them past the call's stream work.  Calls are asynchronous on
+ * nor retains them past the call's stream work.  Outputs must not overlap
+ * inputs (work items of one launch read inputs while others already write
+ * outputs).  Calls are asynchronous on
  * `stream` (a cudaStream_t, NULL = legacy default stream) and never
  * synchronise, except fa_device_status().
  *
