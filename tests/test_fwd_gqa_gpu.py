@@ -65,6 +65,11 @@ CASES = [
     (1, 2, 1, 300, 100, 64, True, 1),
     (1, 2, 1, 300, 100, 128, True, 2),
     (3, 6, 3, 129, 4096, 128, True, 7),
+    # more work items than SMs, so persistent CTAs take several each: decode
+    # and short causal queries (items of equal cost), a non-causal prefill
+    (8, 32, 8, 1, 4096, 128, True, 8),
+    (16, 16, 4, 8, 3000, 128, True, 4),
+    (8, 16, 4, 512, 512, 64, False, 1),
 ]
 
 
