@@ -822,45 +822,71 @@ __global__ void __launch_bounds__(FwdCfg<D, kFp8>::threads(kStage), 1)
 // lse = ln sum_s exp(lse_s) and O = sum_s exp(lse_s - lse) O_s (the split-KV
 // combine of cs2680 Lecture 9 sec. 9.8, the rescaling of sec. 9.4).  One
 // warp per row; lane l owns the d/32 consecutive columns starting at
-// l * d/32.
+// l * d/32.  The split lse values are read 32 at a time, one per lane, and
+// reduced across the warp; the split O rows are then read eight splits at a
+// time with all eight loads in flight, so a row costs a few memory
+// latencies rather than one per split.
 template <int D>
 __global__ void __launch_bounds__(256) fa_combine_kernel(const FwdParams p) {
   constexpr int kPer = D / 32;  // 4 or 2 columns per lane
+  constexpr int kBatch = 8;     // split O rows loaded together
   const long long row = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   const long long rows_total = (long long)p.BH * p.rows;
-  if (row >= rows_total) return;
+  if (row >= rows_total) return;  // whole warps: row is uniform in a warp
   const float ninf = __int_as_float(0xff800000);
   constexpr float kL2e = 1.4426950408889634f;
+  const int S = p.splits;
+  const float* lse_row_s = p.lse_part + row;  // split s at lse_row_s[s * rows_total]
   float m = ninf;
-  for (int s = 0; s < p.splits; ++s) m = fmaxf(m, p.lse_part[s * rows_total + row]);
+  for (int s = lane; s < S; s += 32) m = fmaxf(m, lse_row_s[s * rows_total]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
   float acc[kPer];
 #pragma unroll
   for (int i = 0; i < kPer; ++i) acc[i] = 0.f;
   float lse_row = ninf;
   if (m != ninf) {
     float sum = 0.f;
-    for (int s = 0; s < p.splits; ++s) sum += exp2f((p.lse_part[s * rows_total + row] - m) * kL2e);
+    for (int s = lane; s < S; s += 32) sum += exp2f((lse_row_s[s * rows_total] - m) * kL2e);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
     lse_row = m + logf(sum);
-    for (int s = 0; s < p.splits; ++s) {
-      const float w = exp2f((p.lse_part[s * rows_total + row] - lse_row) * kL2e);
-      if (w == 0.f) continue;
-      const float* src = p.o_part + (s * rows_total + row) * D + lane * kPer;
-      if (kPer == 4) {
-        const float4 v = *reinterpret_cast<const float4*>(src);
-        acc[0] += w * v.x;
-        acc[1] += w * v.y;
-        acc[kPer - 2] += w * v.z;
-        acc[kPer - 1] += w * v.w;
-      } else {
-        const float2 v = *reinterpret_cast<const float2*>(src);
-        acc[0] += w * v.x;
-        acc[1] += w * v.y;
+    for (int s0 = 0; s0 < S; s0 += 32) {
+      // Lane u's weight is split s0 + u's; a split with weight 0 adds nothing.
+      const float wl =
+          s0 + lane < S ? exp2f((lse_row_s[(s0 + lane) * rows_total] - lse_row) * kL2e) : 0.f;
+      const int n = min(32, S - s0);
+      for (int u0 = 0; u0 < n; u0 += kBatch) {
+        float v[kBatch][kPer];
+#pragma unroll
+        for (int b = 0; b < kBatch; ++b) {
+          const float* src = p.o_part + ((s0 + u0 + b) * rows_total + row) * D + lane * kPer;
+#pragma unroll
+          for (int i = 0; i < kPer; ++i) v[b][i] = 0.f;
+          if (u0 + b < n) {
+            if constexpr (kPer == 4) {
+              const float4 x = *reinterpret_cast<const float4*>(src);
+              v[b][0] = x.x, v[b][1] = x.y, v[b][kPer - 2] = x.z, v[b][kPer - 1] = x.w;
+            } else {
+              const float2 x = *reinterpret_cast<const float2*>(src);
+              v[b][0] = x.x, v[b][1] = x.y;
+            }
+          }
+        }
+#pragma unroll
+        for (int b = 0; b < kBatch; ++b) {
+          const float w = __shfl_sync(0xffffffffu, wl, (u0 + b) & 31);
+          if (u0 + b < n && w != 0.f) {
+#pragma unroll
+            for (int i = 0; i < kPer; ++i) acc[i] += w * v[b][i];
+          }
+        }
       }
     }
   }
   __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.o) + (size_t)row * D + lane * kPer;
-  if (kPer == 4) {
+  if constexpr (kPer == 4) {
     uint2 out;
     out.x = pack_bf16x2(acc[0], acc[1]);
     out.y = pack_bf16x2(acc[kPer - 2], acc[kPer - 1]);

@@ -70,6 +70,10 @@ CASES = [
     (8, 32, 8, 1, 4096, 128, True, 8),
     (16, 16, 4, 8, 3000, 128, True, 4),
     (8, 16, 4, 512, 512, 64, False, 1),
+    # more than 32 splits: the combine reads the split lse values 32 at a
+    # time and the split O rows eight at a time (ragged in both)
+    (2, 8, 2, 1, 4700, 128, True, 37),
+    (1, 4, 1, 2, 5000, 64, False, 64),
 ]
 
 
