@@ -48,7 +48,18 @@ struct FwdCfg {
   static constexpr int kTileBytes = kTile * D * (kFp8 ? 1 : 2);  // one 128 x d tile
   static constexpr int kStages = kFp8 ? 10 : ((D == 128) ? 5 : 8);  // K/V ring slots
   // 2 softmax warpgroups, producer, MMA (and the O store warp when staging).
-  static constexpr int threads(bool stage) { return stage ? 352 : 320; }
+  // Ten or eleven warps put three on some SM sub-partitions, which caps a
+  // thread at 168 registers.  At d = 64 (bf16) the kernel launches a twelfth
+  // warp instead, so that the producer / MMA / store warps form a full
+  // warpgroup that gives registers up (setmaxnreg) to the two softmax
+  // warpgroups; the split uses the launch's 384 x 168 registers exactly.
+  static constexpr bool kRealloc = D == 64 && !kFp8;
+  static constexpr int threads(bool stage) { return kRealloc ? 384 : (stage ? 352 : 320); }
+  static constexpr int kRegsLaunch = 168;
+  static constexpr int kRegsCtl = 72;
+  static constexpr int kRegsSoftmax = 216;
+  static_assert(!kRealloc || 2 * 128 * kRegsSoftmax + 128 * kRegsCtl <= 384 * kRegsLaunch,
+                "register split above the launch's total");
   static constexpr uint32_t kTmemCols = 512;
   // TMEM column of S/P and of O for Q tile t.
   static __device__ __forceinline__ uint32_t col_s(int t) { return (uint32_t)t * 128u; }
@@ -240,6 +251,7 @@ __global__ void __launch_bounds__(FwdCfg<D, kFp8>::threads(kStage), 1)
 
   if (warp == 8) {
     // ------------------------------------------------------------ producer
+    if constexpr (Cfg::kRealloc) setmaxnreg_dec<Cfg::kRegsCtl>();
     if (lane_id() == 0) {
       prefetch_tmap(&tq);
       prefetch_tmap(&tk);
@@ -340,6 +352,7 @@ __global__ void __launch_bounds__(FwdCfg<D, kFp8>::threads(kStage), 1)
     __syncwarp();
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
+    if constexpr (Cfg::kRealloc) setmaxnreg_dec<Cfg::kRegsCtl>();
     if (lane_id() == 0) {
       const uint32_t id_s = kFp8 ? idesc_e4m3(128, 128) : idesc_bf16(128, 128, false, false);
       const uint32_t id_pv = kFp8 ? idesc_e4m3(128, D) : idesc_bf16(128, D, false, true);
@@ -531,6 +544,7 @@ __global__ void __launch_bounds__(FwdCfg<D, kFp8>::threads(kStage), 1)
     __syncwarp();
   } else if (warp == 10) {
     // ------------------------------------------------------------ O store warp
+    if constexpr (Cfg::kRealloc) setmaxnreg_dec<Cfg::kRegsCtl>();
     // Sends each staged O tile out with TMA stores (rows past the tensor's
     // end are not written) and releases its ring slot once the stores have
     // read it.
@@ -563,8 +577,12 @@ __global__ void __launch_bounds__(FwdCfg<D, kFp8>::threads(kStage), 1)
       bulk_wait_group0();
     }
     __syncwarp();
+  } else if (Cfg::kRealloc && warp == 11) {
+    // Idle: its registers go to the softmax warpgroups.
+    if constexpr (Cfg::kRealloc) setmaxnreg_dec<Cfg::kRegsCtl>();
   } else if (warp < 8) {
     // ------------------------------------------------------------ softmax
+    if constexpr (Cfg::kRealloc) setmaxnreg_inc<Cfg::kRegsSoftmax>();
     const int t = warp >> 2;             // which Q tile
     const int r = tid & 127;             // row within the tile
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
@@ -905,6 +923,16 @@ int launch_fwd_dn(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMa
   if (cudaFuncSetAttribute(fa_fwd_kernel<D, kNeg, kGeneral, kSparse, kFp8, kStage>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return FA_ERR_LAUNCH;
+  if constexpr (FwdCfg<D, kFp8>::kRealloc) {
+    // The softmax warpgroups' setmaxnreg.inc waits for the registers the
+    // third warpgroup releases, which suffice only at the launch register
+    // count the split assumes: refuse to launch otherwise.
+    cudaFuncAttributes attr;
+    if (cudaFuncGetAttributes(&attr, fa_fwd_kernel<D, kNeg, kGeneral, kSparse, kFp8, kStage>) !=
+            cudaSuccess ||
+        attr.numRegs < FwdCfg<D, kFp8>::kRegsLaunch)
+      return FA_ERR_LAUNCH;
+  }
   fa_fwd_kernel<D, kNeg, kGeneral, kSparse, kFp8, kStage>
       <<<(unsigned)p.grid, FwdCfg<D, kFp8>::threads(kStage), smem, stream>>>(tq, tk, tv, to, p);
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_LAUNCH;
