@@ -33,7 +33,7 @@
 //                          workspace, by the compute warpgroups
 //   3. convert: dQ = bf16(scale * accumulator).
 //
-// Warp roles of the main kernel (576 threads):
+// Warp roles of the main kernel (640 threads):
 //   warps 0-15 compute: four warpgroups, warpgroup g owning query columns
 //              [32g, 32g+32) (thread r owns key row r of the tile): P, dS,
 //              then d/4 of dQ_i's columns from TMEM to the fp32 accumulator
@@ -41,7 +41,11 @@
 //              halves of dV, 2-3 halves of dK).  Four compute warps per SM
 //              sub-partition hide the latency of the exponent and dS phases
 //              better than two (measured +3% at d = 128, +7% at d = 64).
-//   warp 16    TMA producer;  warp 17 MMA issuer and TMEM owner
+//   warp 16    TMA producer;  warp 17 MMA issuer and TMEM owner;
+//   warps 18-19 idle: they complete the fifth warpgroup, which gives its
+//              registers to the compute warpgroups (setmaxnreg: five warps
+//              per SM sub-partition cap a thread at 96 registers at launch;
+//              the compute warps then run with 104, the others with 56).
 // Tensor memory: [0,128) S^T; warpgroup g's 32 columns [32g, 32g+32) take
 // P^T (bf16 pairs) over their first 16 and dS^T over the last 16, so that
 // dV += P^T dO and dK += dS^T Q take their A operand from tensor memory;
@@ -63,7 +67,13 @@ struct BwdCfg {
   static constexpr int kStages = 2;                  // Q/dO ring
   static constexpr int kWG = 4;                      // compute warpgroups
   static constexpr int kQ = kTile / kWG;             // query columns per warpgroup
-  static constexpr int kThreads = kWG * 128 + 64;    // compute, producer, MMA
+  static constexpr int kThreads = kWG * 128 + 128;   // compute, producer, MMA, 2 idle
+  // Registers per thread at launch, after the fifth warpgroup's setmaxnreg.dec
+  // and after the compute warpgroups' setmaxnreg.inc; the split must fit in
+  // the launch's registers, or the increase would wait forever.
+  static constexpr int kRegsLaunch = 96, kRegsCtl = 56, kRegsCompute = 104;
+  static_assert(kWG * 128 * kRegsCompute + 128 * kRegsCtl <= kThreads * kRegsLaunch,
+                "register split above the launch's total");
   static constexpr int kWarpLoad = kWG * 4, kWarpMma = kWG * 4 + 1;
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D;
@@ -327,6 +337,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
 
   if (warp == kWarpLoad) {
     // ------------------------------------------------------------ producer
+    setmaxnreg_dec<Cfg::kRegsCtl>();
     if (lane_id() == 0) {
       prefetch_tmap(&tq);
       prefetch_tmap(&tk);
@@ -391,6 +402,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     __syncwarp();
   } else if (warp == kWarpMma) {
     // ------------------------------------------------------------ MMA issuer
+    setmaxnreg_dec<Cfg::kRegsCtl>();
     if (lane_id() == 0) {
       const uint32_t id_s = idesc_bf16(128, 128, false, false);   // S^T, dP^T
       const uint32_t id_acc = idesc_bf16(128, D, false, true);    // dV, dK
@@ -520,8 +532,12 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       drain_wait(&sm.drain, 0);
     }
     __syncwarp();
+  } else if (warp >= kWG * 4 + 2) {
+    // Idle: its registers go to the compute warpgroups.
+    setmaxnreg_dec<Cfg::kRegsCtl>();
   } else if (warp < kWG * 4) {
     // ------------------------------------------------------------ compute
+    setmaxnreg_inc<Cfg::kRegsCompute>();
     // Warpgroup g handles query columns [kQ g, kQ g + kQ) of the tile;
     // thread r of every warpgroup owns key row r (TMEM lane r).
     const int g = warp >> 2;
@@ -750,6 +766,15 @@ int launch_bwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
         cudaSuccess)
       return FA_ERR_LAUNCH;
+    {
+      // The compute warpgroups' setmaxnreg.inc waits for the registers the
+      // fifth warpgroup releases, which suffice only at the launch register
+      // count the split assumes: refuse to launch otherwise.
+      cudaFuncAttributes attr;
+      if (cudaFuncGetAttributes(&attr, kern) != cudaSuccess ||
+          attr.numRegs < BwdCfg<D>::kRegsLaunch)
+        return FA_ERR_LAUNCH;
+    }
     // One persistent CTA per SM; each claims the next item of the list
     // from the workspace counter when it is ready for one (greedy list
     // scheduling, which under a causal or block mask is the LPT rule).
