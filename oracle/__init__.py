@@ -19,9 +19,12 @@ design notes):
     scale per head and tensor (amax / 448), codes rounded to nearest-even
     and saturated, the rounding decision taken in fp32, then exact
     attention over the dequantised tensors with scale / d.
-Parity of the backward pass against the pages themselves is unpinned: the
-pages print no worked gradient example.  It is pinned instead by finite
-differences of the forward pass and by an independent library routine.
+The pages print no worked gradient example, so the backward pass is pinned
+by the mathematics instead: central finite differences of the forward pass,
+closed forms (scale 0, causal row 0) and invariants (sums of dV and dK, the
+bilinear identity sum q . dQ = sum k . dK, the derivative in the scale, key
+shift and permutation), which on their own catch every planted backward
+mistake; and by an independent library routine (torch autograd).
 """
 from __future__ import annotations
 

@@ -3,9 +3,12 @@
 Each test checks the oracle against something the pages or the mathematics
 fix: the two-block rescaling identity of the CMU 11-868 FlashAttention post
 (slide page 12), the hand check l * e^m = sum e^x of cs2680 Lecture 9
-(sec. 9.4), closed forms (constant scores, causal row 0, two keys), invariants
-(row sums, permutation and shift invariance), central finite differences of
-the forward pass (for the backward pass), an independent library routine
+(sec. 9.4), closed forms (constant scores, causal row 0, two keys; for the backward
+pass: scale 0, causal row 0), invariants (row sums, permutation and shift
+invariance; for the backward pass: sums of dV and dK, the bilinear identity
+sum q . dQ = sum k . dK, the derivative in the scale), central finite
+differences of the forward pass (for the backward pass), an independent
+library routine
 (torch's fp64 scaled_dot_product_attention and autograd), and the FLOP counts
 the pages print.  All run on the CPU.
 """
@@ -268,6 +271,75 @@ def test_backward_of_dV_is_A_transpose_dO():
         A = oracle.attn_probs(q, k, causal=causal, scale=0.6)
         _, _, dv = oracle.attn_bwd(q, k, v, do, causal=causal, scale=0.6)
         assert np.abs(dv - np.swapaxes(A, -1, -2) @ do).max() < 1e-12
+
+
+# ------------------------------------- backward: closed forms, invariants
+#
+# With S = scale Q K^T (masked), P = softmax(S), O = P V and L = sum(dO * O):
+# dV = P^T dO, dS = P o (dO V^T - D) with D_i = dO_i . O_i, dQ = scale dS K,
+# dK = scale dS^T Q.  Each row of P sums to 1 and each row of dS sums to 0;
+# the facts below follow from those two and from S being bilinear in Q, K.
+
+def bwd_math_failures(lib=None):
+    """Names of the backward's mathematical pins that the oracle (or the
+    library ``lib``) fails; empty when it passes them all."""
+    failed = []
+    B, H, N, d = 1, 2, 9, 3
+    q, k, v, do = (rnd((B, H, N, d), s) for s in (40, 41, 42, 43))
+    scale = 0.8
+    for causal in (False, True):
+        tag = "_causal" if causal else ""
+        dq, dk, dv = oracle.attn_bwd(q, k, v, do, causal=causal, scale=scale, lib=lib)
+        # Rows of P sum to 1: sum_j dV_j = sum_i dO_i.
+        if np.abs(dv.sum(2) - do.sum(2)).max() > 1e-12:
+            failed.append("dv_sum" + tag)
+        # Rows of dS sum to 0: sum_j dK_j = scale sum_i (sum_j dS_ij) q_i = 0.
+        if np.abs(dk.sum(2)).max() > 1e-12:
+            failed.append("dk_sum" + tag)
+        # Bilinearity: sum_i q_i . dQ_i = sum_j k_j . dK_j (= sum_ij dS_ij S_ij).
+        lhs, rhs = (q * dq).sum((2, 3)), (k * dk).sum((2, 3))
+        if np.abs(lhs - rhs).max() > 1e-12:
+            failed.append("qdq_kdk" + tag)
+        # dL/dscale = sum_ij dS_ij S_ij / scale = sum_i q_i . dQ_i / scale,
+        # against central differences of the forward pass in the scale.
+        h = 1e-6
+        lp = (oracle.attn_fwd(q, k, v, causal=causal, scale=scale + h, lib=lib)[0] * do).sum()
+        lm = (oracle.attn_fwd(q, k, v, causal=causal, scale=scale - h, lib=lib)[0] * do).sum()
+        if abs((lp - lm) / (2 * h) - lhs.sum() / scale) > 1e-6:
+            failed.append("dscale" + tag)
+        # Adding one vector u to every key shifts row i's scores by
+        # scale q_i . u: P, O and every gradient stay the same.
+        u = rnd((1, 1, 1, d), 44, 3.0)
+        dq2, dk2, dv2 = oracle.attn_bwd(q, k + u, v, do, causal=causal, scale=scale, lib=lib)
+        if max(np.abs(a - b).max() for a, b in ((dq, dq2), (dk, dk2), (dv, dv2))) > 1e-11:
+            failed.append("key_shift" + tag)
+        # Scale 0: P is uniform over the visible keys, so dQ = dK = 0 and
+        # dV_j = sum over the rows i that see key j of dO_i / (keys row i sees).
+        dq0, dk0, dv0 = oracle.attn_bwd(q, k, v, do, causal=causal, scale=0.0, lib=lib)
+        counts = np.arange(1, N + 1) if causal else np.full(N, N)
+        w = do / counts[None, None, :, None]
+        want = np.cumsum(w[:, :, ::-1], axis=2)[:, :, ::-1] if causal else np.broadcast_to(
+            w.sum(2, keepdims=True), dv0.shape)
+        if np.abs(dv0 - want).max() > 1e-12 or np.abs(dq0).max() > 0 or np.abs(dk0).max() > 0:
+            failed.append("scale0" + tag)
+        if causal:
+            # Row 0 sees only key 0: P_00 = 1, O_0 = v_0, so dS_00 = 0, dQ_0 = 0.
+            if np.abs(dq[:, :, 0]).max() > 1e-13:
+                failed.append("causal_dq_row0")
+        else:
+            # Reordering the keys (K and V rows together) reorders dK and dV
+            # the same way and leaves dQ alone.
+            perm = np.random.default_rng(45).permutation(N)
+            dq3, dk3, dv3 = oracle.attn_bwd(q, k[:, :, perm], v[:, :, perm], do, causal=False,
+                                            scale=scale, lib=lib)
+            if (np.abs(dq3 - dq).max() > 1e-12 or np.abs(dk3 - dk[:, :, perm]).max() > 1e-12
+                    or np.abs(dv3 - dv[:, :, perm]).max() > 1e-12):
+                failed.append("key_permutation")
+    return failed
+
+
+def test_backward_closed_forms_and_invariants():
+    assert bwd_math_failures() == []
 
 
 # -------------------------------------------------------- FLOP counts
