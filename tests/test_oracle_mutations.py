@@ -214,14 +214,15 @@ def test_planted_mistake_is_caught(name, tmp_path):
 # invariants (no library routine among them) must catch each planted
 # backward mistake on their own.
 BWD_MUTATIONS = ["dS_wrong_sign", "dQ_drop_scale", "dK_drop_scale", "dK_transposed_operand",
-                 "dV_uses_dS", "D_drops_probability", "bwd_causal_start"]
+                 "dV_uses_dS", "D_drops_probability", "bwd_causal_start",
+                 "blockmask_dk_drops_scale"]
 
 
 @pytest.mark.parametrize("name", BWD_MUTATIONS)
 def test_backward_mistake_fails_a_mathematical_pin(name, tmp_path):
-    from test_oracle_pins import bwd_math_failures
+    from test_oracle_pins import blockmask_bwd_math_failures, bwd_math_failures
     before, after = MUTATIONS[name]
     text = open(SRC).read()
     lib = _build(text.replace(before, after, 1), tmp_path, name)
-    failed = bwd_math_failures(lib)
+    failed = bwd_math_failures(lib) + blockmask_bwd_math_failures(lib)
     assert failed, "mutation %s passed every mathematical backward pin" % name

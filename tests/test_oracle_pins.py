@@ -338,8 +338,40 @@ def bwd_math_failures(lib=None):
     return failed
 
 
+def blockmask_bwd_math_failures(lib=None):
+    """The same identities for the block-sparse backward pass: they hold
+    under any mask (a row's visible keys are its whole softmax); a query
+    row that sees no key has P = 0 and adds nothing to dV."""
+    failed = []
+    B, H, N, d, bs = 1, 2, 12, 3, 2
+    q, k, v, do = (rnd((B, H, N, d), s) for s in (50, 51, 52, 53))
+    scale = 0.7
+    bm = np.array([[1, 0, 1, 0, 0, 1], [0, 0, 0, 0, 0, 0], [1, 1, 0, 0, 1, 0],
+                   [0, 1, 1, 1, 0, 0], [0, 0, 0, 0, 1, 1], [1, 0, 0, 1, 0, 1]], np.uint8)
+    for causal in (False, True):
+        tag = "_causal" if causal else ""
+        dq, dk, dv = oracle.attn_bwd_blockmask(q, k, v, do, causal, scale, bm, bs, lib=lib)
+        _, lse = oracle.attn_fwd_blockmask(q, k, v, causal, scale, bm, bs, lib=lib)
+        sees = np.isfinite(lse)[..., None]
+        if np.abs(dv.sum(2) - (do * sees).sum(2)).max() > 1e-12:
+            failed.append("bs_dv_sum" + tag)
+        if np.abs(dk.sum(2)).max() > 1e-12:
+            failed.append("bs_dk_sum" + tag)
+        if np.abs((q * dq).sum((2, 3)) - (k * dk).sum((2, 3))).max() > 1e-12:
+            failed.append("bs_qdq_kdk" + tag)
+        u = rnd((1, 1, 1, d), 54, 3.0)
+        g2 = oracle.attn_bwd_blockmask(q, k + u, v, do, causal, scale, bm, bs, lib=lib)
+        if max(np.abs(a - b).max() for a, b in zip((dq, dk, dv), g2)) > 1e-11:
+            failed.append("bs_key_shift" + tag)
+    return failed
+
+
 def test_backward_closed_forms_and_invariants():
     assert bwd_math_failures() == []
+
+
+def test_blocksparse_backward_invariants():
+    assert blockmask_bwd_math_failures() == []
 
 
 # -------------------------------------------------------- FLOP counts
