@@ -51,7 +51,10 @@ extern "C" {
 #define FA_ERR_ALIGN (-3)          /* a tensor pointer is not 16-byte aligned */
 #define FA_ERR_WORKSPACE (-4)      /* workspace missing, misaligned or too small */
 #define FA_ERR_DEVICE (-5)         /* current device is not sm_103 / no tcgen05, or no device */
-#define FA_ERR_LAUNCH (-6)         /* a CUDA error was raised by a launch */
+#define FA_ERR_LAUNCH (-6)         /* a CUDA error was raised by a launch, or a
+                                      kernel was compiled with fewer registers
+                                      than its per-warpgroup register split
+                                      needs (nothing is launched then) */
 #define FA_ERR_TIMEOUT (-7)        /* a kernel's pipeline wait timed out (reported by fa_device_status) */
 
 /*
