@@ -51,6 +51,107 @@ FLUSH_NOTE = ("inputs smaller than L2 (each of Q, K, V, dO is %d MiB): L2 flushe
               "step's events")
 
 
+# Nominal dense tensor-core rate per SM and clock, and NVIDIA's published
+# dense per-GPU figures.  8192 bf16 FLOP/clk/SM is the rate at which ncu's
+# sm__pipe_tensor_cycles_active counts a tcgen05 kind::f16 product as busy
+# (the tensor-pipe percentage of every capture under profiles/ equals the
+# achieved FLOP/s over 8192 x 152 SMs x the capture's SM clock); with 152
+# SMs it gives NVIDIA's 2.25 PFLOP/s dense bf16 at 1.807 GHz.  E4M3
+# (kind::f8f6f4) runs at twice that rate (4.5 PFLOP/s published).
+NOMINAL_FLOP_PER_CLK_SM = {"bf16": 8192.0, "e4m3": 16384.0}
+DATASHEET_TFLOPS = {"bf16": 2250.0, "e4m3": 4500.0}
+
+
+def tensor_peaks(dev, sm_mhz, dtype="bf16"):
+    """The nominal tensor peak at the sampled SM clock and the datasheet
+    peak, in TFLOP/s, with how they were obtained."""
+    import torch
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    out = {"datasheet": DATASHEET_TFLOPS[dtype], "sm_count": sms}
+    if sm_mhz:
+        out["nominal_at_clock"] = NOMINAL_FLOP_PER_CLK_SM[dtype] * sms * sm_mhz * 1e6 / 1e12
+        out["clock_mhz"] = sm_mhz
+    return out
+
+
+def add_peak_fracs(roof, achieved, tp, dtype="bf16"):
+    """Beside a roofline's measured-peak fraction, the fractions of the
+    nominal peak at the sampled clock and of the datasheet peak."""
+    roof["peak_datasheet"] = tp["datasheet"]
+    roof["frac_datasheet"] = achieved / tp["datasheet"]
+    if "nominal_at_clock" in tp:
+        roof["peak_nominal_at_clock"] = tp["nominal_at_clock"]
+        roof["frac_nominal"] = achieved / tp["nominal_at_clock"]
+        roof["nominal_note"] = ("%d %s FLOP/clk/SM x %d SMs x %.0f MHz (median SM clock sampled "
+                                "in the timed region)" % (NOMINAL_FLOP_PER_CLK_SM[dtype], dtype,
+                                                          tp["sm_count"], tp["clock_mhz"]))
+    return roof
+
+
+def copy_rates(dev, nbytes=1 << 30, reps=3):
+    """Pinned host <-> device copy rates in GB/s (cudaMemcpyAsync through
+    torch): each direction alone, then both at once on two streams (as the
+    pipelined end-to-end run overlaps them).  Best of `reps`."""
+    import torch
+    h_src = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    h_dst = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    d_a = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    d_b = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    up, down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+
+    def timed(fn_list):
+        best = None
+        for _ in range(reps):
+            torch.cuda.synchronize(dev)
+            evs = []
+            for st, fn in fn_list:
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(st)
+                with torch.cuda.stream(st):
+                    fn()
+                e1.record(st)
+                evs.append((e0, e1))
+            torch.cuda.synchronize(dev)
+            t = [a.elapsed_time(b) / 1e3 for a, b in evs]
+            best = t if best is None else [min(x, y) for x, y in zip(best, t)]
+        return best
+
+    h2d = timed([(up, lambda: d_a.copy_(h_src, non_blocking=True))])[0]
+    d2h = timed([(down, lambda: h_dst.copy_(d_b, non_blocking=True))])[0]
+    both = timed([(up, lambda: d_a.copy_(h_src, non_blocking=True)),
+                  (down, lambda: h_dst.copy_(d_b, non_blocking=True))])
+    del h_src, h_dst, d_a, d_b
+    return {"h2d": nbytes / h2d / 1e9, "d2h": nbytes / d2h / 1e9,
+            "h2d_concurrent": nbytes / both[0] / 1e9, "d2h_concurrent": nbytes / both[1] / 1e9,
+            "bytes_per_copy": nbytes}
+
+
+def fp8_matmul_peak(dev, n=8192, reps=10):
+    """Burst E4M3 matmul rate (torch._scaled_mm, cuBLASLt) in TFLOP/s, best
+    of `reps`, or None where that call is unavailable."""
+    import torch
+    try:
+        a = torch.randn(n, n, device=dev).to(torch.float8_e4m3fn)
+        b = torch.randn(n, n, device=dev).to(torch.float8_e4m3fn).t()
+        one = torch.tensor(1.0, device=dev)
+        for _ in range(3):
+            torch._scaled_mm(a, b, scale_a=one, scale_b=one, out_dtype=torch.bfloat16)
+        best = None
+        for _ in range(reps):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record()
+            torch._scaled_mm(a, b, scale_a=one, scale_b=one, out_dtype=torch.bfloat16)
+            e1.record()
+            torch.cuda.synchronize(dev)
+            t = e0.elapsed_time(e1) / 1e3
+            best = t if best is None else min(best, t)
+        return 2.0 * n ** 3 / best / 1e12
+    except Exception:  # an older torch or cuBLASLt without E4M3 matmuls
+        return None
+
+
 def l2_flush_buffer(dev):
     import torch
     return torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
@@ -485,6 +586,20 @@ def run_gpu(args, w, rank, world, local_rank):
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
                "pipelined": "H2D of step k+1 and D2H of step k-1 overlap step k's kernels "
                             "(two device buffer sets, %d copy streams per direction)" % nc}
+        # The host link, measured on this machine in this run: a pipelined step
+        # can be no shorter than its kernels or than either direction's
+        # copies at the rate both directions reach together.
+        del sets
+        rates = copy_rates(dev)
+        kern_ms = elapsed / args.steps * 1e3
+        h2d_ms = h2d / (rates["h2d_concurrent"] * 1e9) * 1e3
+        d2h_ms = d2h / (rates["d2h_concurrent"] * 1e9) * 1e3
+        bound = max(kern_ms, h2d_ms, d2h_ms)
+        e2e_ms = e2e_sec / e2e_steps * 1e3
+        e2e.update({"ms_per_step": e2e_ms, "copy_gbs": rates,
+                    "bound_ms": bound,
+                    "bound_parts_ms": {"kernels": kern_ms, "h2d": h2d_ms, "d2h": d2h_ms},
+                    "frac_of_bound": bound / e2e_ms})
 
     # ------------------------------------------------------------ roofline
     peaks, peak_kind = load_peaks()
@@ -498,9 +613,14 @@ def run_gpu(args, w, rank, world, local_rank):
                 if peak_kind == "measured" else "fallback burst bf16",
                 "frac_of_sustained": achieved / float(peaks.get("bf16_tflops_sustained", peak)),
                 "traffic": profiled_traffic("fa_bwd_main_kernel_d%d_%s" % (d, w["name"]))}
+    tp = tensor_peaks(dev, clocks.get("sm_mhz") or clocks.get("sm_max_mhz"))
+    add_peak_fracs(roofline, achieved, tp)
     kernels = {nm: {"ms_per_launch": per_kernel[nm] / args.steps * 1e3} for nm in names}
     kernels["fwd"]["tflops"] = ff / fwd_avg / 1e12
     kernels["fwd"]["frac_of_peak"] = ff / fwd_avg / 1e12 / peak
+    if "nominal_at_clock" in tp:
+        kernels["fwd"]["frac_nominal"] = ff / fwd_avg / 1e12 / tp["nominal_at_clock"]
+    kernels["fwd"]["frac_datasheet"] = ff / fwd_avg / 1e12 / tp["datasheet"]
     kernels["bwd_main"]["tflops"] = achieved
     bwd_total = (per_kernel["bwd_prep"] + per_kernel["bwd_main"] + per_kernel["bwd_convert"]) / args.steps
     # The trade the backward pass makes (cs2680 Lecture 9 sec. 9.6): recompute
@@ -512,6 +632,8 @@ def run_gpu(args, w, rank, world, local_rank):
         "ms_at_hbm_peak": p_bytes / (float(load_peaks()[0]["hbm_gbs"]) * 1e9) * 1e3}
     kernels["bwd_total"] = {"ms_per_call": bwd_total * 1e3, "tflops": bf / bwd_total / 1e12,
                             "frac_of_peak": bf / bwd_total / 1e12 / peak}
+    if "nominal_at_clock" in tp:
+        kernels["bwd_total"]["frac_nominal"] = bf / bwd_total / 1e12 / tp["nominal_at_clock"]
     hbm_bytes = 8.0 * B * H * N * d + 4.0 * B * H * N  # fwd: Q, K, V read, O written, lse
     kernels["fwd"]["algorithmic_hbm_gbs"] = hbm_bytes / fwd_avg / 1e9
 
@@ -625,6 +747,8 @@ def run_gqa(args, wl, rank, world, local_rank):
                     "achieved": value / world, "peak": peak, "unit": "TFLOP/s",
                     "frac": value / world / peak, "peak_kind": "%s burst bf16" % peak_kind,
                     "traffic": profiled_traffic("fa_fwd_general_" + wl.name)}
+        add_peak_fracs(roofline, value / world,
+                       tensor_peaks(dev, clocks.get("sm_mhz") or clocks.get("sm_max_mhz")))
     if rank == 0:
         print(json.dumps({
             "metric": metric, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
@@ -740,11 +864,13 @@ def run_blocksparse(args, wl, rank, world, local_rank):
                        "step": "fa_fwd_blocksparse + fa_bwd_blocksparse",
                        "l2": "inputs larger than L2"},
             "clocks": clocks, "gpu_launches": args.steps * 4,
-            "roofline": {"bound": "tensor", "kernel": "fa_bwd_main_kernel (sparse)",
-                         "achieved": f_bwd / t_bwd / 1e12, "peak": peak, "unit": "TFLOP/s",
-                         "frac": f_bwd / t_bwd / 1e12 / peak,
-                         "peak_kind": "%s burst bf16" % peak_kind,
-                         "traffic": profiled_traffic("fa_bwd_main_kernel_sparse_" + wl.name)},
+            "roofline": add_peak_fracs(
+                {"bound": "tensor", "kernel": "fa_bwd_main_kernel (sparse)",
+                 "achieved": f_bwd / t_bwd / 1e12, "peak": peak, "unit": "TFLOP/s",
+                 "frac": f_bwd / t_bwd / 1e12 / peak, "peak_kind": "%s burst bf16" % peak_kind,
+                 "traffic": profiled_traffic("fa_bwd_main_kernel_sparse_" + wl.name)},
+                f_bwd / t_bwd / 1e12,
+                tensor_peaks(dev, clocks.get("sm_mhz") or clocks.get("sm_max_mhz"))),
             "fwd_tflops": f_fwd / t_fwd / 1e12, "bwd_tflops": f_bwd / t_bwd / 1e12,
             "fwd_ms": t_fwd * 1e3, "bwd_ms": t_bwd * 1e3}), flush=True)
     return 0
@@ -812,10 +938,17 @@ def run_fp8(args, w, rank, world, local_rank):
     per_step = sec / args.steps
     flops = fwd_flops(B, H, N, d, causal)
     value = world * flops / per_step / 1e12
-    peaks, peak_kind = load_peaks()
-    # FP8 dense tensor rate = 2x bf16 (nominal 4.5 vs 2.25 PFLOP/s) applied
-    # to the measured bf16 burst figure.
-    peak = 2.0 * float(peaks["bf16_tflops"])
+    # Denominators: a burst E4M3 matmul measured here (cuBLASLt through
+    # torch._scaled_mm), the nominal E4M3 rate at the sampled clock and the
+    # datasheet figure.
+    fp8_peak = fp8_matmul_peak(dev)
+    tp = tensor_peaks(dev, clocks.get("sm_mhz") or clocks.get("sm_max_mhz"), "e4m3")
+    if fp8_peak is not None:
+        peak, peak_kind = fp8_peak, "measured burst E4M3 matmul (torch._scaled_mm 8192^3, this run)"
+    else:
+        peak = tp.get("nominal_at_clock", tp["datasheet"])
+        peak_kind = ("nominal E4M3 at the sampled clock (no E4M3 matmul available to measure)"
+                     if "nominal_at_clock" in tp else "datasheet E4M3")
     t_q, t_a = statistics.median(q_ms) / 1e3, statistics.median(a_ms) / 1e3
     in_bytes = 3.0 * B * H * N * d * 2
     if rank == 0:
@@ -829,11 +962,12 @@ def run_fp8(args, w, rank, world, local_rank):
                        "step": "fa_fp8_quantize + fa_fwd_fp8_quantized",
                        "l2": "inputs larger than L2"},
             "clocks": clocks, "gpu_launches": args.steps * 3,
-            "roofline": {"bound": "tensor", "kernel": "fa_fwd_kernel (FP8)",
-                         "achieved": flops / t_a / 1e12, "peak": peak, "unit": "TFLOP/s",
-                         "frac": flops / t_a / 1e12 / peak,
-                         "peak_kind": "%s burst bf16 x 2 (nominal fp8/bf16 ratio)" % peak_kind,
-                         "traffic": profiled_traffic("fa_fwd_kernel_fp8_" + w["name"])},
+            "roofline": add_peak_fracs(
+                {"bound": "tensor", "kernel": "fa_fwd_kernel (FP8)",
+                 "achieved": flops / t_a / 1e12, "peak": peak, "unit": "TFLOP/s",
+                 "frac": flops / t_a / 1e12 / peak, "peak_kind": peak_kind,
+                 "traffic": profiled_traffic("fa_fwd_kernel_fp8_" + w["name"])},
+                flops / t_a / 1e12, tp, "e4m3"),
             "attention_ms": t_a * 1e3, "quantize_ms": t_q * 1e3,
             "quantize_gbs_inputs_read": in_bytes / t_q / 1e9}), flush=True)
     return 0

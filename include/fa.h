@@ -35,6 +35,12 @@
  * kernel whose internal pipeline wait exceeds its time limit stops early and
  * records FA_ERR_TIMEOUT in a per-device status word; fa_device_status()
  * reports it.
+ *
+ * Device state: the first call on a device caches, per device index, the
+ * device addresses of the library's static device data (the status word,
+ * the no-alloc scratch array) and the SM count.  Do not use the library on
+ * a device after cudaDeviceReset() in the same process: the cached
+ * addresses belong to the context that the reset destroyed.
  */
 #ifndef FA_H_
 #define FA_H_
@@ -234,7 +240,8 @@ int fa_fwd_fp8(const void* q, const void* k, const void* v, void* o, float* lse,
  * point takes it from a fixed scratch array in the library's static device
  * data instead and allocates nothing.
  *   Arguments, layouts and results as fa_bwd, without the workspace.
- *   Returns FA_ERR_WORKSPACE, launching nothing, when
+ *   Argument and alignment errors are checked first and returned as fa_bwd
+ *   returns them; otherwise FA_ERR_WORKSPACE, launching nothing, when
  *   fa_bwd_workspace_size(B, H, N, d) > FA_NOALLOC_SCRATCH_BYTES (for
  *   d = 128 about 64K padded rows B*H*ceil(N/128)*128; for d = 64 about 127K).
  *   The first call on a device looks up the scratch array's device address

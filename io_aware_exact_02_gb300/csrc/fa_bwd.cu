@@ -28,17 +28,19 @@
 //               (masked scores replaced by the value whose exponent is -inf)
 //        dV  += P^T dO_i                    (A operand from TMEM)
 //        dS^T = P^T o (dP^T - D_i)          -> bf16 in smem (128B swizzle)
-//        dK  += dS^T Q_i                   (A operand from TMEM)
 //        dQ_i = dS K_j  -> TMEM (over dP^T) -> fp32 vector atomics into the
-//                          workspace, by the compute warpgroups
+//                          workspace, by the compute warpgroups, spread
+//                          over the next step
+//        dK  += dS^T Q_i                   (A operand from TMEM)
 //   3. convert: dQ = bf16(scale * accumulator).
 //
 // Warp roles of the main kernel (640 threads):
 //   warps 0-15 compute: four warpgroups, warpgroup g owning query columns
 //              [32g, 32g+32) (thread r owns key row r of the tile): P, dS,
 //              then d/4 of dQ_i's columns from TMEM to the fp32 accumulator
-//              with atomic adds; finally the epilogue (warpgroups 0-1 store
-//              halves of dV, 2-3 halves of dK).  Four compute warps per SM
+//              with atomic adds (part of them held in registers until the
+//              next step's P and dS phases); finally the epilogue
+//              (warpgroups 0-1 store halves of dV, 2-3 halves of dK).  Four compute warps per SM
 //              sub-partition hide the latency of the exponent and dS phases
 //              better than two (measured +3% at d = 128, +7% at d = 64).
 //   warp 16    TMA producer;  warp 17 MMA issuer and TMEM owner;
@@ -133,17 +135,6 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
           smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
       : "memory");
-}
-
-// Adds 32 consecutive dQ columns of one row (8 groups of 4) to the
-// tile-blocked accumulator, whose groups are 128 * 4 floats apart.
-__device__ __forceinline__ void add_dq_chunk(float* base, const uint32_t (&a)[32]) {
-#pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    const float4 val = make_float4(__uint_as_float(a[4 * e]), __uint_as_float(a[4 * e + 1]),
-                                   __uint_as_float(a[4 * e + 2]), __uint_as_float(a[4 * e + 3]));
-    atomicAdd(reinterpret_cast<float4*>(base + (size_t)e * kTile * 4), val);
-  }
 }
 
 // Work order of the main kernel: heads in groups of kHeadGroup; inside a
@@ -506,20 +497,22 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
           for (int kk = 0; kk < kTile / 16; ++kk)
             mma_ts(tmem + Cfg::kColDV, tmem + Cfg::kColS + (kk * 16 / kQ) * kQ + (kk * 16 % kQ) / 2,
                    mnmajor_desc(dob, kk), id_acc, (it > 0 || kk > 0) ? 1u : 0u);
-          // dK += dS^T Q_i ; dQ_i = dS K_j
+          // dQ_i = dS K_j ; dK += dS^T Q_i.  dQ goes first: the compute
+          // warps then read it out and start its reductions while the tensor
+          // core runs dK and the next S^T.
           ok = mbar_wait(&sm.ds_ready, par, p.status, abortf, kSiteDsReady);
           if (!ok) break;
           tc_fence_after();
+#pragma unroll 1
+          for (int kk = 0; kk < kTile / 16; ++kk)
+            mma_ss(tmem + Cfg::kColDP, mnmajor_desc(dsb, kk), mnmajor_desc(kb, kk), id_dq, kk > 0);
+          tc_commit(&sm.dq_full);
 #pragma unroll 1
           for (int kk = 0; kk < kTile / 16; ++kk)
             mma_ts(tmem + Cfg::kColDK,
                    tmem + Cfg::kColS + kQ / 2 + (kk * 16 / kQ) * kQ + (kk * 16 % kQ) / 2,
                    mnmajor_desc(qb, kk), id_acc, (it > 0 || kk > 0) ? 1u : 0u);
           tc_commit(&sm.q_empty[s]);
-#pragma unroll 1
-          for (int kk = 0; kk < kTile / 16; ++kk)
-            mma_ss(tmem + Cfg::kColDP, mnmajor_desc(dsb, kk), mnmajor_desc(kb, kk), id_dq, kk > 0);
-          tc_commit(&sm.dq_full);
         }
         if (!ok) break;
         if (w.n_iter > 0) {
@@ -548,6 +541,44 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     const uint32_t colDQ = tmem + lane_base + Cfg::kColDP + g * (D / kWG);
     const uint32_t colS2 = tmem + lane_base + Cfg::kColS2 + g * kQ;
     const float c2 = p.scale_log2;
+    // dQ_i leaves the SM as float4 reductions into the accumulator, 64 KB
+    // per step at d = 128.  Issued all at once they queue on the SM's
+    // outbound write path and hold the compute warps back from the next
+    // step's P phase, while the path idles during the rest of the step.  So
+    // kNow of a thread's kGroups float4 groups go out as soon as dQ_i is read;
+    // the rest wait in registers and go out after the next step's P phase
+    // (kAfterP of them) and after its dS phase (the others), or at the end
+    // of the item.  Measured (main kernel, TFLOP/s): d = 128, N = 8K 1115
+    // with all at once, 1272 spread 4/2/2; d = 64 827 -> 887 spread 2/0/2.
+    constexpr int kGroups = D / kWG / 4;
+    constexpr int kNow = Cfg::kDbl ? 2 : 4;
+    constexpr int kAfterP = Cfg::kDbl ? 0 : 2;
+    constexpr int kHeld = kGroups - kNow;
+    uint32_t held[4 * kHeld];
+    float* held_base = nullptr;  // accumulator address of group kNow of the held row, or null
+    auto red4 = [&](float* base, int e, const uint32_t* v) {
+      atomicAdd(reinterpret_cast<float4*>(base + (size_t)e * kTile * 4),
+                make_float4(__uint_as_float(v[0]), __uint_as_float(v[1]), __uint_as_float(v[2]),
+                            __uint_as_float(v[3])));
+    };
+    // Row r's dQ values a[] for accumulator address `base` (group 0).
+    auto reduce_dq = [&](float* base, const uint32_t* a) {
+#pragma unroll
+      for (int e = 0; e < kNow; ++e) red4(base, e, a + 4 * e);
+#pragma unroll
+      for (int e = 0; e < 4 * kHeld; ++e) held[e] = a[4 * kNow + e];
+      held_base = base + (size_t)kNow * kTile * 4;
+    };
+    // Issue held groups [e0, e1) (compile-time bounds at every call site);
+    // e1 == kHeld ends the held row.
+    auto flush_held = [&](int e0, int e1) {
+      if (held_base != nullptr) {
+#pragma unroll
+        for (int e = 0; e < kHeld; ++e)
+          if (e >= e0 && e < e1) red4(held_base, e, held + 4 * e);
+        if (e1 == kHeld) held_base = nullptr;
+      }
+    };
     // Read dQ of global step gs (query tile qi) out of tensor memory and add
     // it to the accumulator (BwdCfg::kDbl: done one step late, after the
     // next step's P phase).
@@ -561,12 +592,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       tmem_wait_ld16(a);
       tc_fence_before();
       mbar_arrive(&sm.dq_empty);
-      float* base = p.dq_acc + dqacc_index<D>(bh, p.n_kv, qi * kTile + r, g * (D / kWG) / 4);
-#pragma unroll
-      for (int e = 0; e < 4; ++e)
-        atomicAdd(reinterpret_cast<float4*>(base + (size_t)e * kTile * 4),
-                  make_float4(__uint_as_float(a[4 * e]), __uint_as_float(a[4 * e + 1]),
-                              __uint_as_float(a[4 * e + 2]), __uint_as_float(a[4 * e + 3])));
+      reduce_dq(p.dq_acc + dqacc_index<D>(bh, p.n_kv, qi * kTile + r, g * (D / kWG) / 4), a);
       return true;
     };
     const float neutral = c2 < 0.f ? __int_as_float(0x7f800000) : __int_as_float(0xff800000);
@@ -624,6 +650,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(&sm.p_ready);
+        flush_held(0, kAfterP);
         if constexpr (Cfg::kDbl) {
           if (it > 0 && !(ok = drain_dq(gstep - 1, bh, i_prev))) break;
           i_prev = i;
@@ -666,37 +693,26 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         fence_proxy_async_smem();
         tc_fence_before();
         mbar_arrive(&sm.ds_ready);
+        flush_held(kAfterP, kHeld);
         if constexpr (Cfg::kDbl) continue;
 
         ok = mbar_wait(&sm.dq_full, par, p.status, abortf, kSiteDqFull);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         tc_fence_after();
-        if constexpr (D / kWG == 32) {
-          uint32_t a[32];
-          tmem_ld32(colDQ, a);
-          tmem_wait_ld(a);
-          tc_fence_before();
-          mbar_arrive(&sm.dq_empty);
-          add_dq_chunk(p.dq_acc + dqacc_index<D>(bh, p.n_kv, i * kTile + r, g * (D / kWG) / 4), a);
-        } else {
-          uint32_t a[16];
-          tmem_ld16(colDQ, a);
-          tmem_wait_ld16(a);
-          tc_fence_before();
-          mbar_arrive(&sm.dq_empty);
-          float* base = p.dq_acc + dqacc_index<D>(bh, p.n_kv, i * kTile + r, g * (D / kWG) / 4);
-  #pragma unroll
-          for (int e = 0; e < 4; ++e)
-            atomicAdd(reinterpret_cast<float4*>(base + (size_t)e * kTile * 4),
-                      make_float4(__uint_as_float(a[4 * e]), __uint_as_float(a[4 * e + 1]),
-                                  __uint_as_float(a[4 * e + 2]), __uint_as_float(a[4 * e + 3])));
-        }
+        static_assert(Cfg::kDbl || D / kWG == 32, "the single-region path is written for d = 128");
+        uint32_t a[32];
+        tmem_ld32(colDQ, a);
+        tmem_wait_ld(a);
+        tc_fence_before();
+        mbar_arrive(&sm.dq_empty);
+        reduce_dq(p.dq_acc + dqacc_index<D>(bh, p.n_kv, i * kTile + r, g * (D / kWG) / 4), a);
       }
       if (!ok) break;
       if constexpr (Cfg::kDbl) {
         if (w.n_iter > 0 && !(ok = drain_dq(gstep - 1, bh, i_prev))) break;
       }
+      flush_held(0, kHeld);  // the item's last dQ row
       // Epilogue: the first half of the warpgroups stores dV, the second half
       // scale * dK, each a D / (kWG / 2)-column slice.  The next item's first
       // dV and dK products overwrite these columns only after this warp's

@@ -66,12 +66,14 @@ extern "C" int fa_bwd_noalloc(const void* q, const void* k, const void* v, const
                               const void* dout, const float* lse, void* dq, void* dk, void* dv,
                               int B, int H, int N, int d, int causal, float scale, void* stream) {
   const size_t need = fa_bwd_workspace_size(B, H, N, d);
-  if (need == 0) {
-    // Invalid sizes: let fa_bwd report the precise argument error.
+  if (need == 0 || need > fa::kNoAllocScratchBytes) {
+    // Invalid sizes, or a workspace larger than the scratch array: fa_bwd
+    // without a workspace reports the same argument and alignment errors it
+    // would report with one, checked in the same order, and FA_ERR_WORKSPACE
+    // when the arguments are otherwise valid.  Nothing is launched.
     return fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, B, H, N, d, causal, scale, nullptr, 0,
                   stream);
   }
-  if (need > fa::kNoAllocScratchBytes) return FA_ERR_WORKSPACE;
   void* scratch = nullptr;
   const int rc = fa::scratch_address(&scratch);
   if (rc != FA_OK) return rc;

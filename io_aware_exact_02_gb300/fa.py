@@ -30,6 +30,9 @@ FA_ERR_DEVICE = -5
 FA_ERR_LAUNCH = -6
 FA_ERR_TIMEOUT = -7
 
+# Size of the static scratch array fa_bwd_noalloc uses (FA_NOALLOC_SCRATCH_BYTES).
+FA_NOALLOC_SCRATCH_BYTES = 32 << 20
+
 # Every symbol include/fa.h declares, with (restype, argtypes).
 _vp, _i, _f, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
 _ip = ctypes.POINTER(ctypes.c_int)
@@ -117,6 +120,19 @@ def _check_qkv(name, t, shape, dtype=torch.bfloat16):
         raise ValueError("%s must be contiguous" % name)
 
 
+def _on_device(ref, **tensors):
+    """Check that every given tensor is on ``ref``'s device and return a
+    context manager that makes that device current for the call: the library
+    looks up its per-device state (status word, SM count, tensor maps) on the
+    current device, and tensor maps built there must address that device's
+    memory."""
+    for name, t in tensors.items():
+        if t is not None and t.device != ref.device:
+            raise ValueError("%s is on %s, expected %s (one call's tensors must share a device)"
+                             % (name, t.device, ref.device))
+    return torch.cuda.device(ref.device)
+
+
 def default_scale(d: int) -> float:
     return 1.0 / math.sqrt(d)
 
@@ -133,8 +149,10 @@ def fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse
         lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
     _check_qkv("out", out, (B, H, N, d))
     _check_qkv("lse", lse, (B, H, N), torch.float32)
-    rc = load().fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
-                       B, H, N, d, int(bool(causal)), ctypes.c_float(scale), _stream_of(q))
+    with _on_device(q, k=k, v=v, out=out, lse=lse):
+        rc = load().fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                           lse.data_ptr(), B, H, N, d, int(bool(causal)), ctypes.c_float(scale),
+                           _stream_of(q))
     _check("fa_fwd", rc)
     return out, lse
 
@@ -177,9 +195,11 @@ def fwd_gqa(q, k, v, causal: bool = False, scale: float | None = None, num_split
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     ws_ptr = workspace.data_ptr() if workspace is not None else None
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
-    rc = load().fa_fwd_gqa(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
-                           lse.data_ptr(), B, Hq, Hkv, Nq, Nkv, d, int(bool(causal)),
-                           ctypes.c_float(scale), int(num_splits), ws_ptr, ws_bytes, _stream_of(q))
+    with _on_device(q, k=k, v=v, out=out, lse=lse, workspace=workspace):
+        rc = load().fa_fwd_gqa(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                               lse.data_ptr(), B, Hq, Hkv, Nq, Nkv, d, int(bool(causal)),
+                               ctypes.c_float(scale), int(num_splits), ws_ptr, ws_bytes,
+                               _stream_of(q))
     _check("fa_fwd_gqa", rc)
     return out, lse
 
@@ -212,10 +232,12 @@ def bwd(q, k, v, o, dout, lse, causal: bool = False, scale: float | None = None,
     args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(),
             lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, N, d,
             int(bool(causal)), ctypes.c_float(scale), workspace.data_ptr(), nbytes, _stream_of(q))
-    if phases == 7:
-        _check("fa_bwd", load().fa_bwd(*args))
-    else:
-        _check("fa_bwd_phases", load().fa_bwd_phases(*args, int(phases)))
+    with _on_device(q, k=k, v=v, o=o, dout=dout, lse=lse, dq=dq, dk=dk, dv=dv,
+                    workspace=workspace):
+        if phases == 7:
+            _check("fa_bwd", load().fa_bwd(*args))
+        else:
+            _check("fa_bwd_phases", load().fa_bwd_phases(*args, int(phases)))
     return dq, dk, dv
 
 
@@ -234,10 +256,11 @@ def bwd_noalloc(q, k, v, o, dout, lse, causal: bool = False, scale: float | None
     dv = torch.empty_like(q) if dv is None else dv
     for name, t in (("dq", dq), ("dk", dk), ("dv", dv)):
         _check_qkv(name, t, (B, H, N, d))
-    rc = load().fa_bwd_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
-                               dout.data_ptr(), lse.data_ptr(), dq.data_ptr(), dk.data_ptr(),
-                               dv.data_ptr(), B, H, N, d, int(bool(causal)),
-                               ctypes.c_float(scale), _stream_of(q))
+    with _on_device(q, k=k, v=v, o=o, dout=dout, lse=lse, dq=dq, dk=dk, dv=dv):
+        rc = load().fa_bwd_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                   dout.data_ptr(), lse.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                                   dv.data_ptr(), B, H, N, d, int(bool(causal)),
+                                   ctypes.c_float(scale), _stream_of(q))
     _check("fa_bwd_noalloc", rc)
     return dq, dk, dv
 
@@ -266,9 +289,11 @@ def fwd_blocksparse(q, k, v, block_mask, causal: bool = False, scale: float | No
         lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
     _check_qkv("out", out, (B, H, N, d))
     _check_qkv("lse", lse, (B, H, N), torch.float32)
-    rc = load().fa_fwd_blocksparse(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
-                                   lse.data_ptr(), B, H, N, d, int(bool(causal)),
-                                   ctypes.c_float(scale), block_mask.data_ptr(), _stream_of(q))
+    with _on_device(q, k=k, v=v, out=out, lse=lse):
+        rc = load().fa_fwd_blocksparse(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                       lse.data_ptr(), B, H, N, d, int(bool(causal)),
+                                       ctypes.c_float(scale), block_mask.data_ptr(),
+                                       _stream_of(q))
     _check("fa_fwd_blocksparse", rc)
     return out, lse
 
@@ -291,11 +316,14 @@ def bwd_blocksparse(q, k, v, o, dout, lse, block_mask, causal: bool = False,
         workspace = torch.empty(bwd_workspace_size(B, H, N, d), dtype=torch.uint8,
                                 device=q.device)
     nbytes = workspace.numel() * workspace.element_size()
-    rc = load().fa_bwd_blocksparse(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
-                                   dout.data_ptr(), lse.data_ptr(), dq.data_ptr(), dk.data_ptr(),
-                                   dv.data_ptr(), B, H, N, d, int(bool(causal)),
-                                   ctypes.c_float(scale), block_mask.data_ptr(),
-                                   workspace.data_ptr(), nbytes, _stream_of(q))
+    with _on_device(q, k=k, v=v, o=o, dout=dout, lse=lse, dq=dq, dk=dk, dv=dv,
+                    workspace=workspace):
+        rc = load().fa_bwd_blocksparse(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                       dout.data_ptr(), lse.data_ptr(), dq.data_ptr(),
+                                       dk.data_ptr(), dv.data_ptr(), B, H, N, d,
+                                       int(bool(causal)), ctypes.c_float(scale),
+                                       block_mask.data_ptr(), workspace.data_ptr(), nbytes,
+                                       _stream_of(q))
     _check("fa_bwd_blocksparse", rc)
     return dq, dk, dv
 
@@ -325,8 +353,10 @@ def fp8_quantize(q, k, v, hadamard: bool = True, workspace=None):
     for name, t in (("q", q), ("k", k), ("v", v)):
         _check_qkv(name, t, (B, H, N, d))
     workspace, nbytes = _fp8_workspace(workspace, B, H, N, d, q.device)
-    rc = load().fa_fp8_quantize(q.data_ptr(), k.data_ptr(), v.data_ptr(), B, H, N, d,
-                                int(bool(hadamard)), workspace.data_ptr(), nbytes, _stream_of(q))
+    with _on_device(q, k=k, v=v, workspace=workspace):
+        rc = load().fa_fp8_quantize(q.data_ptr(), k.data_ptr(), v.data_ptr(), B, H, N, d,
+                                    int(bool(hadamard)), workspace.data_ptr(), nbytes,
+                                    _stream_of(q))
     _check("fa_fp8_quantize", rc)
     return workspace
 
@@ -341,11 +371,12 @@ def fwd_fp8_quantized(workspace, B, H, N, d, causal: bool = False, scale: float 
         lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
     _check_qkv("out", out, (B, H, N, d))
     _check_qkv("lse", lse, (B, H, N), torch.float32)
-    rc = load().fa_fwd_fp8_quantized(out.data_ptr(), lse.data_ptr(), B, H, N, d,
-                                     int(bool(causal)), ctypes.c_float(scale),
-                                     int(bool(hadamard)), workspace.data_ptr(),
-                                     workspace.numel() * workspace.element_size(),
-                                     _stream_of(out))
+    with _on_device(workspace, out=out, lse=lse):
+        rc = load().fa_fwd_fp8_quantized(out.data_ptr(), lse.data_ptr(), B, H, N, d,
+                                         int(bool(causal)), ctypes.c_float(scale),
+                                         int(bool(hadamard)), workspace.data_ptr(),
+                                         workspace.numel() * workspace.element_size(),
+                                         _stream_of(out))
     _check("fa_fwd_fp8_quantized", rc)
     return out, lse
 
@@ -363,9 +394,11 @@ def fwd_fp8(q, k, v, causal: bool = False, scale: float | None = None, hadamard:
     _check_qkv("out", out, (B, H, N, d))
     _check_qkv("lse", lse, (B, H, N), torch.float32)
     workspace, nbytes = _fp8_workspace(workspace, B, H, N, d, q.device)
-    rc = load().fa_fwd_fp8(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
-                           lse.data_ptr(), B, H, N, d, int(bool(causal)), ctypes.c_float(scale),
-                           int(bool(hadamard)), workspace.data_ptr(), nbytes, _stream_of(q))
+    with _on_device(q, k=k, v=v, out=out, lse=lse, workspace=workspace):
+        rc = load().fa_fwd_fp8(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                               lse.data_ptr(), B, H, N, d, int(bool(causal)),
+                               ctypes.c_float(scale), int(bool(hadamard)), workspace.data_ptr(),
+                               nbytes, _stream_of(q))
     _check("fa_fwd_fp8", rc)
     return out, lse
 

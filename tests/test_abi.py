@@ -283,3 +283,21 @@ def test_selftest_timeout_arguments(lib):
     assert lib.fa_selftest_timeout(1000001, None) == fa.FA_ERR_ARG
     if not torch_cuda_available():
         assert lib.fa_selftest_timeout(1000, None) == fa.FA_ERR_DEVICE
+
+
+def test_noalloc_scratch_size_matches_the_header():
+    import re
+    text = open(os.path.join(ROOT, "include", "fa.h")).read()
+    m = re.search(r"#define FA_NOALLOC_SCRATCH_BYTES \(\(size_t\)(\d+) << (\d+)\)", text)
+    assert m, "FA_NOALLOC_SCRATCH_BYTES not found"
+    assert fa.FA_NOALLOC_SCRATCH_BYTES == int(m.group(1)) << int(m.group(2))
+
+
+def test_binding_rejects_tensors_on_another_device():
+    # One call's tensors must share a device: the library resolves its
+    # per-device state on the current device, which the binding sets to q's.
+    import torch
+    a = torch.empty(4, device="meta")
+    b = torch.empty(4)
+    with pytest.raises(ValueError, match="share a device"):
+        fa._on_device(b, k=a)

@@ -39,12 +39,31 @@ def test_bench_line_contract_small_square():
     assert rl["bound"] == "tensor" and rl["unit"] == "TFLOP/s" and rl["peak"] > 0
     assert rl["frac"] == pytest.approx(rl["achieved"] / rl["peak"], rel=1e-6)
     assert 0 < rl["frac"] < 1.3
+    # The same achieved rate against the nominal peak at the sampled clock
+    # and against the datasheet figure.
+    assert rl["peak_datasheet"] == 2250.0
+    assert rl["frac_datasheet"] == pytest.approx(rl["achieved"] / 2250.0, rel=1e-6)
+    clk_mhz = line["clocks"]["sm_mhz"] or line["clocks"]["sm_max_mhz"]
+    if clk_mhz:
+        assert rl["peak_nominal_at_clock"] == pytest.approx(8192 * 152 * clk_mhz * 1e6 / 1e12,
+                                                            rel=1e-6)
+        assert rl["frac_nominal"] == pytest.approx(rl["achieved"] / rl["peak_nominal_at_clock"],
+                                                   rel=1e-6)
 
     e2e = line["e2e"]
     elems = B * H * N * d
     assert e2e["h2d_bytes_per_step"] == 4 * elems * 2          # Q, K, V, dO (bf16)
     assert e2e["d2h_bytes_per_step"] == 4 * elems * 2 + B * H * N * 4  # O, dQ, dK, dV, lse
     assert 0 < e2e["value"] and e2e["unit"] == line["unit"]
+    # The host link measured in the same run, and the bound it sets.
+    cg = e2e["copy_gbs"]
+    for k in ("h2d", "d2h", "h2d_concurrent", "d2h_concurrent"):
+        assert cg[k] > 1.0, (k, cg)
+    parts = e2e["bound_parts_ms"]
+    assert e2e["bound_ms"] == pytest.approx(max(parts.values()), rel=1e-9)
+    assert parts["h2d"] == pytest.approx(
+        e2e["h2d_bytes_per_step"] / (cg["h2d_concurrent"] * 1e9) * 1e3, rel=1e-9)
+    assert e2e["frac_of_bound"] == pytest.approx(e2e["bound_ms"] / e2e["ms_per_step"], rel=1e-9)
 
     cb = line["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["value"] > 0 and cb["cores"] >= 1 and cb["sample"]

@@ -48,6 +48,46 @@ def test_noalloc_matches_fa_bwd_on_two_calls_in_a_row():
         assert torch.equal(got[1], ref[1]) and torch.equal(got[2], ref[2])
 
 
+def _largest_fitting_n(lib, d):
+    """The largest N (one head) whose workspace fits the scratch array."""
+    lim = fa.FA_NOALLOC_SCRATCH_BYTES
+    n = 128
+    while lib.fa_bwd_workspace_size(1, 1, n + 128, d) <= lim:
+        n += 128
+    assert lib.fa_bwd_workspace_size(1, 1, n, d) <= lim < lib.fa_bwd_workspace_size(1, 1, n + 1, d)
+    return n
+
+
+def test_noalloc_at_the_scratch_limit():
+    """A workspace just under the limit (its last padded rows at the end of
+    the array) matches fa_bwd; one row more is rejected."""
+    lib = fa.load()
+    d = 64
+    N = _largest_fitting_n(lib, d)
+    q, k, v, o, do, lse, causal, scale = _case(1, 1, N, d, False, 3)
+    ref = fa.bwd(q, k, v, o, do, lse, causal=causal, scale=scale)
+    got = fa.bwd_noalloc(q, k, v, o, do, lse, causal=causal, scale=scale)
+    fa.check_device_status()
+    den = ref[0].float().abs().max().item()
+    assert (got[0].float() - ref[0].float()).abs().max().item() <= G_REL * den
+    assert torch.equal(got[1], ref[1]) and torch.equal(got[2], ref[2])
+    del q, k, v, o, do, lse, ref, got
+    dev = torch.device("cuda")
+    buf = torch.zeros(16, dtype=torch.bfloat16, device=dev)  # never touched
+    p = buf.data_ptr()
+    rc = lib.fa_bwd_noalloc(p, p, p, p, p, p, p, p, p, 1, 1, N + 1, d, 0, ctypes.c_float(0.1),
+                            ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert rc == fa.FA_ERR_WORKSPACE
+    # Argument errors come first, as fa_bwd reports them.
+    rc = lib.fa_bwd_noalloc(p + 2, p, p, p, p, p, p, p, p, 1, 1, N + 1, d, 0, ctypes.c_float(0.1),
+                            ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert rc == fa.FA_ERR_ALIGN
+    rc = lib.fa_bwd_noalloc(p, p, p, p, p, p, p, p, p, 1, 1, N + 1, d, 2, ctypes.c_float(0.1),
+                            ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert rc == fa.FA_ERR_ARG
+    assert torch.count_nonzero(buf) == 0
+
+
 def test_noalloc_rejects_sizes_beyond_the_scratch():
     lib = fa.load()
     B, H, N, d = 1, 64, 8192, 128
