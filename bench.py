@@ -515,29 +515,35 @@ def run_gpu(args, w, rank, world, local_rank):
         hlse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
         hdq, hdk, hdv = (torch.empty(q.shape, dtype=q.dtype).pin_memory() for _ in range(3))
 
-        # Pipelined like a user streaming batches: two sets of device
-        # buffers; step k's inputs go up while the compute stream runs step
-        # k-1 and its results come back while it runs step k+1.  With
+        # Pipelined like a user streaming batches: `--e2e-sets` sets of
+        # device buffers (three by default); step k's inputs go up while the
+        # compute stream runs step k-1 and its results come back while it
+        # runs step k+1.  A set is reused every sets-th step, once its
+        # results have come back: with two sets the upload of step k waits
+        # for the download of step k-2, so the two directions take turns on
+        # the link; with three they overlap.  With
         # --e2e-copy-streams > 1 each copy direction is spread over that many
         # streams (tensors round-robin), so that several copy engines can move
         # the step's gigabyte.  Every step still copies its own inputs in and
         # all of its outputs out inside the timed region.
         sets = [(q, k, v, do, o, lse, dq, dk, dv, ws)]
-        sets.append(tuple(torch.empty_like(t) for t in sets[0]))
+        nsets = max(2, args.e2e_sets)
+        for _ in range(nsets - 1):
+            sets.append(tuple(torch.empty_like(t) for t in sets[0]))
         nc = max(1, args.e2e_copy_streams)
         ups = [torch.cuda.Stream(dev) for _ in range(nc)]
         downs = [torch.cuda.Stream(dev) for _ in range(nc)]
         comp = torch.cuda.Stream(dev)
 
         def e2e_run(n):
-            done_down = [[], []]  # set b's last D2H events (its buffers are free after them)
+            done_down = [[] for _ in range(nsets)]  # set b's last D2H events (then it is free)
             start = torch.cuda.Event(enable_timing=True)
             end = torch.cuda.Event(enable_timing=True)
             start.record(ups[0])
             for u in ups[1:]:
                 u.wait_event(start)
             for step in range(n):
-                b = step % 2
+                b = step % nsets
                 bq, bk, bv, bdo, bo, blse, bdq, bdk, bdv, bws = sets[b]
                 loaded = []
                 for i, (dst, src) in enumerate(((bq, hq), (bk, hk), (bv, hv), (bdo, hdo))):
@@ -567,7 +573,7 @@ def run_gpu(args, w, rank, world, local_rank):
                         ev = torch.cuda.Event()
                         ev.record(dn)
                     done_down[b].append(ev)
-            for ev in done_down[0] + done_down[1]:
+            for ev in sum(done_down, []):
                 downs[0].wait_event(ev)
             end.record(downs[0])
             return start, end
@@ -585,7 +591,8 @@ def run_gpu(args, w, rank, world, local_rank):
         e2e = {"value": aggregate((ff + bf) * e2e_steps, world, e2e_sec), "unit": UNIT,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
                "pipelined": "H2D of step k+1 and D2H of step k-1 overlap step k's kernels "
-                            "(two device buffer sets, %d copy streams per direction)" % nc}
+                            "(%d device buffer sets, %d copy streams per direction)"
+                            % (nsets, nc)}
         # The host link, measured on this machine in this run: a pipelined step
         # can be no shorter than its kernels or than either direction's
         # copies at the rate both directions reach together.
@@ -989,6 +996,8 @@ def main(argv=None):
     ap.add_argument("--ref-heads", type=int, default=1,
                     help="heads of the workload per step of the reference arm")
     ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--e2e-sets", type=int, default=3,
+                    help="device buffer sets the end-to-end pipeline rotates through (>= 2)")
     ap.add_argument("--e2e-copy-streams", type=int, default=1,
                     help="streams per copy direction in the end-to-end run")
     ap.add_argument("--no-e2e", action="store_true")
