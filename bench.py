@@ -535,7 +535,15 @@ def run_gpu(args, w, rank, world, local_rank):
         downs = [torch.cuda.Stream(dev) for _ in range(nc)]
         comp = torch.cuda.Stream(dev)
 
+        def timing_event(stream):
+            ev = torch.cuda.Event(enable_timing=True)
+            ev.record(stream)
+            return ev
+
+        stage_events = []  # per step: (h2d start, h2d end, compute start, end, d2h start, end)
+
         def e2e_run(n):
+            stage_events.clear()
             done_down = [[] for _ in range(nsets)]  # set b's last D2H events (then it is free)
             start = torch.cuda.Event(enable_timing=True)
             end = torch.cuda.Event(enable_timing=True)
@@ -546,33 +554,43 @@ def run_gpu(args, w, rank, world, local_rank):
                 b = step % nsets
                 bq, bk, bv, bdo, bo, blse, bdq, bdk, bdv, bws = sets[b]
                 loaded = []
+                stamps = []
                 for i, (dst, src) in enumerate(((bq, hq), (bk, hk), (bv, hv), (bdo, hdo))):
                     u = ups[i % nc]
                     for ev in done_down[b]:
                         u.wait_event(ev)
+                    if i == 0:
+                        stamps.append(timing_event(u))
                     with torch.cuda.stream(u):
                         dst.copy_(src, non_blocking=True)
-                        ev = torch.cuda.Event()
+                        ev = torch.cuda.Event(enable_timing=(i == 3))
                         ev.record(u)
                     loaded.append(ev)
+                stamps.append(loaded[-1])
                 for ev in loaded:
                     comp.wait_event(ev)
+                stamps.append(timing_event(comp))
                 with torch.cuda.stream(comp):
                     fa.fwd(bq, bk, bv, causal=causal, scale=scale, out=bo, lse=blse)
                     fa.bwd(bq, bk, bv, bo, bdo, blse, causal=causal, scale=scale, dq=bdq, dk=bdk,
                            dv=bdv, workspace=bws)
-                    computed = torch.cuda.Event()
+                    computed = torch.cuda.Event(enable_timing=True)
                     computed.record(comp)
+                stamps.append(computed)
                 done_down[b] = []
                 for j, (dst, src) in enumerate(((hdq, bdq), (hdk, bdk), (hdv, bdv), (ho, bo),
                                                 (hlse, blse))):
                     dn = downs[j % nc]
                     dn.wait_event(computed)
+                    if j == 0:
+                        stamps.append(timing_event(dn))
                     with torch.cuda.stream(dn):
                         dst.copy_(src, non_blocking=True)
-                        ev = torch.cuda.Event()
+                        ev = torch.cuda.Event(enable_timing=(j == 4))
                         ev.record(dn)
                     done_down[b].append(ev)
+                stamps.append(done_down[b][-1])
+                stage_events.append(stamps)
             for ev in sum(done_down, []):
                 downs[0].wait_event(ev)
             end.record(downs[0])
@@ -586,6 +604,14 @@ def run_gpu(args, w, rank, world, local_rank):
         barrier()
         fa.check_device_status(stream=comp.cuda_stream)
         e2e_sec = reduce_max(e0.elapsed_time(e1) / 1e3)
+        # Mean duration of each stage of a step (with one copy stream per
+        # direction the stage is contiguous on its stream): what the copies
+        # and the kernels took while running together.
+        stage_ms = None
+        if nc == 1:
+            stage_ms = {name: statistics.mean(st[2 * i].elapsed_time(st[2 * i + 1])
+                                              for st in stage_events)
+                        for i, name in enumerate(("h2d", "kernels", "d2h"))}
         h2d = 4 * in_bytes
         d2h = 4 * in_bytes + lse.numel() * 4
         e2e = {"value": aggregate((ff + bf) * e2e_steps, world, e2e_sec), "unit": UNIT,
@@ -603,7 +629,7 @@ def run_gpu(args, w, rank, world, local_rank):
         d2h_ms = d2h / (rates["d2h_concurrent"] * 1e9) * 1e3
         bound = max(kern_ms, h2d_ms, d2h_ms)
         e2e_ms = e2e_sec / e2e_steps * 1e3
-        e2e.update({"ms_per_step": e2e_ms, "copy_gbs": rates,
+        e2e.update({"ms_per_step": e2e_ms, "stage_ms_in_pipeline": stage_ms, "copy_gbs": rates,
                     "bound_ms": bound,
                     "bound_parts_ms": {"kernels": kern_ms, "h2d": h2d_ms, "d2h": d2h_ms},
                     "frac_of_bound": bound / e2e_ms})
@@ -1004,7 +1030,11 @@ def main(argv=None):
     ap.add_argument("--no-sweep", action="store_true",
                     help="skip the d=128 N sweep (1K, 2K, 4K, 16K) reported beside the headline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--fwd-pair", action="store_true",
+                    help="run the square d=128 forward on the CTA-pair kernel (FA_FWD_PAIR=1)")
     args = ap.parse_args(argv)
+    if args.fwd_pair:
+        os.environ["FA_FWD_PAIR"] = "1"  # read by the library on its first forward call
 
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))

@@ -62,6 +62,9 @@ extern "C" {
                                       than its per-warpgroup register split
                                       needs (nothing is launched then) */
 #define FA_ERR_TIMEOUT (-7)        /* a kernel's pipeline wait timed out (reported by fa_device_status) */
+#define FA_ERR_BOUNDS (-8)         /* bounds-checked build only: a kernel computed a tile, mask
+                                      or row index outside its array and stopped before using it
+                                      (reported by fa_device_status) */
 
 /*
  * Forward pass.
@@ -257,10 +260,14 @@ int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, c
 /*
  * Synchronises `stream`, then returns and clears the status word of the
  * current device: FA_OK, FA_ERR_TIMEOUT if a kernel gave up on a pipeline
- * wait since the last call, or FA_ERR_LAUNCH if the stream holds a CUDA
- * error.  If `site` is not NULL it receives the identifier of the first wait
- * that timed out (0 if none): 101-199 a wait of the forward kernel, 201-299
- * one of the backward main kernel, FA_SITE_SELFTEST the self test's.
+ * wait since the last call, FA_ERR_BOUNDS if a kernel of the bounds-checked
+ * build caught an out-of-range index, or FA_ERR_LAUNCH if the stream holds a
+ * CUDA error.  The first error recorded wins.  If `site` is not NULL it
+ * receives the identifier of the wait or check that raised it (0 if none):
+ * 101-199 a wait of the forward kernel, 201-299 one of the backward main
+ * kernel, 1101-1199 a bounds check of the forward kernels, 1201-1299 one of
+ * the backward kernels, FA_SITE_SELFTEST and FA_SITE_SELFTEST_BOUNDS the self
+ * tests'.
  */
 int fa_device_status(void* stream, int* site);
 
@@ -275,6 +282,25 @@ int fa_device_status(void* stream, int* site);
  */
 #define FA_SITE_SELFTEST 901
 int fa_selftest_timeout(int timeout_us, void* stream);
+
+/*
+ * Bounds-checked build (no counterpart on the pages).  Compiled with
+ * FA_CHECKS defined, every kernel range-checks the tile, mask and row indices
+ * it computes before it uses them; a violation records FA_ERR_BOUNDS and the
+ * check's site in the status word, and the CTA winds down through the same
+ * path as a timed-out wait (no trap, no access out of range).  The default
+ * build compiles the checks out.  fa_checks_enabled() returns 1 in the
+ * checked build and 0 otherwise.
+ *
+ * fa_selftest_bounds launches one thread that evaluates a bounds check on an
+ * index one past its range, touching no memory but the status word: in the
+ * checked build the status word then reads FA_ERR_BOUNDS at site
+ * FA_SITE_SELFTEST_BOUNDS; in the default build it stays FA_OK.  Returns as
+ * a launch.
+ */
+#define FA_SITE_SELFTEST_BOUNDS 902
+int fa_checks_enabled(void);
+int fa_selftest_bounds(void* stream);
 
 /* A static, human-readable description of a status code. */
 const char* fa_status_string(int status);

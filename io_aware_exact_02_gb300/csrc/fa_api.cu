@@ -7,6 +7,7 @@
 #include <cmath>
 #include <cstddef>
 #include <cstdint>
+#include <cstdlib>
 #include <mutex>
 
 #include "fa_internal.h"
@@ -27,6 +28,7 @@ struct DeviceState {
   bool supported = false;
   int* status = nullptr;  // device address of g_status
   int sm_count = 0;
+  int pair_max = 0;       // forward CTA pairs resident at once (0: not yet known)
 };
 
 std::mutex g_mu;
@@ -140,12 +142,16 @@ int gqa_shape(int B, int Hq, int Hkv, int Nq, int Nkv, int d, int num_splits, fl
 }  // namespace
 
 int make_tmap_bhnd(const void* base, int BH, int N, int d, CUtensorMap* out) {
+  return make_tmap_bhnd_rows(base, BH, N, d, kTile, out);
+}
+
+int make_tmap_bhnd_rows(const void* base, int BH, int N, int d, int box_rows, CUtensorMap* out) {
   PFN_cuTensorMapEncodeTiled_v12000 enc;
   int rc = get_encode(&enc);
   if (rc != FA_OK) return rc;
   cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
   cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)N * d * 2};
-  cuuint32_t box[3] = {64, kTile, 1};
+  cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
   cuuint32_t es[3] = {1, 1, 1};
   CUresult r = enc(out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
                    strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -170,6 +176,15 @@ __global__ void fa_selftest_timeout_kernel(int* status, unsigned long long limit
       return;
     }
   }
+}
+
+// The bounds-check self test: one thread checks an index one past its range
+// (n = 1, index 1) through the kernels' check; it touches no memory but the
+// status word, which the check writes only in the checked build.
+__global__ void fa_selftest_bounds_kernel(int* status, int n) {
+  int abort_flag = 0;
+  const int index = n;
+  if (!bound_ok(index < n, status, &abort_flag, FA_SITE_SELFTEST_BOUNDS)) return;
 }
 
 int make_tmap_u8(const void* base, int BH, int rows, int inner, CUtensorMap* out) {
@@ -314,6 +329,28 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
   // the persistent grid serves them.
   const bool uneven = block_mask != nullptr || (causal && Nq > 16);
   p.grid = fwd_grid(g.BH, g.n_pairs * g.splits, uneven, ds->sm_count);
+  // Square, d = 128, no mask, and FA_FWD_PAIR=1 in the environment: the
+  // CTA-pair kernel (tcgen05 cta_group::2).  It is correct (bitwise equal to
+  // the one-CTA kernel) but measured slower on this GPU -- with its products
+  // at full rate the per-tile softmax chain and the cross-SM hops of P-ready
+  // and S-done bound it -- so the one-CTA kernel is the default.
+  static const bool pair_requested = [] {
+    const char* e = std::getenv("FA_FWD_PAIR");
+    return e != nullptr && e[0] == '1' && e[1] == 0;
+  }();
+  if (pair_requested && d == 128 && !causal && block_mask == nullptr && g.splits == 1 &&
+      Hq == Hkv && Nq == Nkv) {
+    CUtensorMap tkh;
+    if ((rc = make_tmap_bhnd_rows(k, g.BH, Nkv, d, 64, &tkh)) != FA_OK) return rc;
+    if (p.scale_log2 == 0.f) p.scale_log2 = 1.17549435e-38f;  // as launch_fwd does
+    int pairs;
+    {
+      std::lock_guard<std::mutex> lk(g_mu);
+      if (ds->pair_max == 0) ds->pair_max = fwd_pair_max_active(ds->sm_count);
+      pairs = ds->pair_max;
+    }
+    return launch_fwd_pair(tq, tkh, tv, p, static_cast<cudaStream_t>(stream), pairs);
+  }
   return launch_fwd(tq, tk, tv, to, p, d, static_cast<cudaStream_t>(stream));
 }
 
@@ -385,6 +422,7 @@ const char* fa_status_string(int status) {
     case FA_ERR_DEVICE: return "no usable device (needs sm_103 with tcgen05)";
     case FA_ERR_LAUNCH: return "CUDA launch error";
     case FA_ERR_TIMEOUT: return "a kernel pipeline wait timed out";
+    case FA_ERR_BOUNDS: return "a kernel computed an out-of-range index (bounds-checked build)";
     default: return "unknown status";
   }
 }
@@ -538,6 +576,16 @@ int fa_selftest_timeout(int timeout_us, void* stream) {
   if (rc != FA_OK) return rc;
   fa_selftest_timeout_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
       ds->status, (unsigned long long)timeout_us * 1000ull);
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+}
+
+int fa_checks_enabled(void) { return kChecks ? 1 : 0; }
+
+int fa_selftest_bounds(void* stream) {
+  DeviceState* ds;
+  int rc = device_state(&ds);
+  if (rc != FA_OK) return rc;
+  fa_selftest_bounds_kernel<<<1, 1, 0, static_cast<cudaStream_t>(stream)>>>(ds->status, 1);
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 

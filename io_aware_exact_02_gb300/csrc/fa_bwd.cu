@@ -111,6 +111,16 @@ enum : int {
   kSiteDsReady, kSiteDqFull, kSiteDqEmpty, kSiteAccFull, kSiteAlign, kSiteKvEmpty,
   kSiteItemFull, kSiteItemEmpty
 };
+// Bounds checks of the checked build (FA_CHECKS).
+enum : int {
+  kChkItem = 1201,  // a work item's head, key tile or step count
+  kChkQTile,        // a query tile a key tile visits
+  kChkDqRow,        // a row of the dQ accumulator
+  kChkKvRow,        // a key row of dK / dV
+  kChkPrepRow,      // a row of the prep kernel
+  kChkConvRow,      // a row of the convert kernel
+  kChkMask          // an entry of the block mask
+};
 
 __device__ __forceinline__ uint64_t kmajor_desc(uint32_t base, int kk) {
   return sdesc_sw128(base + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
@@ -173,10 +183,14 @@ __global__ void __launch_bounds__(256) fa_bwd_prep_kernel(const BwdParams p) {
   const int sub = lane % kLanesPerRow;
   float acc = 0.f;
   int bh = 0, row = 0;
-  const bool in_range = row_g < total_rows;
+  bool in_range = row_g < total_rows;
   if (in_range) {
     bh = (int)(row_g / npad);
     row = (int)(row_g % npad);
+    int no_abort = 0;
+    in_range = bound_ok(bh < p.BH && row < npad, p.status, &no_abort, kChkPrepRow);
+  }
+  if (in_range) {
     if (row < p.N) {
       const size_t off = ((size_t)bh * p.N + row) * D + sub * 8;
       const uint4 a = *reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(p.o) + off);
@@ -218,6 +232,8 @@ __global__ void __launch_bounds__(256) fa_bwd_convert_kernel(const BwdParams p) 
   const int c8 = (int)(idx % (D / 8));
   const long long rg = idx / (D / 8);
   const int bh = (int)(rg / p.N), row = (int)(rg % p.N);
+  int no_abort = 0;
+  if (!bound_ok(bh < p.BH && row < p.N, p.status, &no_abort, kChkConvRow)) return;
   const float4 a = *reinterpret_cast<const float4*>(p.dq_acc + dqacc_index<D>(bh, p.n_kv, row, 2 * c8));
   const float4 b = *reinterpret_cast<const float4*>(p.dq_acc + dqacc_index<D>(bh, p.n_kv, row, 2 * c8 + 1));
   uint4 out;
@@ -308,9 +324,17 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     w.n_iter = p.n_kv - w.i0;
     if (kSparse) {
       w.n_iter = 0;
-      for (int i = w.i0; i < p.n_kv; ++i) w.n_iter += p.block_mask[(size_t)i * p.n_kv + w.j] != 0;
+      if (bound_ok(w.j < p.n_kv, p.status, abortf, kChkMask))
+        for (int i = w.i0; i < p.n_kv; ++i) w.n_iter += p.block_mask[(size_t)i * p.n_kv + w.j] != 0;
     }
     return w;
+  };
+  // Checked build: the item's head and key tile exist and it has at most
+  // n_kv steps starting at a query tile that exists.
+  auto item_ok = [&](const ItemInfo& w) -> bool {
+    return bound_ok(w.bh >= 0 && w.bh < p.BH && w.j >= 0 && w.j < p.n_kv && w.i0 >= 0 &&
+                        w.n_iter >= 0 && w.n_iter <= p.n_kv - w.i0,
+                    p.status, abortf, kChkItem);
   };
   // The next query tile at or after c that key tile j visits (callers ask
   // only for tiles that exist; the scan stops at the last tile anyway).
@@ -348,6 +372,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         mbar_arrive(&sm.item_full[slot]);
         if (t >= total) break;
         const ItemInfo w = item_info(t);
+        if (!item_ok(w)) {
+          ok = false;
+          break;
+        }
         int cur = w.i0;
         for (int it = 0; it < w.n_iter; ++it) {
           const int s = gstep % NS, use = gstep / NS;
@@ -357,6 +385,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
           }
           const int i = next_i(cur, w.j);
           cur = i + 1;
+          if (!bound_ok(i < p.n_kv, p.status, abortf, kChkQTile)) {
+            ok = false;
+            break;
+          }
           mbar_arrive_expect_tx(&sm.q_full[s], 2 * Cfg::kTileBytes + 2 * kTile * 4);
           for (int h = 0; h < D / 64; ++h) {
             tma_load_3d(sm.q[s] + h * 16384, &tq, &sm.q_full[s], h * 64, i * kTile, w.bh);
@@ -407,6 +439,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         mbar_arrive(&sm.item_empty[m & 1]);
         if (t >= total) break;
         const ItemInfo w = item_info(t);
+        if (!item_ok(w)) {
+          ok = false;
+          break;
+        }
         if (w.n_iter > 0) {
           ok = mbar_wait(&sm.kv_full, kvc & 1, p.status, abortf, kSiteKvFull);
           if (!ok) break;
@@ -606,6 +642,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       if (lane_id() == 0) mbar_arrive(&sm.item_empty[m & 1]);
       if (t >= total) break;
       const ItemInfo w = item_info(t);
+      if (!warp_bound_ok(item_ok(w), p.status, abortf, kChkItem)) {
+        ok = false;
+        break;
+      }
       const int j = w.j, bh = w.bh;
       const int kv_row = j * kTile + r;
       int cur = w.i0;
@@ -615,6 +655,11 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         const uint32_t par = gstep & 1;
         const int i = next_i(cur, j);
         cur = i + 1;
+        // The query tile, hence the dQ accumulator rows it adds to.
+        if (!warp_bound_ok(i < p.n_kv && i * kTile + r < npad, p.status, abortf, kChkDqRow)) {
+          ok = false;
+          break;
+        }
         const uint32_t cS = (Cfg::kDbl && par) ? colS2 : colS;
         ok = mbar_wait(&sm.q_full[s], (gstep / NS) & 1, p.status, abortf, kSiteQFull);
         if (ok)
@@ -720,6 +765,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       // loads below.
       ok = mbar_wait(&sm.acc_full, m & 1, p.status, abortf, kSiteAccFull);
       ok = __all_sync(0xffffffffu, ok);
+      if (ok) ok = warp_bound_ok(kv_row < npad, p.status, abortf, kChkKvRow);
       if (!ok) break;
       tc_fence_after();
       constexpr int kCols = D / (kWG / 2);

@@ -35,12 +35,12 @@
 // exponentials stay below 2^kRescaleSlack.  O and l always share the same
 // reference, so O / l and lse = (m + log2 l) * ln 2 are exact.
 #include "fa_internal.h"
+#include "fa_softmax.cuh"
 #include "sm100_ptx.cuh"
 
 namespace fa {
 namespace {
 
-constexpr float kRescaleSlack = 8.0f;  // log2 units
 constexpr float kLn2 = 0.69314718055994530942f;
 
 template <int D, bool kFp8 = false>
@@ -96,6 +96,14 @@ struct alignas(1024) FwdSmem {
 enum : int {
   kSiteQFull = 101, kSiteKvEmpty, kSiteKvFull, kSitePFull, kSiteSFull, kSiteOFull, kSiteDrain,
   kSiteQEmpty, kSiteOEmpty, kSiteStageSlot, kSiteStaged, kSiteStored
+};
+// Bounds checks of the checked build (FA_CHECKS).
+enum : int {
+  kChkItem = 1101,  // a work item's head, pair, split or key-tile range
+  kChkKvTile,       // a key tile loaded or scored
+  kChkMask,         // an entry of the block mask
+  kChkRow,          // an output row (O, lse, or a split's O and lse)
+  kChkCombine       // a row or split of the combine kernel
 };
 
 // Descriptor of the K-major, 128B-swizzled tile at `base` for MMA K-step kk:
@@ -204,7 +212,10 @@ __global__ void __launch_bounds__(FwdCfg<D, kFp8>::threads(kStage), 1)
   };
   // Block-sparse: is key tile jj active for query tile t of the item?
   auto active = [&](const Item& it, int t, int jj) -> bool {
-    return jj < it.hi[t] && p.block_mask[(size_t)(it.row0 / kTile + t) * p.n_kv + jj] != 0;
+    if (jj >= it.hi[t]) return false;
+    const int qt = it.row0 / kTile + t;
+    if (!bound_ok(qt < p.n_kv && jj >= 0 && jj < p.n_kv, p.status, abortf, kChkMask)) return false;
+    return p.block_mask[(size_t)qt * p.n_kv + jj] != 0;
   };
   // The next key tile at or after c that query tile t uses; callers ask only
   // for tiles that exist, and the scan stops at the tile's last visible key
@@ -248,6 +259,14 @@ __global__ void __launch_bounds__(FwdCfg<D, kFp8>::threads(kStage), 1)
     }
     return it;
   };
+  // Checked build: the item's head, pair and split exist and its key tiles
+  // [j0, j0 + n_t) lie inside the head's.
+  auto item_ok = [&](const Item& it) -> bool {
+    bool in = it.bh >= 0 && it.bh < p.BH && it.pair >= 0 && it.pair < p.n_pairs &&
+              it.split >= 0 && it.split < splits && it.j0 >= 0;
+    for (int t = 0; t < 2; ++t) in = in && it.n_t[t] >= 0 && it.j0 + it.n_t[t] <= p.n_kv;
+    return bound_ok(in, p.status, abortf, kChkItem);
+  };
 
   if (warp == 8) {
     // ------------------------------------------------------------ producer
@@ -264,6 +283,10 @@ __global__ void __launch_bounds__(FwdCfg<D, kFp8>::threads(kStage), 1)
         const int idx = item_of_round(k);
         if (idx >= num_items) continue;
         const Item it = decode(idx);
+        if (!item_ok(it)) {
+          ok = false;
+          break;
+        }
         if (it.nmax == 0) continue;  // no key visible to any row of the item
         if (q_issued > 0 &&
             !mbar_wait(&sm.q_empty, (q_issued - 1) & 1, p.status, abortf, kSiteQEmpty)) {
@@ -278,6 +301,7 @@ __global__ void __launch_bounds__(FwdCfg<D, kFp8>::threads(kStage), 1)
         if constexpr (kSparse) {
           // K (w = 0) or V (w = 1) of key tile jj into the next ring slot.
           auto load_kv = [&](int w, int jj) -> bool {
+            if (!bound_ok(jj >= 0 && jj < p.n_kv, p.status, abortf, kChkKvTile)) return false;
             const int slot = c % S, use = c / S;
             if (use > 0 &&
                 !mbar_wait(&sm.kv_empty[slot], (use - 1) & 1, p.status, abortf, kSiteKvEmpty))
@@ -305,6 +329,10 @@ __global__ void __launch_bounds__(FwdCfg<D, kFp8>::threads(kStage), 1)
         } else {
           for (int j = 0; j < it.nmax && ok; ++j) {
             const int jj = it.j0 + j;
+            if (!bound_ok(jj < p.n_kv, p.status, abortf, kChkKvTile)) {
+              ok = false;
+              break;
+            }
             for (int w = 0; w < 2 && ok; ++w, ++c) {
               const int slot = c % S, use = c / S;
               if (use > 0 &&
@@ -410,6 +438,10 @@ __global__ void __launch_bounds__(FwdCfg<D, kFp8>::threads(kStage), 1)
         const int idx = item_of_round(k);
         if (idx >= num_items) continue;
         const Item it = decode(idx);
+        if (!item_ok(it)) {
+          ok = false;
+          break;
+        }
         const int nmax = it.nmax;
         if constexpr (!kSparse) {
           // A Q tile without keys is final at once (its rows get O = 0).
@@ -555,6 +587,10 @@ __global__ void __launch_bounds__(FwdCfg<D, kFp8>::threads(kStage), 1)
         const int idx = item_of_round(k);
         if (idx >= num_items) continue;
         const Item it = decode(idx);
+        if (!item_ok(it)) {
+          ok = false;
+          break;
+        }
         if (it.nmax == 0) continue;
         for (int t = 0; t < 2 && ok; ++t) {
           const int use = cb + 2 * it.nmax + t;
@@ -587,9 +623,6 @@ __global__ void __launch_bounds__(FwdCfg<D, kFp8>::threads(kStage), 1)
     const int r = tid & 127;             // row within the tile
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     float c2 = p.scale_log2;  // nonzero: a zero scale arrives as a tiny positive one
-    // A masked score is replaced by the value that loses every max (min)
-    // and whose exponent c2 * s is -inf, so its probability is exactly 0.
-    const float neutral = kNeg ? __int_as_float(0x7f800000) : __int_as_float(0xff800000);
     const float ninf = __int_as_float(0xff800000);
     const uint32_t colS = tmem + lane_base + Cfg::col_s(t);
     const uint32_t colO = tmem + lane_base + Cfg::col_o(t);
@@ -603,6 +636,10 @@ __global__ void __launch_bounds__(FwdCfg<D, kFp8>::threads(kStage), 1)
       const int idx = item_of_round(k);
       if (idx >= num_items) continue;
       const Item item = decode(idx);
+      if (!warp_bound_ok(item_ok(item), p.status, abortf, kChkItem)) {
+        ok = false;
+        break;
+      }
       const int bh = item.bh;
       const int n_t = item.n_t[t];
       // This tile's O staging use of the ring, when the item has one.
@@ -633,6 +670,10 @@ __global__ void __launch_bounds__(FwdCfg<D, kFp8>::threads(kStage), 1)
       for (int j = 0; j < n_t; ++j) {
         const int jj = next_tile_t(item, t, cur);  // key tile
         cur = jj + 1;
+        if (!warp_bound_ok(jj >= 0 && jj < p.n_kv, p.status, abortf, kChkKvTile)) {
+          ok = false;
+          break;
+        }
         // Columns >= tlim of this key tile are masked for this row.
         const int tlim = lim - jj * kTile;
         ok = mbar_wait(&sm.s_full[t], s_par, p.status, abortf, kSiteSFull);
@@ -640,102 +681,7 @@ __global__ void __launch_bounds__(FwdCfg<D, kFp8>::threads(kStage), 1)
         s_par ^= 1;
         if (!ok) break;
         tc_fence_after();
-        uint32_t sr[4][32];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_ld32(colS + c * 32, sr[c]);
-#pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_wait_ld(sr[c]);
-
-        if (tlim < kTile) {
-#pragma unroll
-          for (int c = 0; c < 4; ++c)
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-              if (c * 32 + i >= tlim) sr[c][i] = __float_as_uint(neutral);
-        }
-        // Tile extreme of the raw scores: eight independent chains of
-        // three-input max (min), joined by a tree (exact in any order).
-        float mx8[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) mx8[u] = neutral;
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-#pragma unroll
-          for (int i = 0; i < 32; i += 2) {
-            const int u = (i >> 1) & 7;
-            mx8[u] = kNeg ? fmin3(mx8[u], __uint_as_float(sr[c][i]), __uint_as_float(sr[c][i + 1]))
-                          : fmax3(mx8[u], __uint_as_float(sr[c][i]), __uint_as_float(sr[c][i + 1]));
-          }
-#pragma unroll
-        for (int w = 4; w > 0; w >>= 1)
-#pragma unroll
-          for (int u = 0; u < w; ++u)
-            mx8[u] = kNeg ? fminf(mx8[u], mx8[u + w]) : fmaxf(mx8[u], mx8[u + w]);
-        const float m_tile = mx8[0] * c2;
-        float alpha = 1.f;
-        if (m_tile > m_ref + kRescaleSlack) {
-          alpha = ex2_approx(m_ref - m_tile);  // 0 on the first tile (m_ref = -inf)
-          m_ref = m_tile;
-        }
-        l *= alpha;
-        // p = 2^(c2 * s - m) for pairs of scores with packed f32x2 FMAs (a
-        // row that has seen no key yet keeps m = -inf and all p = 0); four
-        // packed partial row sums, joined by a tree below.
-        const float neg_m = m_ref == ninf ? 0.f : -m_ref;
-        const uint64_t c2x2 = f2_pack(c2, c2);
-        const uint64_t negm2 = f2_pack(neg_m, neg_m);
-        uint64_t ls4[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) ls4[u] = 0;
-        uint32_t pk8[kFp8 ? 32 : 1];  // FP8: all 128 probabilities, four per column
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          uint32_t pk[32];
-#pragma unroll
-          for (int c2i = 0; c2i < 2; ++c2i) {
-            const int c = 2 * h + c2i;
-#pragma unroll
-            for (int i = 0; i < 32; i += 2) {
-              float x0, x1;
-              f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[c][i]), __uint_as_float(sr[c][i + 1])),
-                               c2x2, negm2),
-                        x0, x1);
-              const float p0 = ex2_approx(x0);
-              const float p1 = ex2_approx(x1);
-              ls4[(i >> 1) & 3] = f2_add(ls4[(i >> 1) & 3], f2_pack(p0, p1));
-              if constexpr (kFp8) {
-                const uint32_t two = pack_e4m3x2(p0, p1);
-                if (((i >> 1) & 1) == 0)
-                  pk8[(c * 32 + i) >> 2] = two;
-                else
-                  pk8[(c * 32 + i) >> 2] |= two << 16;
-              } else {
-                pk[c2i * 16 + i / 2] = pack_bf16x2(p0, p1);
-              }
-            }
-          }
-          if constexpr (!kFp8) tmem_st32(colS + h * 32, pk);
-        }
-        if constexpr (kFp8) tmem_st32(colS, pk8);
-        ls4[0] = f2_add(f2_add(ls4[0], ls4[1]), f2_add(ls4[2], ls4[3]));
-        float lsa, lsb;
-        f2_unpack(ls4[0], lsa, lsb);
-        l += lsa + lsb;
-        tmem_wait_st();
-        // Correct the O accumulator if this row's reference moved (warp-wide
-        // decision: TMEM loads/stores are warp-collective).
-        if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-#pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t orow[32];
-            tmem_ld32(colO + c * 32, orow);
-            tmem_wait_ld(orow);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) orow[i] = __float_as_uint(__uint_as_float(orow[i]) * alpha);
-            tmem_st32(colO + c * 32, orow);
-          }
-          tmem_wait_st();
-        }
+        softmax_tile<D, kNeg, kFp8>(colS, colO, c2, tlim, j > 0, m_ref, l);
         tc_fence_before();
         mbar_arrive(&sm.p_full[t]);
       }
@@ -749,6 +695,11 @@ __global__ void __launch_bounds__(FwdCfg<D, kFp8>::threads(kStage), 1)
       const float inv_l = any ? o_mul / l : 0.f;
       const bool valid = R < p.rows;
       const size_t row_g = (size_t)bh * p.rows + R;
+      if (!warp_bound_ok(!valid || (R >= 0 && row_g < (size_t)p.BH * p.rows), p.status, abortf,
+                         kChkRow)) {
+        ok = false;
+        break;
+      }
       if (staged) {
         const int slot = stage_use % S;
         ok = mbar_wait(&sm.stage_ready[t], n_staged & 1, p.status, abortf, kSiteStageSlot);
@@ -855,6 +806,8 @@ __global__ void __launch_bounds__(256) fa_combine_kernel(const FwdParams p) {
   const float ninf = __int_as_float(0xff800000);
   constexpr float kL2e = 1.4426950408889634f;
   const int S = p.splits;
+  int no_abort = 0;
+  if (!bound_ok(S >= 1 && row >= 0, p.status, &no_abort, kChkCombine)) return;
   const float* lse_row_s = p.lse_part + row;  // split s at lse_row_s[s * rows_total]
   float m = ninf;
   for (int s = lane; s < S; s += 32) m = fmaxf(m, lse_row_s[s * rows_total]);

@@ -126,6 +126,16 @@ struct BwdParams {
 // FA_ERR_* code.
 int make_tmap_bhnd(const void* base, int BH, int N, int d, CUtensorMap* out);
 
+// The same map with a box of `box_rows` rows (the pair kernel's K halves).
+int make_tmap_bhnd_rows(const void* base, int BH, int N, int d, int box_rows, CUtensorMap* out);
+
+// The forward pass on CTA pairs (tcgen05 cta_group::2): square shapes with
+// d = 128 and no mask.  tkh is K's map with a 64-row box.  At most
+// `max_pairs` pairs are launched (fwd_pair_max_active: pairs that fit at once).
+int launch_fwd_pair(const CUtensorMap& tq, const CUtensorMap& tkh, const CUtensorMap& tv,
+                    const FwdParams& p, cudaStream_t stream, int max_pairs);
+int fwd_pair_max_active(int sm_count);
+
 // `to` is a tensor map over O with the shape of tq's; only the square bf16
 // kernels that stage O for TMA stores use it.
 int launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,

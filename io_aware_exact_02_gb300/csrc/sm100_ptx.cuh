@@ -15,6 +15,15 @@ namespace fa {
 
 // Status codes written by kernels into the library's device status word.
 constexpr int kStatusTimeout = -7;
+constexpr int kStatusBounds = -8;
+
+// Bounds-checked build: compiled with FA_CHECKS, the kernels range-check
+// the tile, mask and row indices they compute (bound_ok below).
+#ifdef FA_CHECKS
+constexpr bool kChecks = true;
+#else
+constexpr bool kChecks = false;
+#endif
 
 // A wait gives up after this many nanoseconds of %globaltimer (2 s).  Every
 // legitimate wait in these kernels lasts microseconds.
@@ -79,13 +88,42 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Per-CTA abort protocol: the first waiter that times out stores the code
-// in the device status word (first error wins) and sets the CTA's abort
-// flag; every other waiter polls that flag and gives up too.
-static __device__ __noinline__ void report_timeout(int* status, volatile int* abort_flag, int site) {
-  atomicCAS(status, 0, kStatusTimeout);
-  atomicCAS(status + 1, 0, site);
+// Per-CTA abort protocol: the first waiter that times out (or check that
+// fails) stores its code and site in the device status word (first error
+// wins) and sets the CTA's abort flag; every other waiter polls that flag
+// and gives up too.
+static __device__ __noinline__ void report_status(int* status, volatile int* abort_flag, int code,
+                                                  int site) {
+  if (atomicCAS(status, 0, code) == 0) atomicExch(status + 1, site);
   *abort_flag = 1;
+}
+static __device__ __forceinline__ void report_timeout(int* status, volatile int* abort_flag,
+                                                      int site) {
+  report_status(status, abort_flag, kStatusTimeout, site);
+}
+
+// A bounds check: in the checked build, false (with FA_ERR_BOUNDS and the
+// site recorded, and the CTA's abort flag raised) when `in_range` is false;
+// the caller then skips the access and winds down.  Always true, and
+// compiled out, in the default build.
+__device__ __forceinline__ bool bound_ok(bool in_range, int* status, volatile int* abort_flag,
+                                         int site) {
+  if constexpr (kChecks) {
+    if (!in_range) {
+      report_status(status, abort_flag, kStatusBounds, site);
+      return false;
+    }
+  }
+  return true;
+}
+// The same for warp-collective code: false in every lane if any lane's
+// check fails.
+__device__ __forceinline__ bool warp_bound_ok(bool in_range, int* status,
+                                              volatile int* abort_flag, int site) {
+  if constexpr (kChecks) {
+    return __all_sync(0xffffffffu, bound_ok(in_range, status, abort_flag, site));
+  }
+  return true;
 }
 
 // Wait until the phase with the given parity of `bar` has completed.

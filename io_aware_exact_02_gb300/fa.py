@@ -19,7 +19,11 @@ import threading
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libfa.so")
+# FA_CHECKED=1 selects the bounds-checked build (python -m
+# io_aware_exact_02_gb300.build --checked), whose kernels range-check every
+# tile, mask and row index they compute.
+CHECKED = os.environ.get("FA_CHECKED") == "1"
+LIB_PATH = os.path.join(_HERE, "libfa_checked.so" if CHECKED else "libfa.so")
 
 FA_OK = 0
 FA_ERR_ARG = -1
@@ -29,6 +33,7 @@ FA_ERR_WORKSPACE = -4
 FA_ERR_DEVICE = -5
 FA_ERR_LAUNCH = -6
 FA_ERR_TIMEOUT = -7
+FA_ERR_BOUNDS = -8
 
 # Size of the static scratch array fa_bwd_noalloc uses (FA_NOALLOC_SCRATCH_BYTES).
 FA_NOALLOC_SCRATCH_BYTES = 32 << 20
@@ -59,6 +64,8 @@ SIGNATURES = {
     "fa_fwd_fp8": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _vp, _sz, _vp]),
     "fa_device_status": (_i, [_vp, _ip]),
     "fa_selftest_timeout": (_i, [_i, _vp]),
+    "fa_checks_enabled": (_i, []),
+    "fa_selftest_bounds": (_i, [_vp]),
     "fa_status_string": (ctypes.c_char_p, [_i]),
     "fa_fwd_schedule": (_i, [_i, _i, _i, _i, _i, _ip, _ip, _ip, _ip, _i]),
     "fa_snake_assign": (_i, [_i, _i, _ip]),
@@ -419,6 +426,21 @@ def selftest_timeout(timeout_us: int = 20000):
     fa_selftest_timeout); read the result with device_status()."""
     s = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
     _check("fa_selftest_timeout", load().fa_selftest_timeout(int(timeout_us), s))
+
+
+FA_SITE_SELFTEST_BOUNDS = 902
+
+
+def checks_enabled() -> bool:
+    """True for the bounds-checked build of the library."""
+    return bool(load().fa_checks_enabled())
+
+
+def selftest_bounds():
+    """Launch the bounds-check self test on the current stream (see
+    fa_selftest_bounds); read the result with device_status()."""
+    s = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    _check("fa_selftest_bounds", load().fa_selftest_bounds(s))
 
 
 def check_device_status(stream=None):

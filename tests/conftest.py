@@ -26,3 +26,16 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+@pytest.fixture(autouse=True)
+def _status_word_clear_under_checks(request):
+    """With the bounds-checked library (FA_CHECKED=1), every GPU test must
+    leave the device status word clear: no kernel caught an out-of-range
+    index (tests that provoke an error on purpose read and clear it)."""
+    yield
+    if os.environ.get("FA_CHECKED") == "1" and "gpu" in request.keywords:
+        from io_aware_exact_02_gb300 import fa
+        code, site = fa.device_status()
+        assert code == fa.FA_OK, "status word %d at site %d after %s" % (code, site,
+                                                                      request.node.name)

@@ -301,3 +301,19 @@ def test_binding_rejects_tensors_on_another_device():
     b = torch.empty(4)
     with pytest.raises(ValueError, match="share a device"):
         fa._on_device(b, k=a)
+
+
+def test_checks_compiled_out_of_the_default_build(lib):
+    assert lib.fa_checks_enabled() == (1 if fa.CHECKED else 0)
+
+
+def test_checked_build_compiles_and_reports_it():
+    """The bounds-checked variant builds from the same sources (nvcc with
+    -DFA_CHECKS) and exports the same symbols."""
+    from io_aware_exact_02_gb300 import build
+    path = build.build(checked=True)
+    chk = fa.load(path)
+    assert chk.fa_checks_enabled() == 1
+    for name in declared_symbols():
+        assert hasattr(chk, name), name
+    assert chk.fa_status_string(fa.FA_ERR_BOUNDS) != b"unknown status"

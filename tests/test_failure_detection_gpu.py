@@ -1,7 +1,9 @@
 """Failure detection on the GPU without a fault: a kernel wait that runs out
 (a barrier nothing completes, with a short limit) is reported through the
 status word, the word is cleared by reading it, and the context stays
-usable for the attention kernels afterwards."""
+usable for the attention kernels afterwards.  The bounds check of the
+checked build is exercised the same way: a check on an index one past its
+range, which touches no memory."""
 import math
 
 import numpy as np
@@ -42,3 +44,11 @@ def test_context_usable_after_a_timeout():
     assert np.abs(o.float().cpu().numpy() - o_ref).max() <= 2e-2
     assert np.abs(lse.cpu().numpy() - lse_ref).max() <= 1e-3
     fa.check_device_status()
+
+
+def test_bounds_check_self_test():
+    assert fa.device_status() == (fa.FA_OK, 0)
+    fa.selftest_bounds()
+    if fa.checks_enabled():
+        assert fa.device_status() == (fa.FA_ERR_BOUNDS, fa.FA_SITE_SELFTEST_BOUNDS)
+    assert fa.device_status() == (fa.FA_OK, 0)
