@@ -172,6 +172,7 @@ __device__ __forceinline__ size_t dqacc_index(int bh, int n_kv, int row, int c4)
 
 template <int D>
 __global__ void __launch_bounds__(256) fa_bwd_prep_kernel(const BwdParams p) {
+  wait_prior_grid();  // O (and the workspace) belong to the previous kernel until it ends
   constexpr int kLanesPerRow = D / 8;  // 16-byte loads of 8 bf16
   constexpr int kRowsPerWarp = 32 / kLanesPerRow;
   const int lane = threadIdx.x & 31;
@@ -225,6 +226,7 @@ __global__ void __launch_bounds__(256) fa_bwd_prep_kernel(const BwdParams p) {
 
 template <int D>
 __global__ void __launch_bounds__(256) fa_bwd_convert_kernel(const BwdParams p) {
+  wait_prior_grid();  // the main kernel's dQ reductions
   // One thread per 8 output elements (one 16-byte store).
   const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   const long long total = (long long)p.BH * p.N * (D / 8);
@@ -304,6 +306,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
+  // The setup above overlaps the prep kernel's end; its outputs (the work
+  // counter, the row terms, the zeroed accumulator) are read only after it.
+  wait_prior_grid();
 
   // Work items t = (head, key tile j) in the order of bwd_item.  The
   // producer claims them one at a time from the workspace counter and hands
@@ -813,13 +818,33 @@ int launch_bwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap
   // are still multiplied by the exact scale.
   if (p.scale_log2 == 0.f) p.scale_log2 = 1.17549435e-38f;
   const long long npad = (long long)p.n_kv * kTile;
+  // Each kernel is launched with programmatic stream serialization: its
+  // launch (and the main kernel's setup) overlaps the end of the kernel
+  // before it on the stream, and it waits for that kernel's completion
+  // (wait_prior_grid) before it touches memory that kernel writes.
+  cudaLaunchAttribute pdl[1];
+  pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl[0].val.programmaticStreamSerializationAllowed = 1;
+  auto config = [&](unsigned grid, unsigned block, size_t smem) {
+    cudaLaunchConfig_t c = {};
+    c.gridDim = dim3(grid, 1, 1);
+    c.blockDim = dim3(block, 1, 1);
+    c.dynamicSmemBytes = smem;
+    c.stream = stream;
+    c.attrs = pdl;
+    c.numAttrs = 1;
+    return c;
+  };
   // 1. prep: one warp per (32 / (D/8)) rows.
   if (mask & 1) {
     const long long rows = (long long)p.BH * npad;
     const long long warps = (rows + (32 / (D / 8)) - 1) / (32 / (D / 8));
     const long long blocks = (warps * 32 + 255) / 256;
-    fa_bwd_prep_kernel<D><<<(unsigned)blocks, 256, 0, stream>>>(p);
-    if (cudaGetLastError() != cudaSuccess) return FA_ERR_LAUNCH;
+    const cudaLaunchConfig_t c = config((unsigned)blocks, 256, 0);
+    if (cudaLaunchKernelEx(&c, fa_bwd_prep_kernel<D>, p) != cudaSuccess) {
+      cudaGetLastError();
+      return FA_ERR_LAUNCH;
+    }
   }
   // 2. main
   if (mask & 2) {
@@ -842,14 +867,20 @@ int launch_bwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap
     // scheduling, which under a causal or block mask is the LPT rule).
     const long long items = (long long)p.BH * p.n_kv;
     const unsigned grid = (unsigned)(p.sm_count < 1 || items <= p.sm_count ? items : p.sm_count);
-    kern<<<grid, BwdCfg<D>::kThreads, smem, stream>>>(tq, tk, tv, tdo, p);
-    if (cudaGetLastError() != cudaSuccess) return FA_ERR_LAUNCH;
+    const cudaLaunchConfig_t c = config(grid, BwdCfg<D>::kThreads, smem);
+    if (cudaLaunchKernelEx(&c, kern, tq, tk, tv, tdo, p) != cudaSuccess) {
+      cudaGetLastError();
+      return FA_ERR_LAUNCH;
+    }
   }
   // 3. convert
   if (mask & 4) {
     const long long total = (long long)p.BH * p.N * (D / 8);
-    fa_bwd_convert_kernel<D><<<(unsigned)((total + 255) / 256), 256, 0, stream>>>(p);
-    if (cudaGetLastError() != cudaSuccess) return FA_ERR_LAUNCH;
+    const cudaLaunchConfig_t c = config((unsigned)((total + 255) / 256), 256, 0);
+    if (cudaLaunchKernelEx(&c, fa_bwd_convert_kernel<D>, p) != cudaSuccess) {
+      cudaGetLastError();
+      return FA_ERR_LAUNCH;
+    }
   }
   return FA_OK;
 }

@@ -182,6 +182,9 @@ __global__ void __launch_bounds__(FwdCfg<D, kFp8>::threads(kStage), 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
+  // The setup above may overlap the end of the previous kernel on the stream
+  // (programmatic dependent launch); its outputs are read only after this.
+  wait_prior_grid();
 
   // Persistent CTAs: CTA c takes the work items of the longest-first list
   // in "snake" order -- items c, 2G-1-c, 2G+c, 4G-1-c, ... for G CTAs -- so
@@ -797,6 +800,7 @@ __global__ void __launch_bounds__(FwdCfg<D, kFp8>::threads(kStage), 1)
 // latencies rather than one per split.
 template <int D>
 __global__ void __launch_bounds__(256) fa_combine_kernel(const FwdParams p) {
+  wait_prior_grid();  // the forward kernel's split results
   constexpr int kPer = D / 32;  // 4 or 2 columns per lane
   constexpr int kBatch = 8;     // split O rows loaded together
   const long long row = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -886,13 +890,33 @@ int launch_fwd_dn(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMa
         attr.numRegs < FwdCfg<D, kFp8>::kRegsLaunch)
       return FA_ERR_LAUNCH;
   }
-  fa_fwd_kernel<D, kNeg, kGeneral, kSparse, kFp8, kStage>
-      <<<(unsigned)p.grid, FwdCfg<D, kFp8>::threads(kStage), smem, stream>>>(tq, tk, tv, to, p);
-  if (cudaGetLastError() != cudaSuccess) return FA_ERR_LAUNCH;
+  // Launched with programmatic stream serialization: the kernel's launch
+  // and setup overlap the end of the previous kernel on the stream, and it
+  // waits for that kernel (wait_prior_grid) before reading any input.
+  cudaLaunchAttribute pdl[1];
+  pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t c = {};
+  c.gridDim = dim3((unsigned)p.grid, 1, 1);
+  c.blockDim = dim3(FwdCfg<D, kFp8>::threads(kStage), 1, 1);
+  c.dynamicSmemBytes = smem;
+  c.stream = stream;
+  c.attrs = pdl;
+  c.numAttrs = 1;
+  if (cudaLaunchKernelEx(&c, fa_fwd_kernel<D, kNeg, kGeneral, kSparse, kFp8, kStage>, tq, tk, tv, to,
+                         p) != cudaSuccess) {
+    cudaGetLastError();
+    return FA_ERR_LAUNCH;
+  }
   if (p.splits > 1) {
     const long long threads = (long long)p.BH * p.rows * 32;
-    fa_combine_kernel<D><<<(unsigned)((threads + 255) / 256), 256, 0, stream>>>(p);
-    if (cudaGetLastError() != cudaSuccess) return FA_ERR_LAUNCH;
+    c.gridDim = dim3((unsigned)((threads + 255) / 256), 1, 1);
+    c.blockDim = dim3(256, 1, 1);
+    c.dynamicSmemBytes = 0;
+    if (cudaLaunchKernelEx(&c, fa_combine_kernel<D>, p) != cudaSuccess) {
+      cudaGetLastError();
+      return FA_ERR_LAUNCH;
+    }
   }
   return FA_OK;
 }
