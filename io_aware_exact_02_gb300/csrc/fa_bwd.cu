@@ -73,7 +73,7 @@ struct BwdCfg {
   // Registers per thread at launch, after the fifth warpgroup's setmaxnreg.dec
   // and after the compute warpgroups' setmaxnreg.inc; the split must fit in
   // the launch's registers, or the increase would wait forever.
-  static constexpr int kRegsLaunch = 96, kRegsCtl = 56, kRegsCompute = 104;
+  static constexpr int kRegsLaunch = 96, kRegsCtl = 64, kRegsCompute = 104;
   static_assert(kWG * 128 * kRegsCompute + 128 * kRegsCtl <= kThreads * kRegsLaunch,
                 "register split above the launch's total");
   static constexpr int kWarpLoad = kWG * 4, kWarpMma = kWG * 4 + 1;
@@ -128,6 +128,9 @@ __device__ __forceinline__ uint64_t kmajor_desc(uint32_t base, int kk) {
 __device__ __forceinline__ uint64_t mnmajor_desc(uint32_t base, int kk) {
   return sdesc_sw128(base + kk * 2048, 16384, 1024);
 }
+// Byte offsets of K-step kk in a K-major tile and in an MN-major tile.
+__host__ __device__ constexpr uint32_t kmajor_off(int kk) { return (kk >> 2) * 16384 + (kk & 3) * 32; }
+__host__ __device__ constexpr uint32_t mnmajor_off(int kk) { return kk * 2048; }
 
 __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
   const uint32_t a = smem_u32(bar);
@@ -461,9 +464,11 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
             tc_fence_after();
             const uint32_t qb2 = smem_u32(sm.q[s2]);
             const uint32_t col = (gs & 1) ? Cfg::kColS2 : Cfg::kColS;
-#pragma unroll 1
+            const uint64_t kd = desc_here(kmajor_desc(kb, 0)), qd = desc_here(kmajor_desc(qb2, 0));
+#pragma unroll
             for (int kk = 0; kk < D / 16; ++kk)
-              mma_ss(tmem + col, kmajor_desc(kb, kk), kmajor_desc(qb2, kk), id_s, kk > 0);
+              mma_ss(tmem + col, desc_plus(kd, kmajor_off(kk)), desc_plus(qd, kmajor_off(kk)), id_s,
+                     kk > 0);
             tc_commit(&sm.s_full[gs & 1]);
             return true;
           };
@@ -479,9 +484,13 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
               if (!ok) break;
               tc_fence_after();
             }
-#pragma unroll 1
-            for (int kk = 0; kk < D / 16; ++kk)
-              mma_ss(tmem + Cfg::kColDP, kmajor_desc(vb, kk), kmajor_desc(dob, kk), id_s, kk > 0);
+            {
+              const uint64_t vd = desc_here(kmajor_desc(vb, 0)), dd = desc_here(kmajor_desc(dob, 0));
+#pragma unroll
+              for (int kk = 0; kk < D / 16; ++kk)
+                mma_ss(tmem + Cfg::kColDP, desc_plus(vd, kmajor_off(kk)),
+                       desc_plus(dd, kmajor_off(kk)), id_s, kk > 0);
+            }
             tc_commit(&sm.dp_full);
             // The next step's S^T into the other region (its previous step's
             // dV and dK, issued earlier, have read it).
@@ -489,21 +498,32 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
             ok = mbar_wait(&sm.p_ready, par, p.status, abortf, kSitePReady);
             if (!ok) break;
             tc_fence_after();
-#pragma unroll 1
-            for (int kk = 0; kk < kTile / 16; ++kk)
-              mma_ts(tmem + Cfg::kColDV, tmem + cs + (kk * 16 / kQ) * kQ + (kk * 16 % kQ) / 2,
-                     mnmajor_desc(dob, kk), id_acc, (it > 0 || kk > 0) ? 1u : 0u);
+            {
+              const uint64_t dd = desc_here(mnmajor_desc(dob, 0));
+#pragma unroll
+              for (int kk = 0; kk < kTile / 16; ++kk)
+                mma_ts(tmem + Cfg::kColDV, tmem + cs + (kk * 16 / kQ) * kQ + (kk * 16 % kQ) / 2,
+                       desc_plus(dd, mnmajor_off(kk)), id_acc, (it > 0 || kk > 0) ? 1u : 0u);
+            }
             ok = mbar_wait(&sm.ds_ready, par, p.status, abortf, kSiteDsReady);
             if (!ok) break;
             tc_fence_after();
-#pragma unroll 1
-            for (int kk = 0; kk < kTile / 16; ++kk)
-              mma_ts(tmem + Cfg::kColDK, tmem + cs + kQ / 2 + (kk * 16 / kQ) * kQ + (kk * 16 % kQ) / 2,
-                     mnmajor_desc(qb, kk), id_acc, (it > 0 || kk > 0) ? 1u : 0u);
+            {
+              const uint64_t qd = desc_here(mnmajor_desc(qb, 0));
+#pragma unroll
+              for (int kk = 0; kk < kTile / 16; ++kk)
+                mma_ts(tmem + Cfg::kColDK,
+                       tmem + cs + kQ / 2 + (kk * 16 / kQ) * kQ + (kk * 16 % kQ) / 2,
+                       desc_plus(qd, mnmajor_off(kk)), id_acc, (it > 0 || kk > 0) ? 1u : 0u);
+            }
             tc_commit(&sm.q_empty[s]);
-#pragma unroll 1
-            for (int kk = 0; kk < kTile / 16; ++kk)
-              mma_ss(tmem + Cfg::kColDP, mnmajor_desc(dsb, kk), mnmajor_desc(kb, kk), id_dq, kk > 0);
+            {
+              const uint64_t sd = desc_here(mnmajor_desc(dsb, 0)), kd = desc_here(mnmajor_desc(kb, 0));
+#pragma unroll
+              for (int kk = 0; kk < kTile / 16; ++kk)
+                mma_ss(tmem + Cfg::kColDP, desc_plus(sd, mnmajor_off(kk)),
+                       desc_plus(kd, mnmajor_off(kk)), id_dq, kk > 0);
+            }
             tc_commit(&sm.dq_full);
           }
         } else
@@ -515,9 +535,13 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
           if (!ok) break;
           tc_fence_after();
           // S^T = K_j Q_i^T
-#pragma unroll 1
-          for (int kk = 0; kk < D / 16; ++kk)
-            mma_ss(tmem + Cfg::kColS, kmajor_desc(kb, kk), kmajor_desc(qb, kk), id_s, kk > 0);
+          {
+            const uint64_t kd = desc_here(kmajor_desc(kb, 0)), qd = desc_here(kmajor_desc(qb, 0));
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk)
+              mma_ss(tmem + Cfg::kColS, desc_plus(kd, kmajor_off(kk)), desc_plus(qd, kmajor_off(kk)),
+                     id_s, kk > 0);
+          }
           tc_commit(&sm.s_full[0]);
           // dP^T = V_j dO_i^T, into the columns the previous step's dQ occupied
           if (gstep > 0) {
@@ -525,34 +549,49 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
             if (!ok) break;
             tc_fence_after();
           }
-#pragma unroll 1
-          for (int kk = 0; kk < D / 16; ++kk)
-            mma_ss(tmem + Cfg::kColDP, kmajor_desc(vb, kk), kmajor_desc(dob, kk), id_s, kk > 0);
+          {
+            const uint64_t vd = desc_here(kmajor_desc(vb, 0)), dd = desc_here(kmajor_desc(dob, 0));
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk)
+              mma_ss(tmem + Cfg::kColDP, desc_plus(vd, kmajor_off(kk)),
+                     desc_plus(dd, kmajor_off(kk)), id_s, kk > 0);
+          }
           tc_commit(&sm.dp_full);
           // dV += P^T dO_i.  Warpgroup g's P^T sits in TMEM columns
           // [kQ g, kQ g + kQ/2) as bf16 pairs.
           ok = mbar_wait(&sm.p_ready, par, p.status, abortf, kSitePReady);
           if (!ok) break;
           tc_fence_after();
-#pragma unroll 1
-          for (int kk = 0; kk < kTile / 16; ++kk)
-            mma_ts(tmem + Cfg::kColDV, tmem + Cfg::kColS + (kk * 16 / kQ) * kQ + (kk * 16 % kQ) / 2,
-                   mnmajor_desc(dob, kk), id_acc, (it > 0 || kk > 0) ? 1u : 0u);
+          {
+            const uint64_t dd = desc_here(mnmajor_desc(dob, 0));
+#pragma unroll
+            for (int kk = 0; kk < kTile / 16; ++kk)
+              mma_ts(tmem + Cfg::kColDV,
+                     tmem + Cfg::kColS + (kk * 16 / kQ) * kQ + (kk * 16 % kQ) / 2,
+                     desc_plus(dd, mnmajor_off(kk)), id_acc, (it > 0 || kk > 0) ? 1u : 0u);
+          }
           // dQ_i = dS K_j ; dK += dS^T Q_i.  dQ goes first: the compute
           // warps then read it out and start its reductions while the tensor
           // core runs dK and the next S^T.
           ok = mbar_wait(&sm.ds_ready, par, p.status, abortf, kSiteDsReady);
           if (!ok) break;
           tc_fence_after();
-#pragma unroll 1
-          for (int kk = 0; kk < kTile / 16; ++kk)
-            mma_ss(tmem + Cfg::kColDP, mnmajor_desc(dsb, kk), mnmajor_desc(kb, kk), id_dq, kk > 0);
+          {
+            const uint64_t sd = desc_here(mnmajor_desc(dsb, 0)), kd = desc_here(mnmajor_desc(kb, 0));
+#pragma unroll
+            for (int kk = 0; kk < kTile / 16; ++kk)
+              mma_ss(tmem + Cfg::kColDP, desc_plus(sd, mnmajor_off(kk)),
+                     desc_plus(kd, mnmajor_off(kk)), id_dq, kk > 0);
+          }
           tc_commit(&sm.dq_full);
-#pragma unroll 1
-          for (int kk = 0; kk < kTile / 16; ++kk)
-            mma_ts(tmem + Cfg::kColDK,
-                   tmem + Cfg::kColS + kQ / 2 + (kk * 16 / kQ) * kQ + (kk * 16 % kQ) / 2,
-                   mnmajor_desc(qb, kk), id_acc, (it > 0 || kk > 0) ? 1u : 0u);
+          {
+            const uint64_t qd = desc_here(mnmajor_desc(qb, 0));
+#pragma unroll
+            for (int kk = 0; kk < kTile / 16; ++kk)
+              mma_ts(tmem + Cfg::kColDK,
+                     tmem + Cfg::kColS + kQ / 2 + (kk * 16 / kQ) * kQ + (kk * 16 % kQ) / 2,
+                     desc_plus(qd, mnmajor_off(kk)), id_acc, (it > 0 || kk > 0) ? 1u : 0u);
+          }
           tc_commit(&sm.q_empty[s]);
         }
         if (!ok) break;

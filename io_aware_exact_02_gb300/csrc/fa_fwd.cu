@@ -395,15 +395,14 @@ __global__ void __launch_bounds__(FwdCfg<D, kFp8>::threads(kStage), 1)
       bool ok = true;
 
       auto issue_s = [&](int t, int kslot) {
-        const uint32_t kb = smem_u32(sm.kv[kslot]);
-#pragma unroll 1
+        const uint64_t qd = desc_here(kmajor_desc(q_addr[t], 0)), kd = desc_here(kmajor_desc(smem_u32(sm.kv[kslot]), 0));
+#pragma unroll
         for (int kk = 0; kk < Cfg::kKSteps; ++kk) {
+          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
           if constexpr (kFp8)
-            mma_ss_f8(tmem + Cfg::col_s(t), kmajor_desc(q_addr[t], kk), kmajor_desc(kb, kk), id_s,
-                      kk > 0);
+            mma_ss_f8(tmem + Cfg::col_s(t), desc_plus(qd, off), desc_plus(kd, off), id_s, kk > 0);
           else
-            mma_ss(tmem + Cfg::col_s(t), kmajor_desc(q_addr[t], kk), kmajor_desc(kb, kk), id_s,
-                   kk > 0);
+            mma_ss(tmem + Cfg::col_s(t), desc_plus(qd, off), desc_plus(kd, off), id_s, kk > 0);
         }
         tc_commit(&sm.s_full[t]);
       };
@@ -416,14 +415,16 @@ __global__ void __launch_bounds__(FwdCfg<D, kFp8>::threads(kStage), 1)
           tc_fence_after();
         }
         const uint32_t vb = smem_u32(sm.kv[vslot]);
-#pragma unroll 1
+        const uint64_t vd = desc_here(kFp8 ? kmajor_desc(vb, 0) : mnmajor_desc(vb, 0));
+#pragma unroll
         for (int kk = 0; kk < Cfg::kPvSteps; ++kk) {
           // P occupies 8 TMEM columns per K-step: 16 bf16 or 32 E4M3 keys.
           if constexpr (kFp8)
-            mma_ts_f8(tmem + Cfg::col_o(t), tmem + Cfg::col_s(t) + kk * 8, kmajor_desc(vb, kk),
-                      id_pv, (accumulate || kk > 0) ? 1u : 0u);
+            mma_ts_f8(tmem + Cfg::col_o(t), tmem + Cfg::col_s(t) + kk * 8,
+                      desc_plus(vd, (kk >> 2) * 16384 + (kk & 3) * 32), id_pv,
+                      (accumulate || kk > 0) ? 1u : 0u);
           else
-            mma_ts(tmem + Cfg::col_o(t), tmem + Cfg::col_s(t) + kk * 8, mnmajor_desc(vb, kk),
+            mma_ts(tmem + Cfg::col_o(t), tmem + Cfg::col_s(t) + kk * 8, desc_plus(vd, kk * 2048),
                    id_pv, (accumulate || kk > 0) ? 1u : 0u);
         }
         return true;

@@ -331,6 +331,25 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
   return d;
 }
 
+// The descriptor of the same operand `bytes` further on (the next K-step of a
+// tile).  The start-address field holds address >> 4 in its low 14 bits and
+// shared-memory addresses stay below 256 KB, so the step is a plain add.
+// One thread issues every product of a CTA and a product at full rate takes
+// only 64 cycles (M = 128, N = 128, K = 16): descriptors are built once per
+// tile and stepped like this in fully unrolled issue loops, or the issuing
+// thread itself holds the tensor core back.
+__device__ __forceinline__ uint64_t desc_plus(uint64_t desc, uint32_t bytes) {
+  return desc + (uint64_t)(bytes >> 4);
+}
+// A tile's base descriptor, built where it is used: the compiler may not
+// hoist it (and the unrolled steps derived from it) out of the loop around,
+// which would keep every step's descriptor live in the issuing warp's
+// small register budget.
+__device__ __forceinline__ uint64_t desc_here(uint64_t desc) {
+  asm volatile("" : "+l"(desc));
+  return desc;
+}
+
 // 32 consecutive 32-bit TMEM columns of this thread's lane (warp w of a
 // warpgroup reaches lanes 32*(w%4) .. +31).
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
