@@ -1030,11 +1030,12 @@ def main(argv=None):
     ap.add_argument("--no-sweep", action="store_true",
                     help="skip the d=128 N sweep (1K, 2K, 4K, 16K) reported beside the headline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--fwd-pair", action="store_true",
-                    help="run the square d=128 forward on the CTA-pair kernel (FA_FWD_PAIR=1)")
+    ap.add_argument("--fwd-kernel", choices=["auto", "pair", "one"], default="auto",
+                    help="non-causal d=128 forward kernel: the library's choice (CTA pairs for "
+                         "N > 2048), or forced CTA pairs / one CTA per item (FA_FWD_PAIR)")
     args = ap.parse_args(argv)
-    if args.fwd_pair:
-        os.environ["FA_FWD_PAIR"] = "1"  # read by the library on its first forward call
+    if args.fwd_kernel != "auto":  # read by the library on its first forward call
+        os.environ["FA_FWD_PAIR"] = "1" if args.fwd_kernel == "pair" else "0"
 
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))

@@ -329,17 +329,21 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
   // the persistent grid serves them.
   const bool uneven = block_mask != nullptr || (causal && Nq > 16);
   p.grid = fwd_grid(g.BH, g.n_pairs * g.splits, uneven, ds->sm_count);
-  // Square, d = 128, no mask, and FA_FWD_PAIR=1 in the environment: the
-  // CTA-pair kernel (tcgen05 cta_group::2).  It is correct (bitwise equal to
-  // the one-CTA kernel) but measured slower on this GPU -- with its products
-  // at full rate the per-tile softmax chain and the cross-SM hops of P-ready
-  // and S-done bound it -- so the one-CTA kernel is the default.
-  static const bool pair_requested = [] {
+  // Square, d = 128, no mask, N > 2048: the CTA-pair kernel (tcgen05
+  // cta_group::2), whose products read half the shared memory per CTA.
+  // Measured at B8 H16 (TFLOP/s, pair / one CTA): N = 1K 950 / 1007, 2K
+  // 1469 / 1470, 4K 1666 / 1564, 8K 1753 / 1663, 16K 1689 / 1631; below 4K
+  // the one-CTA kernel's staged O stores win.  FA_FWD_PAIR=1 (or 0) in the
+  // environment forces the pair (or the one-CTA) kernel wherever the pair
+  // kernel applies; the library reads it once.
+  static const int pair_mode = [] {
     const char* e = std::getenv("FA_FWD_PAIR");
-    return e != nullptr && e[0] == '1' && e[1] == 0;
+    if (e != nullptr && (e[0] == '0' || e[0] == '1') && e[1] == 0) return e[0] - '0';
+    return -1;
   }();
-  if (pair_requested && d == 128 && !causal && block_mask == nullptr && g.splits == 1 &&
-      Hq == Hkv && Nq == Nkv) {
+  const bool pair_shape = d == 128 && !causal && block_mask == nullptr && g.splits == 1 &&
+                          Hq == Hkv && Nq == Nkv;
+  if (pair_shape && (pair_mode == 1 || (pair_mode == -1 && Nkv > 2048))) {
     CUtensorMap tkh;
     if ((rc = make_tmap_bhnd_rows(k, g.BH, Nkv, d, 64, &tkh)) != FA_OK) return rc;
     if (p.scale_log2 == 0.f) p.scale_log2 = 1.17549435e-38f;  // as launch_fwd does

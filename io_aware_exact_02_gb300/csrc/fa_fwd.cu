@@ -81,6 +81,7 @@ struct alignas(1024) FwdSmem {
   uint64_t kv_full[FwdCfg<D, kFp8>::kStages];
   uint64_t kv_empty[FwdCfg<D, kFp8>::kStages];
   uint64_t s_full[2];
+  uint64_t p_half[2];   // bf16: P of keys 0-63 of the tile in tensor memory
   uint64_t p_full[2];
   uint64_t o_full[2];
   uint64_t o_empty[2];  // softmax t has read O_t of the item (epilogue done)
@@ -95,7 +96,7 @@ struct alignas(1024) FwdSmem {
 // Wait sites reported through the status word.
 enum : int {
   kSiteQFull = 101, kSiteKvEmpty, kSiteKvFull, kSitePFull, kSiteSFull, kSiteOFull, kSiteDrain,
-  kSiteQEmpty, kSiteOEmpty, kSiteStageSlot, kSiteStaged, kSiteStored
+  kSiteQEmpty, kSiteOEmpty, kSiteStageSlot, kSiteStaged, kSiteStored, kSitePHalf
 };
 // Bounds checks of the checked build (FA_CHECKS).
 enum : int {
@@ -163,6 +164,7 @@ __global__ void __launch_bounds__(FwdCfg<D, kFp8>::threads(kStage), 1)
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&sm.s_full[t], 1);
+      mbar_init(&sm.p_half[t], 128);
       mbar_init(&sm.p_full[t], 128);
       mbar_init(&sm.o_full[t], 1);
       mbar_init(&sm.o_empty[t], 128);
@@ -418,6 +420,13 @@ __global__ void __launch_bounds__(FwdCfg<D, kFp8>::threads(kStage), 1)
         const uint64_t vd = desc_here(kFp8 ? kmajor_desc(vb, 0) : mnmajor_desc(vb, 0));
 #pragma unroll
         for (int kk = 0; kk < Cfg::kPvSteps; ++kk) {
+          if (!kFp8 && kk == Cfg::kPvSteps / 2) {
+            // bf16: the second half of P (keys 64-127).
+            const bool r = mbar_wait(&sm.p_full[t], p_par[t], p.status, abortf, kSitePFull);
+            p_par[t] ^= 1;
+            if (!r) return false;
+            tc_fence_after();
+          }
           // P occupies 8 TMEM columns per K-step: 16 bf16 or 32 E4M3 keys.
           if constexpr (kFp8)
             mma_ts_f8(tmem + Cfg::col_o(t), tmem + Cfg::col_s(t) + kk * 8,
@@ -432,10 +441,28 @@ __global__ void __launch_bounds__(FwdCfg<D, kFp8>::threads(kStage), 1)
       auto wait_full = [&](int cnt) -> bool {
         return mbar_wait(&sm.kv_full[cnt % S], (cnt / S) & 1, p.status, abortf, kSiteKvFull);
       };
+      // A Q tile without keys in this item: its O is final at once.  Softmax
+      // t must first have seen the previous item's o_full[t] phase (its
+      // epilogue's o_empty arrival says so): a commit right after that
+      // phase could otherwise complete the next one before the softmax
+      // looked, and its parity wait would then miss both.
+      auto finish_empty = [&](int t) -> bool {
+        if (n_done > 0 &&
+            !mbar_wait(&sm.o_empty[t], (n_done - 1) & 1, p.status, abortf, kSiteOEmpty))
+          return false;
+        tc_commit(&sm.o_full[t]);
+        return true;
+      };
+      // P_t ready for the next O += P V: all of it (FP8), or its first half
+      // (bf16; issue_pv waits for the second half itself).
       auto wait_p = [&](int t) -> bool {
-        const bool r = mbar_wait(&sm.p_full[t], p_par[t], p.status, abortf, kSitePFull);
-        p_par[t] ^= 1;
-        return r;
+        if constexpr (kFp8) {
+          const bool r = mbar_wait(&sm.p_full[t], p_par[t], p.status, abortf, kSitePFull);
+          p_par[t] ^= 1;
+          return r;
+        } else {
+          return mbar_wait(&sm.p_half[t], p_par[t], p.status, abortf, kSitePHalf);
+        }
       };
 
       for (int k = 0; ok && k * G < num_items; ++k) {
@@ -449,8 +476,9 @@ __global__ void __launch_bounds__(FwdCfg<D, kFp8>::threads(kStage), 1)
         const int nmax = it.nmax;
         if constexpr (!kSparse) {
           // A Q tile without keys is final at once (its rows get O = 0).
-          for (int t = 0; t < 2; ++t)
-            if (it.n_t[t] == 0) tc_commit(&sm.o_full[t]);
+          for (int t = 0; t < 2 && ok; ++t)
+            if (it.n_t[t] == 0) ok = finish_empty(t);
+          if (!ok) break;
           if (nmax == 0) {
             ++n_done;
             continue;
@@ -506,8 +534,9 @@ __global__ void __launch_bounds__(FwdCfg<D, kFp8>::threads(kStage), 1)
           // Step j's loads are K and V of tile 0's j-th tile, then of tile
           // 1's (for the tiles that have one), so the load index of each
           // product follows from the counts alone.
-          for (int t = 0; t < 2; ++t)
-            if (it.n_t[t] == 0) tc_commit(&sm.o_full[t]);
+          for (int t = 0; t < 2 && ok; ++t)
+            if (it.n_t[t] == 0) ok = finish_empty(t);
+          if (!ok) break;
           if (nmax == 0) {
             ++n_done;
             continue;
@@ -685,7 +714,8 @@ __global__ void __launch_bounds__(FwdCfg<D, kFp8>::threads(kStage), 1)
         s_par ^= 1;
         if (!ok) break;
         tc_fence_after();
-        softmax_tile<D, kNeg, kFp8>(colS, colO, c2, tlim, j > 0, m_ref, l);
+        softmax_tile<D, kNeg, kFp8>(colS, colO, c2, tlim, j > 0, m_ref, l,
+                                    [&] { mbar_arrive(&sm.p_half[t]); });
         tc_fence_before();
         mbar_arrive(&sm.p_full[t]);
       }

@@ -17,6 +17,9 @@
 // for its two P V products, and takes in 32 KB of K and V halves, against
 // 128 + 64 + 64 KB in the one-CTA kernel.
 //
+// The host runs this kernel for square shapes with d = 128 and no mask when
+// N > 2048 (below that the one-CTA kernel's staged O stores win).
+//
 // A work item is 512 query rows of one head.  CTA c of a pair holds Q tiles
 // t = 0, 1: rows row0 + (2t + c) * 128, so that pair tile t (the M = 256 rows
 // of one product) is the contiguous rows row0 + 256 t .. + 255.  Each CTA
@@ -57,7 +60,7 @@ struct alignas(1024) PairSmem {
   uint8_t kv[kPairStages][kHalfBytes];
   uint64_t q_full, q_empty;
   uint64_t kv_full[kPairStages], kv_empty[kPairStages];
-  uint64_t s_full[2], p_full[2], o_full[2], o_empty[2];
+  uint64_t s_full[2], p_half[2], p_full[2], o_full[2], o_empty[2];
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
@@ -65,7 +68,7 @@ struct alignas(1024) PairSmem {
 
 enum : int {
   kSitePQFull = 151, kSitePKvEmpty, kSitePKvFull, kSitePPFull, kSitePSFull, kSitePOFull,
-  kSitePQEmpty, kSitePOEmpty
+  kSitePQEmpty, kSitePOEmpty, kSitePPHalf
 };
 enum : int { kChkPItem = 1151, kChkPRow };
 
@@ -189,6 +192,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     for (int t = 0; t < 2; ++t) {
       mbar_init(&sm.s_full[t], 1);
       // the leader's own 128 threads plus one arrival per peer warp
+      mbar_init(&sm.p_half[t], 128 + 4);
       mbar_init(&sm.p_full[t], 128 + 4);
       mbar_init(&sm.o_full[t], 1);
       mbar_init(&sm.o_empty[t], 128 + 4);
@@ -307,15 +311,22 @@ __global__ void __launch_bounds__(kPairThreads, 1)
         }
         const uint64_t vd = desc_here(vdesc(smem_u32(sm.kv[vslot]), 0));
 #pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk)
+        for (int kk = 0; kk < kTile / 16; ++kk) {
+          if (kk == kTile / 32) {  // the second half of P (keys 64-127)
+            const bool r = mbar_wait(&sm.p_full[t], p_par[t], p.status, abortf, kSitePPFull);
+            p_par[t] ^= 1;
+            if (!r) return false;
+            tc_fence_after();
+          }
           mma_pair_ts(tmem + 256u + (uint32_t)t * kPD, tmem + (uint32_t)t * 128u + kk * 8,
                       desc_plus(vd, kk * 2048), id_pv, (accumulate || kk > 0) ? 1u : 0u);
+        }
         return true;
       };
+      // The first half of P_t (keys 0-63) in both CTAs; issue_pv waits for
+      // the second half itself.
       auto wait_p = [&](int t) -> bool {
-        const bool r = mbar_wait(&sm.p_full[t], p_par[t], p.status, abortf, kSitePPFull);
-        p_par[t] ^= 1;
-        return r;
+        return mbar_wait(&sm.p_half[t], p_par[t], p.status, abortf, kSitePPHalf);
       };
       for (int k = 0; ok && k * G < num_items; ++k) {
         const int idx = item_of_round(k);
@@ -378,6 +389,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     const uint32_t colO = tmem + lane_base + 256u + (uint32_t)t * kPD;
     // P ready / O read: the leader's threads arrive on their own barrier,
     // the peer's warps once each on the leader's.
+    const uint32_t lead_p_half = peer_addr(&sm.p_half[t], 0);
     const uint32_t lead_p_full = peer_addr(&sm.p_full[t], 0);
     const uint32_t lead_o_empty = peer_addr(&sm.o_empty[t], 0);
     auto signal = [&](uint64_t* own, uint32_t lead) {
@@ -410,7 +422,8 @@ __global__ void __launch_bounds__(kPairThreads, 1)
         s_par ^= 1;
         if (!ok) break;
         tc_fence_after();
-        softmax_tile<kPD, kNeg, false>(colS, colO, c2, tlim, j > 0, m_ref, l);
+        softmax_tile<kPD, kNeg, false>(colS, colO, c2, tlim, j > 0, m_ref, l,
+                                       [&] { signal(&sm.p_half[t], lead_p_half); });
         tc_fence_before();
         signal(&sm.p_full[t], lead_p_full);
       }

@@ -24,10 +24,15 @@ constexpr float kRescaleSlack = 8.0f;  // log2 units
 // c2 = scale * log2(e) (nonzero).  may_rescale: O holds earlier tiles'
 // products (false on the row's first key tile, whose O is overwritten).
 // The caller waits for S and fences before the call, and fences and signals
-// P's completion after it.  Warp-collective (TMEM loads and stores).
-template <int D, bool kNeg, bool kFp8>
+// P's completion after it.  bf16 P is published in two halves: once the
+// probabilities of keys 0-63 are in tensor memory, half_ready() is called,
+// so that the first half of O += P V can run while keys 64-127 are
+// exponentiated.  A warp that rescales O (rarely) calls it only after the
+// rescale, at the end.  Warp-collective (TMEM loads and stores).
+template <int D, bool kNeg, bool kFp8, class HalfReady>
 __device__ __forceinline__ void softmax_tile(uint32_t colS, uint32_t colO, float c2, int tlim,
-                                             bool may_rescale, float& m_ref, float& l) {
+                                             bool may_rescale, float& m_ref, float& l,
+                                             HalfReady&& half_ready) {
   // A masked score is replaced by the value that loses every max (min)
   // and whose exponent c2 * s is -inf, so its probability is exactly 0.
   const float neutral = kNeg ? __int_as_float(0x7f800000) : __int_as_float(0xff800000);
@@ -70,6 +75,9 @@ __device__ __forceinline__ void softmax_tile(uint32_t colS, uint32_t colO, float
     m_ref = m_tile;
   }
   l *= alpha;
+  // O must be rescaled if this row's reference moved (warp-wide decision:
+  // TMEM loads/stores are warp-collective).
+  const bool rescale = may_rescale && __any_sync(0xffffffffu, alpha != 1.f);
   // p = 2^(c2 * s - m) for pairs of scores with packed f32x2 FMAs (a
   // row that has seen no key yet keeps m = -inf and all p = 0); four
   // packed partial row sums, joined by a tree below.
@@ -106,7 +114,14 @@ __device__ __forceinline__ void softmax_tile(uint32_t colS, uint32_t colO, float
         }
       }
     }
-    if constexpr (!kFp8) tmem_st32(colS + h * 32, pk);
+    if constexpr (!kFp8) {
+      tmem_st32(colS + h * 32, pk);
+      if (h == 0 && !rescale) {
+        tmem_wait_st();
+        tc_fence_before();
+        half_ready();
+      }
+    }
   }
   if constexpr (kFp8) tmem_st32(colS, pk8);
   ls4[0] = f2_add(f2_add(ls4[0], ls4[1]), f2_add(ls4[2], ls4[3]));
@@ -114,9 +129,10 @@ __device__ __forceinline__ void softmax_tile(uint32_t colS, uint32_t colO, float
   f2_unpack(ls4[0], lsa, lsb);
   l += lsa + lsb;
   tmem_wait_st();
-  // Correct the O accumulator if this row's reference moved (warp-wide
-  // decision: TMEM loads/stores are warp-collective).
-  if (may_rescale && __any_sync(0xffffffffu, alpha != 1.f)) {
+  // Correct the O accumulator (S being complete means the previous P V
+  // product, which wrote O, is complete too); no product of this tile's P
+  // reads O before the warp's half_ready().
+  if (rescale) {
 #pragma unroll
     for (int c = 0; c < D / 32; ++c) {
       uint32_t orow[32];
@@ -127,6 +143,10 @@ __device__ __forceinline__ void softmax_tile(uint32_t colS, uint32_t colO, float
       tmem_st32(colO + c * 32, orow);
     }
     tmem_wait_st();
+    if constexpr (!kFp8) {
+      tc_fence_before();
+      half_ready();
+    }
   }
 }
 
