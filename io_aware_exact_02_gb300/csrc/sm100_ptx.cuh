@@ -202,6 +202,14 @@ __device__ __forceinline__ void bulk_wait_group0() {
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
+// 32-byte global store of eight words (sm_100+); `ptr` must be 32-byte
+// aligned.
+__device__ __forceinline__ void st_global_v8(void* ptr, const uint32_t* w) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(ptr), "r"(w[0]),
+               "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+               : "memory");
+}
+
 // Make generic-proxy writes to shared memory visible to the async proxy
 // (tensor-core operand reads, TMA).
 __device__ __forceinline__ void fence_proxy_async_smem() {

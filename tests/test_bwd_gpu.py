@@ -136,6 +136,30 @@ def test_bwd_many_items_per_cta_deterministic_and_phased(d):
     check((sel(a[0]), sel(a[1]), sel(a[2])), ref, "B4 H16 N2048 causal d=%d" % d)
 
 
+@pytest.mark.parametrize("d", [64, 128])
+def test_bwd_outputs_16_byte_aligned(d):
+    # dK and dV leave with 32-byte stores when their tensors are 32-byte
+    # aligned and with 16-byte stores otherwise: outputs at a 16-byte (but
+    # not 32-byte) offset give the same gradients bit for bit.
+    B, H, N = 2, 3, 640
+    q, k, v, do = synth.draw(B, H, N, d, seed=40 + d)
+    dev = torch.device("cuda")
+    q, k, v, do = (t.to(dev) for t in (q, k, v, do))
+    o, lse = fa.fwd(q, k, v)
+    a = fa.bwd(q, k, v, o, do, lse)
+    n = q.numel()
+    outs = []
+    for _ in range(3):
+        buf = torch.empty(n + 64, dtype=torch.bfloat16, device=dev)
+        base = (32 - buf.data_ptr() % 32) // 2  # elements to a 32-byte boundary
+        outs.append(buf[base + 8: base + 8 + n].view(B, H, N, d))  # 16 bytes past it
+    assert all(t.data_ptr() % 32 == 16 for t in outs)
+    b = fa.bwd(q, k, v, o, do, lse, dq=outs[0], dk=outs[1], dv=outs[2])
+    fa.check_device_status()
+    assert torch.equal(a[1], b[1]) and torch.equal(a[2], b[2])
+    assert (a[0].float() - b[0].float()).abs().max().item() < 1e-2
+
+
 def test_bwd_rejects_small_workspace():
     q, k, v, do = synth.draw(1, 1, 128, 64, seed=2)
     dev = torch.device("cuda")
