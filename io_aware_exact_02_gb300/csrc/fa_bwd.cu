@@ -218,36 +218,58 @@ __global__ void __launch_bounds__(256) fa_bwd_prep_kernel(const BwdParams p) {
       p.delta[ri] = -acc;
       p.lse2[ri] = row < p.N ? -(p.lse[(size_t)bh * p.N + row] * kLog2e) : __int_as_float(0xff800000);
     }
-    // Zero this row of the dQ accumulator: D floats, 4 per lane-slot.
-    for (int c4 = sub; c4 < D / 4; c4 += kLanesPerRow)
-      *reinterpret_cast<float4*>(p.dq_acc + dqacc_index<D>(bh, p.n_kv, row, c4)) =
-          make_float4(0.f, 0.f, 0.f, 0.f);
   }
+  // Zero the dQ accumulator (BH * npad * D floats, contiguous) with
+  // consecutive threads on consecutive 16-byte words.
+  const size_t n4 = (size_t)p.BH * npad * (D / 4);
+  float4* acc4 = reinterpret_cast<float4*>(p.dq_acc);
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4;
+       i += (size_t)gridDim.x * blockDim.x)
+    acc4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
 // ------------------------------------------------------------------ convert
 
+// One CTA per (head, 128-row tile, 64 columns): the accumulator's block of
+// [16 column groups][128 rows][4] floats is read with consecutive threads on
+// consecutive 16-byte words, turned into rows in shared memory (one word of
+// padding per row keeps eight consecutive rows on different banks), and
+// written out as rows of bf16, eight threads per 128-byte row segment.
+constexpr int kConvThreads = 256;
 template <int D>
-__global__ void __launch_bounds__(256) fa_bwd_convert_kernel(const BwdParams p) {
+__global__ void __launch_bounds__(kConvThreads) fa_bwd_convert_kernel(const BwdParams p) {
   wait_prior_grid();  // the main kernel's dQ reductions
-  // One thread per 8 output elements (one 16-byte store).
-  const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  const long long total = (long long)p.BH * p.N * (D / 8);
-  if (idx >= total) return;
-  const int c8 = (int)(idx % (D / 8));
-  const long long rg = idx / (D / 8);
-  const int bh = (int)(rg / p.N), row = (int)(rg % p.N);
+  constexpr int kGroups = 16;  // float4 column groups per CTA (64 columns)
+  constexpr int kHalves = D / 64;
+  __shared__ float4 buf[kTile][kGroups + 1];
+  const int half = blockIdx.x % kHalves;
+  const int tile = (blockIdx.x / kHalves) % p.n_kv;
+  const int bh = blockIdx.x / kHalves / p.n_kv;
   int no_abort = 0;
-  if (!bound_ok(bh < p.BH && row < p.N, p.status, &no_abort, kChkConvRow)) return;
-  const float4 a = *reinterpret_cast<const float4*>(p.dq_acc + dqacc_index<D>(bh, p.n_kv, row, 2 * c8));
-  const float4 b = *reinterpret_cast<const float4*>(p.dq_acc + dqacc_index<D>(bh, p.n_kv, row, 2 * c8 + 1));
-  uint4 out;
-  out.x = pack_bf16x2(a.x * p.scale, a.y * p.scale);
-  out.y = pack_bf16x2(a.z * p.scale, a.w * p.scale);
-  out.z = pack_bf16x2(b.x * p.scale, b.y * p.scale);
-  out.w = pack_bf16x2(b.z * p.scale, b.w * p.scale);
-  *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.dq) + ((size_t)bh * p.N + row) * D +
-                            c8 * 8) = out;
+  if (!bound_ok(bh < p.BH, p.status, &no_abort, kChkConvRow)) return;
+  const float4* src = reinterpret_cast<const float4*>(
+      p.dq_acc + dqacc_index<D>(bh, p.n_kv, tile * kTile, half * kGroups));
+#pragma unroll
+  for (int k = 0; k < kTile * kGroups / kConvThreads; ++k) {
+    const int idx = threadIdx.x + k * kConvThreads;  // = group * 128 + row
+    buf[idx % kTile][idx / kTile] = src[idx];
+  }
+  __syncthreads();
+#pragma unroll
+  for (int k = 0; k < kTile * 8 / kConvThreads; ++k) {
+    const int idx = threadIdx.x + k * kConvThreads;
+    const int r = idx / 8, q = idx % 8;  // row, 8-column chunk
+    const int row = tile * kTile + r;
+    if (row >= p.N) continue;
+    const float4 a = buf[r][2 * q], b = buf[r][2 * q + 1];
+    uint4 out;
+    out.x = pack_bf16x2(a.x * p.scale, a.y * p.scale);
+    out.y = pack_bf16x2(a.z * p.scale, a.w * p.scale);
+    out.z = pack_bf16x2(b.x * p.scale, b.y * p.scale);
+    out.w = pack_bf16x2(b.z * p.scale, b.w * p.scale);
+    *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.dq) +
+                              ((size_t)bh * p.N + row) * D + half * 64 + q * 8) = out;
+  }
 }
 
 // ------------------------------------------------------------------ main
@@ -932,8 +954,8 @@ int launch_bwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap
   }
   // 3. convert
   if (mask & 4) {
-    const long long total = (long long)p.BH * p.N * (D / 8);
-    const cudaLaunchConfig_t c = config((unsigned)((total + 255) / 256), 256, 0);
+    const long long blocks = (long long)p.BH * p.n_kv * (D / 64);
+    const cudaLaunchConfig_t c = config((unsigned)blocks, kConvThreads, 0);
     if (cudaLaunchKernelEx(&c, fa_bwd_convert_kernel<D>, p) != cudaSuccess) {
       cudaGetLastError();
       return FA_ERR_LAUNCH;
