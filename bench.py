@@ -1031,8 +1031,8 @@ def main(argv=None):
                     help="skip the d=128 N sweep (1K, 2K, 4K, 16K) reported beside the headline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--fwd-kernel", choices=["auto", "pair", "one"], default="auto",
-                    help="non-causal d=128 forward kernel: the library's choice (CTA pairs for "
-                         "N > 2048), or forced CTA pairs / one CTA per item (FA_FWD_PAIR)")
+                    help="non-causal d=128 forward kernel: the library's choice (one CTA per "
+                         "item), or forced CTA pairs / one CTA per item (FA_FWD_PAIR)")
     args = ap.parse_args(argv)
     if args.fwd_kernel != "auto":  # read by the library on its first forward call
         os.environ["FA_FWD_PAIR"] = "1" if args.fwd_kernel == "pair" else "0"

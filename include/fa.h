@@ -77,12 +77,10 @@ extern "C" {
  *             or negative).
  * Passes: cs2680 Lecture 9 sec. 9.4 (online softmax, running max m and
  * denominator l, correction by exp(m - m_new)); CMU post slide page 12.
- * Kernels: non-causal d = 128 with N > 2048 runs on CTA pairs (tcgen05
- * cta_group::2, the 2-CTA products of the CMU post's slide pages 50-52);
- * everything else on one CTA per work item.  Both give bitwise the same
- * results.  The environment variable FA_FWD_PAIR=1 (or 0), read once per
- * process, forces the pair (or the one-CTA) kernel for every non-causal
- * d = 128 call.
+ * Kernels: one CTA per work item by default.  With the environment
+ * variable FA_FWD_PAIR=1 (read once per process), non-causal d = 128 calls
+ * run on CTA pairs instead (tcgen05 cta_group::2, the 2-CTA products of the
+ * CMU post's slide pages 50-52); both give bitwise the same results.
  */
 int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
            int N, int d, int causal, float scale, void* stream);

@@ -329,13 +329,13 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
   // the persistent grid serves them.
   const bool uneven = block_mask != nullptr || (causal && Nq > 16);
   p.grid = fwd_grid(g.BH, g.n_pairs * g.splits, uneven, ds->sm_count);
-  // Square, d = 128, no mask, N > 2048: the CTA-pair kernel (tcgen05
-  // cta_group::2), whose products read half the shared memory per CTA.
-  // Measured at B8 H16 (TFLOP/s, pair / one CTA): N = 1K 950 / 1007, 2K
-  // 1469 / 1470, 4K 1666 / 1564, 8K 1753 / 1663, 16K 1689 / 1631; below 4K
-  // the one-CTA kernel's staged O stores win.  FA_FWD_PAIR=1 (or 0) in the
-  // environment forces the pair (or the one-CTA) kernel wherever the pair
-  // kernel applies; the library reads it once.
+  // Square, d = 128, no mask: the CTA-pair kernel (tcgen05 cta_group::2),
+  // whose products read half the shared memory per CTA, runs only when
+  // FA_FWD_PAIR=1 is in the environment (0 or unset: the one-CTA kernel;
+  // the library reads it once).  It was the faster one at N > 2K (B8 H16,
+  // TFLOP/s, pair / one CTA: 4K 1666 / 1564, 8K 1753 / 1663) until the
+  // one-CTA kernel's epilogue moved to its own warpgroup (then, on one box:
+  // 4K 1655 / 1697, 8K 1635 / 1712, 16K 1632 / 1664).
   static const int pair_mode = [] {
     const char* e = std::getenv("FA_FWD_PAIR");
     if (e != nullptr && (e[0] == '0' || e[0] == '1') && e[1] == 0) return e[0] - '0';
@@ -343,7 +343,7 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
   }();
   const bool pair_shape = d == 128 && !causal && block_mask == nullptr && g.splits == 1 &&
                           Hq == Hkv && Nq == Nkv;
-  if (pair_shape && (pair_mode == 1 || (pair_mode == -1 && Nkv > 2048))) {
+  if (pair_shape && pair_mode == 1) {
     CUtensorMap tkh;
     if ((rc = make_tmap_bhnd_rows(k, g.BH, Nkv, d, 64, &tkh)) != FA_OK) return rc;
     if (p.scale_log2 == 0.f) p.scale_log2 = 1.17549435e-38f;  // as launch_fwd does

@@ -54,11 +54,29 @@ struct FwdCfg {
   // warpgroup that gives registers up (setmaxnreg) to the two softmax
   // warpgroups; the split uses the launch's 384 x 168 registers exactly.
   static constexpr bool kRealloc = D == 64 && !kFp8;
-  static constexpr int threads(bool stage) { return kRealloc ? 384 : (stage ? 352 : 320); }
+  // kEpi (d = 128, O staged): a third warpgroup takes each finished O tile
+  // out of tensor memory, normalises it and stages it for the store, so
+  // that the softmax warpgroups go straight on to the next item's first key
+  // tile instead of spending the epilogue at every item boundary.  Sixteen
+  // warps: softmax 0-7, epilogue 8-11, producer, MMA, store and one idle
+  // warp 12-15; the registers of the launch (512 x 128) are split
+  // 184 / 80 / 56.  (At d = 64 it measured no faster than the twelve-warp
+  // split: 1097 against 1093 TFLOP/s at N = 8K, 693 against 712 for
+  // B16 H12 N1K.)
+  static constexpr bool epi(bool stage) { return stage && D == 128 && !kFp8; }
+  static constexpr bool realloc(bool stage) { return kRealloc && !epi(stage); }
+  static constexpr int threads(bool stage) {
+    return epi(stage) ? 512 : (kRealloc ? 384 : (stage ? 352 : 320));
+  }
   static constexpr int kRegsLaunch = 168;
   static constexpr int kRegsCtl = 72;
   static constexpr int kRegsSoftmax = 216;
   static_assert(!kRealloc || 2 * 128 * kRegsSoftmax + 128 * kRegsCtl <= 384 * kRegsLaunch,
+                "register split above the launch's total");
+  static constexpr int kEpiRegsLaunch = 128, kEpiRegsSoftmax = 184, kEpiRegsEpi = 80,
+                       kEpiRegsCtl = 56;
+  static_assert(2 * 128 * kEpiRegsSoftmax + 128 * kEpiRegsEpi + 128 * kEpiRegsCtl <=
+                    512 * kEpiRegsLaunch,
                 "register split above the launch's total");
   static constexpr uint32_t kTmemCols = 512;
   // TMEM column of S/P and of O for Q tile t.
@@ -88,6 +106,9 @@ struct alignas(1024) FwdSmem {
   uint64_t staged[2];   // softmax t has written O_t into its ring slot for the store
   uint64_t stored[2];   // the store warp has read softmax t's staged O_t
   uint64_t stage_ready[2];  // softmax t's staging slot of the item is free
+  uint64_t ml_full[2];      // kEpi: softmax t has published its rows' 1 / l
+  uint64_t ml_empty[2];     // kEpi: the epilogue has read them
+  float inv_l[2][kTile];    // kEpi: 1 / l per row of each Q tile (0: no key seen)
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
@@ -96,7 +117,8 @@ struct alignas(1024) FwdSmem {
 // Wait sites reported through the status word.
 enum : int {
   kSiteQFull = 101, kSiteKvEmpty, kSiteKvFull, kSitePFull, kSiteSFull, kSiteOFull, kSiteDrain,
-  kSiteQEmpty, kSiteOEmpty, kSiteStageSlot, kSiteStaged, kSiteStored, kSitePHalf
+  kSiteQEmpty, kSiteOEmpty, kSiteStageSlot, kSiteStaged, kSiteStored, kSitePHalf, kSiteMlFull,
+  kSiteMlEmpty
 };
 // Bounds checks of the checked build (FA_CHECKS).
 enum : int {
@@ -154,6 +176,11 @@ __global__ void __launch_bounds__(FwdCfg<D, kFp8>::threads(kStage), 1)
   volatile int* abortf = &sm.abort_flag;
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
+  constexpr bool kEpi = Cfg::epi(kStage);
+  constexpr bool kRe = Cfg::realloc(kStage);
+  // Warp roles: softmax 0-7, then (kEpi) the epilogue warpgroup 8-11, then
+  // the producer, the MMA issuer and the O store warp.
+  constexpr int kWarpLoad = kEpi ? 12 : 8, kWarpMma = kWarpLoad + 1, kWarpStore = kWarpLoad + 2;
 
   if (tid == 0) {
     mbar_init(&sm.q_full, 1);
@@ -171,12 +198,14 @@ __global__ void __launch_bounds__(FwdCfg<D, kFp8>::threads(kStage), 1)
       mbar_init(&sm.staged[t], 128);
       mbar_init(&sm.stored[t], 1);
       mbar_init(&sm.stage_ready[t], 1);
+      mbar_init(&sm.ml_full[t], 128);
+      mbar_init(&sm.ml_empty[t], 128);
     }
     mbar_init(&sm.drain, 1);
     sm.abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 9) {
+  if (warp == kWarpMma) {
     tmem_alloc(&sm.tmem_base, Cfg::kTmemCols);
     tmem_relinquish();
   }
@@ -273,9 +302,92 @@ __global__ void __launch_bounds__(FwdCfg<D, kFp8>::threads(kStage), 1)
     return bound_ok(in, p.status, abortf, kChkItem);
   };
 
-  if (warp == 8) {
+  // kEpi: warps 8-11 (thread r of the warpgroup owns row r of both Q tiles'
+  // O accumulators) take each O tile once the MMA thread has committed its
+  // last product and the softmax warpgroup has published the rows' 1 / l:
+  // O / l as bf16 into the tile's staging slot of the ring (or, for an item
+  // without keys, zeros straight to memory), o_empty as soon as the tensor
+  // memory reads are done, staged for the store warp.
+  auto epilogue_role = [&] {
+    const int r = tid & 127;
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    int n_done = 0, cb = 0, n_staged = 0;
+    bool ok = true;
+    for (int k = 0; ok && k * G < num_items; ++k) {
+      const int idx = item_of_round(k);
+      if (idx >= num_items) continue;
+      const Item item = decode(idx);
+      if (!warp_bound_ok(item_ok(item), p.status, abortf, kChkItem)) {
+        ok = false;
+        break;
+      }
+      const bool staged = item.nmax > 0;
+      const int cb_item = cb;
+      if (item.nmax > 0) cb += 2 * item.nmax + ring_per_item_extra;
+      for (int t = 0; t < 2 && ok; ++t) {
+        const uint32_t colO = tmem + lane_base + Cfg::col_o(t);
+        const int R = item.row0 + t * kTile + r;
+        const bool valid = R < p.rows;
+        const size_t row_g = (size_t)item.bh * p.rows + R;
+        ok = mbar_wait(&sm.o_full[t], n_done & 1, p.status, abortf, kSiteOFull);
+        if (ok) ok = mbar_wait(&sm.ml_full[t], n_done & 1, p.status, abortf, kSiteMlFull);
+        if (ok) ok = warp_bound_ok(!valid || (R >= 0 && row_g < (size_t)p.BH * p.rows), p.status,
+                                   abortf, kChkRow);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        tc_fence_after();
+        const float inv_l = sm.inv_l[t][r];
+        mbar_arrive(&sm.ml_empty[t]);
+        const bool any = inv_l != 0.f;  // 1 / l of a row that saw a key is positive
+        if (staged) {
+          const int slot = (cb_item + 2 * item.nmax + t) % S;
+          ok = mbar_wait(&sm.stage_ready[t], n_staged & 1, p.status, abortf, kSiteStageSlot);
+          ok = __all_sync(0xffffffffu, ok);
+          if (!ok) break;
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t orow[32];
+            tmem_ld32(colO + c * 32, orow);
+            tmem_wait_ld(orow);
+            if (c == D / 32 - 1) {
+              // O_t may now be overwritten by the next item's first product.
+              tc_fence_before();
+              mbar_arrive(&sm.o_empty[t]);
+            }
+            uint8_t* rowp = sm.kv[slot] + (c / 2) * 16384 + r * 128;
+            uint32_t w[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              w[i] = any ? pack_bf16x2(__uint_as_float(orow[2 * i]) * inv_l,
+                                       __uint_as_float(orow[2 * i + 1]) * inv_l)
+                         : 0u;
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              *reinterpret_cast<uint4*>(rowp + ((((c % 2) * 4 + e) ^ (r & 7)) << 4)) =
+                  make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+          }
+          fence_proxy_async_smem();
+          mbar_arrive(&sm.staged[t]);
+        } else {
+          // No key for any row of the item: O = 0.
+          tc_fence_before();
+          mbar_arrive(&sm.o_empty[t]);
+          if (valid) {
+            uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.o) + row_g * D);
+#pragma unroll
+            for (int i = 0; i < D / 8; ++i) dst[i] = make_uint4(0u, 0u, 0u, 0u);
+          }
+        }
+      }
+      if (staged) ++n_staged;
+      ++n_done;
+    }
+  };
+
+  if (warp == kWarpLoad) {
     // ------------------------------------------------------------ producer
-    if constexpr (Cfg::kRealloc) setmaxnreg_dec<Cfg::kRegsCtl>();
+    if constexpr (kRe) setmaxnreg_dec<Cfg::kRegsCtl>();
+    if constexpr (kEpi) setmaxnreg_dec<Cfg::kEpiRegsCtl>();
     if (lane_id() == 0) {
       prefetch_tmap(&tq);
       prefetch_tmap(&tk);
@@ -383,9 +495,10 @@ __global__ void __launch_bounds__(FwdCfg<D, kFp8>::threads(kStage), 1)
       }
     }
     __syncwarp();
-  } else if (warp == 9) {
+  } else if (warp == kWarpMma) {
     // ------------------------------------------------------------ MMA issuer
-    if constexpr (Cfg::kRealloc) setmaxnreg_dec<Cfg::kRegsCtl>();
+    if constexpr (kRe) setmaxnreg_dec<Cfg::kRegsCtl>();
+    if constexpr (kEpi) setmaxnreg_dec<Cfg::kEpiRegsCtl>();
     if (lane_id() == 0) {
       const uint32_t id_s = kFp8 ? idesc_e4m3(128, 128) : idesc_bf16(128, 128, false, false);
       const uint32_t id_pv = kFp8 ? idesc_e4m3(128, D) : idesc_bf16(128, D, false, true);
@@ -607,9 +720,10 @@ __global__ void __launch_bounds__(FwdCfg<D, kFp8>::threads(kStage), 1)
       drain_wait(&sm.drain, 0);
     }
     __syncwarp();
-  } else if (warp == 10) {
+  } else if (warp == kWarpStore) {
     // ------------------------------------------------------------ O store warp
-    if constexpr (Cfg::kRealloc) setmaxnreg_dec<Cfg::kRegsCtl>();
+    if constexpr (kRe) setmaxnreg_dec<Cfg::kRegsCtl>();
+    if constexpr (kEpi) setmaxnreg_dec<Cfg::kEpiRegsCtl>();
     // Sends each staged O tile out with TMA stores (rows past the tensor's
     // end are not written) and releases its ring slot once the stores have
     // read it.
@@ -646,12 +760,20 @@ __global__ void __launch_bounds__(FwdCfg<D, kFp8>::threads(kStage), 1)
       bulk_wait_group0();
     }
     __syncwarp();
-  } else if (Cfg::kRealloc && warp == 11) {
+  } else if ((kRe && warp == 11) || (kEpi && warp == 15)) {
     // Idle: its registers go to the softmax warpgroups.
-    if constexpr (Cfg::kRealloc) setmaxnreg_dec<Cfg::kRegsCtl>();
+    if constexpr (kRe) setmaxnreg_dec<Cfg::kRegsCtl>();
+    if constexpr (kEpi) setmaxnreg_dec<Cfg::kEpiRegsCtl>();
+  } else if (kEpi && warp >= 8) {
+    // ------------------------------------------------------------ epilogue
+    if constexpr (kEpi) {
+      setmaxnreg_dec<Cfg::kEpiRegsEpi>();
+      epilogue_role();
+    }
   } else if (warp < 8) {
     // ------------------------------------------------------------ softmax
-    if constexpr (Cfg::kRealloc) setmaxnreg_inc<Cfg::kRegsSoftmax>();
+    if constexpr (kRe) setmaxnreg_inc<Cfg::kRegsSoftmax>();
+    if constexpr (kEpi) setmaxnreg_inc<Cfg::kEpiRegsSoftmax>();
     const int t = warp >> 2;             // which Q tile
     const int r = tid & 127;             // row within the tile
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
@@ -718,6 +840,24 @@ __global__ void __launch_bounds__(FwdCfg<D, kFp8>::threads(kStage), 1)
                                     [&] { mbar_arrive(&sm.p_half[t]); });
         tc_fence_before();
         mbar_arrive(&sm.p_full[t]);
+      }
+      if constexpr (kEpi) {
+        // The epilogue warpgroup takes O; this warpgroup writes lse and
+        // hands over 1 / l (0 for a row that saw no key).
+        const bool any = l > 0.f;
+        const bool valid = R < p.rows;
+        const size_t row_g = (size_t)bh * p.rows + R;
+        if (ok && n_done > 0)
+          ok = mbar_wait(&sm.ml_empty[t], (n_done - 1) & 1, p.status, abortf, kSiteMlEmpty);
+        if (ok) ok = warp_bound_ok(!valid || (R >= 0 && row_g < (size_t)p.BH * p.rows), p.status,
+                                   abortf, kChkRow);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        if (valid) p.lse[row_g] = any ? (m_ref + __log2f(l)) * kLn2 : ninf;
+        sm.inv_l[t][r] = any ? o_mul / l : 0.f;
+        mbar_arrive(&sm.ml_full[t]);
+        ++n_done;
+        continue;
       }
       if (ok) ok = mbar_wait(&sm.o_full[t], n_done & 1, p.status, abortf, kSiteOFull);
       ok = __all_sync(0xffffffffu, ok);
@@ -815,7 +955,7 @@ __global__ void __launch_bounds__(FwdCfg<D, kFp8>::threads(kStage), 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == kWarpMma) {
     tc_fence_after();
     tmem_dealloc(tmem, Cfg::kTmemCols);
   }
@@ -911,14 +1051,15 @@ int launch_fwd_dn(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMa
   if (cudaFuncSetAttribute(fa_fwd_kernel<D, kNeg, kGeneral, kSparse, kFp8, kStage>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return FA_ERR_LAUNCH;
-  if constexpr (FwdCfg<D, kFp8>::kRealloc) {
+  if constexpr (FwdCfg<D, kFp8>::realloc(kStage) || FwdCfg<D, kFp8>::epi(kStage)) {
     // The softmax warpgroups' setmaxnreg.inc waits for the registers the
-    // third warpgroup releases, which suffice only at the launch register
+    // other warpgroups release, which suffice only at the launch register
     // count the split assumes: refuse to launch otherwise.
     cudaFuncAttributes attr;
     if (cudaFuncGetAttributes(&attr, fa_fwd_kernel<D, kNeg, kGeneral, kSparse, kFp8, kStage>) !=
             cudaSuccess ||
-        attr.numRegs < FwdCfg<D, kFp8>::kRegsLaunch)
+        attr.numRegs < (FwdCfg<D, kFp8>::epi(kStage) ? FwdCfg<D, kFp8>::kEpiRegsLaunch
+                                                     : FwdCfg<D, kFp8>::kRegsLaunch))
       return FA_ERR_LAUNCH;
   }
   // Launched with programmatic stream serialization: the kernel's launch
@@ -974,10 +1115,10 @@ int launch_fwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap
     if (p.scale_log2 < 0.f) return launch_fwd_dn<D, true, true>(tq, tk, tv, to, p, stream);
     return launch_fwd_dn<D, false, true>(tq, tk, tv, to, p, stream);
   }
-  // Staged O stores pay where items are short (N <= 2K at d = 128) and, at
-  // d = 64, at every length; they need persistent CTAs (no mask).
+  // Staged O stores (at d = 128 with the epilogue warpgroup) pay at every
+  // length; they need persistent CTAs (no mask, more items than CTAs).
   const long long items = (long long)p.BH * p.n_pairs;
-  if (p.grid < items && (D == 64 || p.n_kv <= 16)) {
+  if (p.grid < items) {
     if (p.scale_log2 < 0.f)
       return launch_fwd_dn<D, true, false, false, false, true>(tq, tk, tv, to, p, stream);
     return launch_fwd_dn<D, false, false, false, false, true>(tq, tk, tv, to, p, stream);

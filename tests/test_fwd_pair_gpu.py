@@ -1,6 +1,6 @@
 """The forward pass's two kernels for non-causal d = 128: the CTA-pair kernel
-(tcgen05 cta_group::2; the default for N > 2048) and the one-CTA kernel,
-each forced for every size by FA_FWD_PAIR=1 / 0 in a child process (the
+(tcgen05 cta_group::2; opt-in) and the one-CTA kernel (the default), each
+forced for every size by FA_FWD_PAIR=1 / 0 in a child process (the
 library reads the switch once per process).  Both must agree bit for bit
 (they share the softmax code and the products' summation order), and with
 the fp64 oracle on the cases small enough for it.
@@ -27,7 +27,7 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 # (B, H, N, scale, seed): ragged N inside one 512-row item and across
 # several, a row count that leaves a CTA of the pair without valid rows,
 # negative and zero scales, several items per pair, and sizes on both sides
-# of the default switch (N = 2048).
+# of N = 2048.
 CASES = [
     (1, 1, 1, None, 1),
     (1, 2, 129, None, 2),
