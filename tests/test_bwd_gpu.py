@@ -183,8 +183,10 @@ def test_bwd_full_size_sampled_heads(name):
     dq, dk, dv = run(q, k, v, do, w.causal, w.softmax_scale)
     BH = w.BH
     rng = np.random.default_rng(1)
-    heads = sorted(set([BH - 1] + rng.choice(BH, size=FULL_BWD[name], replace=False).tolist()))[
-        : FULL_BWD[name]]
+    # The last head (whose items are the work list's last, claimed by CTAs
+    # that have been through every earlier item) and random others.
+    others = [h for h in rng.permutation(BH - 1).tolist()][: FULL_BWD[name] - 1]
+    heads = sorted(set([BH - 1] + others))
 
     def sel(t):
         return t.reshape(BH, w.N, w.d)[heads].unsqueeze(0)

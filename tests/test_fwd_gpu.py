@@ -135,12 +135,28 @@ def test_fwd_bad_arguments_raise():
 FULL = [w.name for w in synth.ALL if w.name != "tiny"]
 
 
-def sampled_check(w, o_dev, lse_dev, q, k, v, n_heads=3, n_rows=48, seed=0):
+def late_items(w, n=2):
+    """(head, first row) of the last n items of the forward's work list on
+    this GPU's persistent grid: the items a CTA reaches last, after its
+    barriers, rings and tensor memory have gone through every earlier
+    item's phases."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    sched = fa.fwd_schedule(w.B, w.H, w.N, w.causal, num_ctas=sms)
+    return [(bh, pair * 256) for bh, pair, _, _ in sched[-n:]]
+
+
+def sampled_check(w, o_dev, lse_dev, q, k, v, n_heads=3, n_rows=48, seed=0, extra=()):
+    """Oracle rows of a few heads: random ones, the last head, and the heads
+    of `extra` (head, first row) items with rows from those items' 256."""
     rng = np.random.default_rng(seed)
     BH = w.B * w.H
-    heads = sorted(set(rng.choice(BH, size=min(n_heads, BH), replace=False).tolist()) | {BH - 1})
+    heads = sorted(set(rng.choice(BH, size=min(n_heads, BH), replace=False).tolist()) | {BH - 1}
+                   | {bh for bh, _ in extra})
+    late_rows = [r0 + rng.choice(min(256, w.N - r0), size=min(6, w.N - r0), replace=False)
+                 for _, r0 in extra if r0 < w.N]
     rows = np.unique(np.concatenate([rng.choice(w.N, size=n_rows, replace=False),
-                                     [0, w.N - 1, min(w.N - 1, 128), min(w.N - 1, 255)]]))
+                                     [0, w.N - 1, min(w.N - 1, 128), min(w.N - 1, 255)]] +
+                                    late_rows))
     qf = q.reshape(BH, w.N, w.d)[heads].unsqueeze(0)
     kf = k.reshape(BH, w.N, w.d)[heads].unsqueeze(0)
     vf = v.reshape(BH, w.N, w.d)[heads].unsqueeze(0)
@@ -160,7 +176,7 @@ def test_fwd_full_size_sampled(name):
     o, lse = fa.fwd(q.to(dev), k.to(dev), v.to(dev), causal=w.causal, scale=w.softmax_scale)
     fa.check_device_status()
     assert torch.isfinite(lse).all()
-    sampled_check(w, o, lse, q, k, v)
+    sampled_check(w, o, lse, q, k, v, extra=late_items(w))
 
 
 @pytest.mark.parametrize("N,d", [(1000, 128), (1920, 128), (3000, 64), (257, 64)])
