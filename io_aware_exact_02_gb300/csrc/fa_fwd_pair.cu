@@ -18,7 +18,8 @@
 // 128 + 64 + 64 KB in the one-CTA kernel.
 //
 // The host runs this kernel for square shapes with d = 128 and no mask when
-// N > 2048 (below that the one-CTA kernel's staged O stores win).
+// FA_FWD_PAIR=1 is in the environment: the one-CTA kernel, whose epilogue
+// runs in its own warpgroup, measured faster at every length.
 //
 // A work item is 512 query rows of one head.  CTA c of a pair holds Q tiles
 // t = 0, 1: rows row0 + (2t + c) * 128, so that pair tile t (the M = 256 rows
