@@ -179,12 +179,15 @@ def test_fwd_full_size_sampled(name):
     sampled_check(w, o, lse, q, k, v, extra=late_items(w))
 
 
-@pytest.mark.parametrize("N,d", [(1000, 128), (1920, 128), (3000, 64), (257, 64)])
+@pytest.mark.parametrize("N,d", [(1000, 128), (1920, 128), (3000, 64), (257, 64), (100, 128),
+                                 (129, 128), (300, 128), (64, 64)])
 def test_fwd_staged_stores_ragged(N, d):
-    # Non-causal grids with more items than SMs, at d = 64 or N <= 2K, store
-    # O through the staging ring slots with TMA; the tail tile of every head
-    # is partly past N (rows there must not be written).  Sampled rows of the
-    # first, last and random heads, including each head's last rows.
+    # Non-causal grids with more items than SMs store O through the staging
+    # ring slots with TMA (at d = 128 from the epilogue warpgroup); the tail
+    # tile of every head is partly past N (rows there must not be written),
+    # and at N <= 128 every item's second Q tile has no rows at all.
+    # Sampled rows of the first, last and random heads, including each
+    # head's last rows.
     from io_aware_exact_02_gb300.synth import Workload
     w = Workload("staged_N%d_d%d" % (N, d), 8, 24, N, d, False)
     q, k, v, _ = synth.draw_workload(w, seed=N + d, with_dout=False)
