@@ -316,13 +316,24 @@ const char* fa_status_string(int status);
  * first (the LPT rule of the CMU post's slide pages 27-46: under a causal
  * mask later query tiles see more keys).  Without a mask the kernel runs
  * min(items, num_ctas) persistent CTAs (num_ctas = the device's SM count)
- * and CTA c takes the list in snake order (fa_snake_assign); under a causal
- * mask every item gets its own CTA and the hardware dispatches them in list
- * order as SMs free up (greedy list scheduling).  Writes up to max_items
- * entries of item_bh, item_pair, item_cost (the item's number of 128-key
- * tiles summed over its two query tiles) and item_cta (any of them may be
- * NULL) and returns the number of items, or a negative FA_ERR_* code.
- * Host only; needs no device.
+ * and CTA c takes the list in snake order (fa_snake_assign).  Under a causal
+ * mask (and under a block mask) items differ in cost and are taken greedily
+ * in list order (greedy list scheduling): with more items than num_ctas,
+ * num_ctas persistent CTAs claim them from a device work counter as each
+ * becomes ready for another, so item_cta is -1 (decided at run time);
+ * otherwise item t gets CTA t.  The counter is the library's: one slot per
+ * stream, so launches on one stream (which run in order) share it and
+ * launches on different streams do not; a launch leaves its slot as it
+ * found it.  A CUDA graph that holds a masked forward pass uses the slot of
+ * the stream it was captured on: it must not run at the same time as
+ * another masked forward pass on that stream, nor twice at once.  After
+ * 64 streams on a device have run masked forward passes, calls on further
+ * streams give every item its own CTA instead (the hardware then hands CTAs
+ * to SMs in list order as SMs free up).  Writes up to max_items entries of
+ * item_bh, item_pair, item_cost (the item's number of 128-key tiles summed
+ * over its two query tiles) and item_cta (any of them may be NULL) and
+ * returns the number of items, or a negative FA_ERR_* code.  Host only;
+ * needs no device.
  */
 int fa_fwd_schedule(int B, int H, int N, int causal, int num_ctas, int* item_bh,
                     int* item_pair, int* item_cost, int* item_cta, int max_items);

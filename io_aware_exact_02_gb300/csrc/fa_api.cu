@@ -18,6 +18,10 @@ namespace fa {
 // The status word: [0] = first error code a kernel recorded, [1] = the wait
 // site that raised it.  One per device, part of the module's static data.
 __device__ int g_status[2];
+// The forward's work counters for dynamic item claiming, one 128-byte slot
+// per stream (FwdParams::sched); zero at load, and each launch leaves its
+// slot at zero.
+__device__ int g_fwd_sched[kFwdSchedSlots * kFwdSchedStride];
 
 namespace {
 
@@ -29,6 +33,9 @@ struct DeviceState {
   int* status = nullptr;  // device address of g_status
   int sm_count = 0;
   int pair_max = 0;       // forward CTA pairs resident at once (0: not yet known)
+  int* fwd_sched = nullptr;                  // device address of g_fwd_sched
+  cudaStream_t sched_stream[kFwdSchedSlots];  // the stream each slot serves
+  int sched_used = 0;
 };
 
 std::mutex g_mu;
@@ -65,12 +72,44 @@ int device_state(DeviceState** out) {
         return FA_ERR_DEVICE;
       }
       s.status = static_cast<int*>(addr);
+      if (cudaGetSymbolAddress(&addr, g_fwd_sched) != cudaSuccess) {
+        cudaGetLastError();
+        return FA_ERR_DEVICE;
+      }
+      s.fwd_sched = static_cast<int*>(addr);
     }
     s.checked = true;
   }
   if (!s.supported) return FA_ERR_DEVICE;
   *out = &s;
   return FA_OK;
+}
+
+// The forward's grid and work counter.  Items of equal cost (no mask) or
+// no more items than SMs: the static grid of fwd_grid.  Uneven items (a
+// causal or block mask) on more items than SMs: one persistent CTA per SM
+// claiming items from the stream's counter slot (bf16 kernels; the FP8
+// kernel gives every item its own CTA).  Launches on one stream run in
+// order, so one slot per stream is never used by two launches at once; a
+// launch leaves its slot at zero.  When every slot is taken (more than
+// kFwdSchedSlots streams have run masked forward passes on the device)
+// the call falls back to one CTA per item.
+void set_fwd_grid(FwdParams* p, DeviceState* ds, long long items, bool uneven, bool claim,
+                  cudaStream_t stream) {
+  p->sched = nullptr;
+  p->grid = fwd_grid(1, (int)items, uneven ? 1 : 0, ds->sm_count);
+  if (!uneven || !claim || items <= ds->sm_count) return;
+  std::lock_guard<std::mutex> lk(g_mu);
+  int slot = -1;
+  for (int i = 0; i < ds->sched_used; ++i)
+    if (ds->sched_stream[i] == stream) slot = i;
+  if (slot < 0 && ds->sched_used < kFwdSchedSlots) {
+    slot = ds->sched_used++;
+    ds->sched_stream[slot] = stream;
+  }
+  if (slot < 0) return;
+  p->sched = ds->fwd_sched + slot * kFwdSchedStride;
+  p->grid = ds->sm_count;
 }
 
 int get_encode(PFN_cuTensorMapEncodeTiled_v12000* fn) {
@@ -258,7 +297,8 @@ int fwd_fp8_quantized_impl(void* o, float* lse, int B, int H, int N, int d, int 
   p.tiles_per_split = p.n_kv;
   p.causal = causal;
   p.scale_log2 = scale * 1.4426950408889634f;
-  p.grid = fwd_grid(BH, p.n_pairs, causal, ds->sm_count);
+  set_fwd_grid(&p, ds, (long long)BH * p.n_pairs, causal != 0, false,
+               static_cast<cudaStream_t>(stream));
   return launch_fwd(tq, tk, tv, tq, p, d, static_cast<cudaStream_t>(stream));  // O stored directly
 }
 
@@ -323,12 +363,13 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
   p.tiles_per_split = g.tiles_per_split;
   p.causal = causal;
   p.scale_log2 = scale * 1.4426950408889634f;
-  // Block-sparse items differ in cost like causal ones: one CTA per item.
-  // Under the bottom-right causal mask, items cost the same when the query
-  // rows are few (decode, N_q <= 16: every row sees about all keys), and
-  // the persistent grid serves them.
+  // Block-sparse items differ in cost like causal ones and are claimed
+  // dynamically.  Under the bottom-right causal mask, items cost the same
+  // when the query rows are few (decode, N_q <= 16: every row sees about all
+  // keys), and the static split serves them.
   const bool uneven = block_mask != nullptr || (causal && Nq > 16);
-  p.grid = fwd_grid(g.BH, g.n_pairs * g.splits, uneven, ds->sm_count);
+  set_fwd_grid(&p, ds, (long long)g.BH * g.n_pairs * g.splits, uneven, true,
+               static_cast<cudaStream_t>(stream));
   // Square, d = 128, no mask: the CTA-pair kernel (tcgen05 cta_group::2),
   // whose products read half the shared memory per CTA, runs only when
   // FA_FWD_PAIR=1 is in the environment (0 or unset: the one-CTA kernel;
@@ -604,6 +645,9 @@ int fa_fwd_schedule(int B, int H, int N, int causal, int num_ctas, int* item_bh,
   const int n_kv = ceil_div(N, kTile);
   const long long total = (long long)BH * n_pairs;
   const int ctas = fwd_grid(BH, n_pairs, causal, num_ctas);
+  // Under a causal mask with more items than CTAs, persistent CTAs claim
+  // the items in list order at run time: no CTA is fixed in advance.
+  const bool claimed = causal && total > num_ctas;
   for (long long t = 0; t < total && t < max_items; ++t) {
     int bh, pair;
     fwd_item((int)t, BH, n_pairs, &bh, &pair);
@@ -611,7 +655,7 @@ int fa_fwd_schedule(int B, int H, int N, int causal, int num_ctas, int* item_bh,
     if (item_pair) item_pair[t] = pair;
     if (item_cost)
       item_cost[t] = fwd_kv_tiles(2 * pair, n_kv, causal) + fwd_kv_tiles(2 * pair + 1, n_kv, causal);
-    if (item_cta) item_cta[t] = snake_cta((int)t, ctas);
+    if (item_cta) item_cta[t] = claimed ? -1 : snake_cta((int)t, ctas);
   }
   return (int)total;
 }

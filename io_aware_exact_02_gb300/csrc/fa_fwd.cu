@@ -42,6 +42,7 @@ namespace fa {
 namespace {
 
 constexpr float kLn2 = 0.69314718055994530942f;
+constexpr int kItemRing = 4;  // claimed item indices in flight between the roles
 
 template <int D, bool kFp8 = false>
 struct FwdCfg {
@@ -109,6 +110,12 @@ struct alignas(1024) FwdSmem {
   uint64_t ml_full[2];      // kEpi: softmax t has published its rows' 1 / l
   uint64_t ml_empty[2];     // kEpi: the epilogue has read them
   float inv_l[2][kTile];    // kEpi: 1 / l per row of each Q tile (0: no key seen)
+  // Dynamic item claiming: the producer writes the m-th claimed item index
+  // into slot m % kItemRing (item_full); every other role reads it and
+  // arrives on item_empty.
+  uint64_t item_full[kItemRing];
+  uint64_t item_empty[kItemRing];
+  int item_idx[kItemRing];
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
@@ -118,7 +125,7 @@ struct alignas(1024) FwdSmem {
 enum : int {
   kSiteQFull = 101, kSiteKvEmpty, kSiteKvFull, kSitePFull, kSiteSFull, kSiteOFull, kSiteDrain,
   kSiteQEmpty, kSiteOEmpty, kSiteStageSlot, kSiteStaged, kSiteStored, kSitePHalf, kSiteMlFull,
-  kSiteMlEmpty
+  kSiteMlEmpty, kSiteItemFull, kSiteItemEmpty
 };
 // Bounds checks of the checked build (FA_CHECKS).
 enum : int {
@@ -163,7 +170,9 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
 // slide pages 18 and 24); S and O += P V run as kind::f8f6f4 products, P is
 // rounded to E4M3 in tensor memory, and V arrives transposed ([d][keys]) so
 // that both operands of O += P V are K-major.
-template <int D, bool kNeg, bool kGeneral, bool kSparse, bool kFp8, bool kStage>
+// kDyn: persistent CTAs claim their items from the work counter p.sched
+// (under a causal or block mask); otherwise the list is split statically.
+template <int D, bool kNeg, bool kGeneral, bool kSparse, bool kFp8, bool kStage, bool kDyn>
 __global__ void __launch_bounds__(FwdCfg<D, kFp8>::threads(kStage), 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap to,
@@ -201,6 +210,13 @@ __global__ void __launch_bounds__(FwdCfg<D, kFp8>::threads(kStage), 1)
       mbar_init(&sm.ml_full[t], 128);
       mbar_init(&sm.ml_empty[t], 128);
     }
+    // Readers of a claimed index: the MMA thread, the eight softmax warps,
+    // the four epilogue warps and the store thread (when the kernel has them).
+    if (kDyn)
+      for (int i = 0; i < kItemRing; ++i) {
+        mbar_init(&sm.item_full[i], 1);
+        mbar_init(&sm.item_empty[i], 1 + 8 + (kEpi ? 4 : 0) + (kStage ? 1 : 0));
+      }
     mbar_init(&sm.drain, 1);
     sm.abort_flag = 0;
     fence_mbar_init();
@@ -217,10 +233,14 @@ __global__ void __launch_bounds__(FwdCfg<D, kFp8>::threads(kStage), 1)
   // (programmatic dependent launch); its outputs are read only after this.
   wait_prior_grid();
 
-  // Persistent CTAs: CTA c takes the work items of the longest-first list
-  // in "snake" order -- items c, 2G-1-c, 2G+c, 4G-1-c, ... for G CTAs -- so
-  // that every CTA gets a similar mix of long and short items.  With one CTA
-  // per item (G = items) each CTA takes exactly item c.
+  // Persistent CTAs without a work counter: CTA c takes the work items of
+  // the longest-first list in "snake" order -- items c, 2G-1-c, 2G+c,
+  // 4G-1-c, ... for G CTAs -- so that every CTA gets a similar mix of long
+  // and short items.  With one CTA per item (G = items) each CTA takes
+  // exactly item c.  With a work counter (p.sched) the producer claims the
+  // next item of the list whenever it is ready to load one, and hands the
+  // index to the other roles through the item ring.
+  constexpr bool dyn = kDyn;
   const int splits = kGeneral ? p.splits : 1;
   const int num_items = p.BH * p.n_pairs * splits;
   const int G = gridDim.x;
@@ -236,6 +256,19 @@ __global__ void __launch_bounds__(FwdCfg<D, kFp8>::threads(kStage), 1)
   auto item_of_round = [&](int k) -> int {
     const int base = k * G;
     return (k & 1) ? base + (G - 1 - (int)blockIdx.x) : base + (int)blockIdx.x;
+  };
+  // The CTA's m-th item (num_items: none left).  Dynamic claiming: waits
+  // for the producer's m-th claim; the caller then releases the ring slot
+  // with release_item(m), once per warp (or by the single thread of a
+  // one-thread role) after all of its lanes have read the index.
+  auto item_at = [&](int m, bool& ok) -> int {
+    if (!dyn) return m * G < num_items ? item_of_round(m) : num_items;
+    const int slot = m % kItemRing;
+    ok = mbar_wait(&sm.item_full[slot], (m / kItemRing) & 1, p.status, abortf, kSiteItemFull);
+    return ok ? *reinterpret_cast<volatile int*>(&sm.item_idx[slot]) : num_items;
+  };
+  auto release_item = [&](int m) {
+    if (dyn) mbar_arrive(&sm.item_empty[m % kItemRing]);
   };
   // An item: K/V head bh, pair `pair` of its packed query rows, key split.
   // Q tile t's rows see key tiles [j0, j0 + n_t[t]) of the split.  Block-
@@ -313,9 +346,13 @@ __global__ void __launch_bounds__(FwdCfg<D, kFp8>::threads(kStage), 1)
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     int n_done = 0, cb = 0, n_staged = 0;
     bool ok = true;
-    for (int k = 0; ok && k * G < num_items; ++k) {
-      const int idx = item_of_round(k);
-      if (idx >= num_items) continue;
+    for (int m = 0; ok; ++m) {
+      const int idx = item_at(m, ok);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      __syncwarp();  // every lane has read the index
+      if (lane_id() == 0) release_item(m);
+      if (idx >= num_items) break;
       const Item item = decode(idx);
       if (!warp_bound_ok(item_ok(item), p.status, abortf, kChkItem)) {
         ok = false;
@@ -396,9 +433,24 @@ __global__ void __launch_bounds__(FwdCfg<D, kFp8>::threads(kStage), 1)
       int q_issued = 0;  // Q pairs issued
       int n_staged = 0;  // items whose O staging uses were handed over
       bool ok = true;
-      for (int k = 0; ok && k * G < num_items; ++k) {
-        const int idx = item_of_round(k);
-        if (idx >= num_items) continue;
+      for (int m = 0; ok; ++m) {
+        int idx;
+        if (dyn) {
+          // Claim the next item once every role has read the index that
+          // last used this ring slot.
+          const int slot = m % kItemRing;
+          if (m >= kItemRing && !mbar_wait(&sm.item_empty[slot], (m / kItemRing - 1) & 1,
+                                           p.status, abortf, kSiteItemEmpty)) {
+            ok = false;
+            break;
+          }
+          idx = min(atomicAdd(p.sched, 1), num_items);
+          *reinterpret_cast<volatile int*>(&sm.item_idx[slot]) = idx;
+          mbar_arrive(&sm.item_full[slot]);
+        } else {
+          idx = item_at(m, ok);
+        }
+        if (idx >= num_items) break;
         const Item it = decode(idx);
         if (!item_ok(it)) {
           ok = false;
@@ -578,9 +630,11 @@ __global__ void __launch_bounds__(FwdCfg<D, kFp8>::threads(kStage), 1)
         }
       };
 
-      for (int k = 0; ok && k * G < num_items; ++k) {
-        const int idx = item_of_round(k);
-        if (idx >= num_items) continue;
+      for (int m = 0; ok; ++m) {
+        const int idx = item_at(m, ok);
+        if (!ok) break;
+        release_item(m);
+        if (idx >= num_items) break;
         const Item it = decode(idx);
         if (!item_ok(it)) {
           ok = false;
@@ -730,9 +784,11 @@ __global__ void __launch_bounds__(FwdCfg<D, kFp8>::threads(kStage), 1)
     if (lane_id() == 0 && stage_epi) {
       int cb = 0, n_staged = 0;
       bool ok = true;
-      for (int k = 0; ok && k * G < num_items; ++k) {
-        const int idx = item_of_round(k);
-        if (idx >= num_items) continue;
+      for (int m = 0; ok; ++m) {
+        const int idx = item_at(m, ok);
+        if (!ok) break;
+        release_item(m);
+        if (idx >= num_items) break;
         const Item it = decode(idx);
         if (!item_ok(it)) {
           ok = false;
@@ -787,9 +843,13 @@ __global__ void __launch_bounds__(FwdCfg<D, kFp8>::threads(kStage), 1)
     int n_staged = 0;  // this warpgroup's O tiles handed to the store warp
     bool ok = true;
 
-    for (int k = 0; ok && k * G < num_items; ++k) {
-      const int idx = item_of_round(k);
-      if (idx >= num_items) continue;
+    for (int m = 0; ok; ++m) {
+      const int idx = item_at(m, ok);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      __syncwarp();  // every lane has read the index
+      if (lane_id() == 0) release_item(m);
+      if (idx >= num_items) break;
       const Item item = decode(idx);
       if (!warp_bound_ok(item_ok(item), p.status, abortf, kChkItem)) {
         ok = false;
@@ -959,6 +1019,16 @@ __global__ void __launch_bounds__(FwdCfg<D, kFp8>::threads(kStage), 1)
     tc_fence_after();
     tmem_dealloc(tmem, Cfg::kTmemCols);
   }
+  if (dyn && tid == 0) {
+    // This CTA's claims are over (the producer made them before the barrier
+    // above): count the CTA out, and the last one out zeroes the counter
+    // for the next launch on the stream.
+    __threadfence();
+    if (atomicAdd(p.sched + 1, 1) == G - 1) {
+      atomicExch(p.sched, 0);
+      atomicExch(p.sched + 1, 0);
+    }
+  }
 }
 
 // Merge the key splits of the general forward pass: per row,
@@ -1043,12 +1113,12 @@ __global__ void __launch_bounds__(256) fa_combine_kernel(const FwdParams p) {
   if (lane == 0) p.lse[row] = lse_row;
 }
 
-template <int D, bool kNeg, bool kGeneral, bool kSparse = false, bool kFp8 = false,
-          bool kStage = false>
+template <int D, bool kNeg, bool kGeneral, bool kSparse, bool kFp8, bool kStage, bool kDyn>
 int launch_fwd_dn(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                   const CUtensorMap& to, const FwdParams& p, cudaStream_t stream) {
+  if (kDyn != (p.sched != nullptr)) return FA_ERR_LAUNCH;
   const size_t smem = sizeof(FwdSmem<D, kFp8>) + 1024;
-  if (cudaFuncSetAttribute(fa_fwd_kernel<D, kNeg, kGeneral, kSparse, kFp8, kStage>,
+  if (cudaFuncSetAttribute(fa_fwd_kernel<D, kNeg, kGeneral, kSparse, kFp8, kStage, kDyn>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return FA_ERR_LAUNCH;
   if constexpr (FwdCfg<D, kFp8>::realloc(kStage) || FwdCfg<D, kFp8>::epi(kStage)) {
@@ -1056,7 +1126,7 @@ int launch_fwd_dn(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMa
     // other warpgroups release, which suffice only at the launch register
     // count the split assumes: refuse to launch otherwise.
     cudaFuncAttributes attr;
-    if (cudaFuncGetAttributes(&attr, fa_fwd_kernel<D, kNeg, kGeneral, kSparse, kFp8, kStage>) !=
+    if (cudaFuncGetAttributes(&attr, fa_fwd_kernel<D, kNeg, kGeneral, kSparse, kFp8, kStage, kDyn>) !=
             cudaSuccess ||
         attr.numRegs < (FwdCfg<D, kFp8>::epi(kStage) ? FwdCfg<D, kFp8>::kEpiRegsLaunch
                                                      : FwdCfg<D, kFp8>::kRegsLaunch))
@@ -1075,7 +1145,7 @@ int launch_fwd_dn(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMa
   c.stream = stream;
   c.attrs = pdl;
   c.numAttrs = 1;
-  if (cudaLaunchKernelEx(&c, fa_fwd_kernel<D, kNeg, kGeneral, kSparse, kFp8, kStage>, tq, tk, tv, to,
+  if (cudaLaunchKernelEx(&c, fa_fwd_kernel<D, kNeg, kGeneral, kSparse, kFp8, kStage, kDyn>, tq, tk, tv, to,
                          p) != cudaSuccess) {
     cudaGetLastError();
     return FA_ERR_LAUNCH;
@@ -1093,6 +1163,16 @@ int launch_fwd_dn(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMa
   return FA_OK;
 }
 
+// The kernel for the sign of the scale (kNeg: a negative scale turns the
+// row maximum into a minimum).
+template <int D, bool kGeneral, bool kSparse, bool kFp8, bool kStage, bool kDyn>
+int launch_fwd_signed(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                      const CUtensorMap& to, const FwdParams& p, cudaStream_t stream) {
+  if (p.scale_log2 < 0.f)
+    return launch_fwd_dn<D, true, kGeneral, kSparse, kFp8, kStage, kDyn>(tq, tk, tv, to, p, stream);
+  return launch_fwd_dn<D, false, kGeneral, kSparse, kFp8, kStage, kDyn>(tq, tk, tv, to, p, stream);
+}
+
 template <int D>
 int launch_fwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                  const CUtensorMap& to, FwdParams p, cudaStream_t stream) {
@@ -1100,31 +1180,31 @@ int launch_fwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap
   // smallest normal positive scale, whose exponents round to exactly 0.
   if (p.scale_log2 == 0.f) p.scale_log2 = 1.17549435e-38f;
   const bool general = p.splits > 1 || p.Nq != p.rows || p.Nkv != p.rows;
-  if (p.fp8_amax) {  // square case, d = 128 only (checked by the caller)
+  const bool dyn = p.sched != nullptr;
+  if (p.fp8_amax) {  // square case, d = 128 only (checked by the caller); static split
     if constexpr (D == 128) {
-      if (p.scale_log2 < 0.f) return launch_fwd_dn<D, true, false, false, true>(tq, tk, tv, to, p, stream);
-      return launch_fwd_dn<D, false, false, false, true>(tq, tk, tv, to, p, stream);
+      if (dyn) return FA_ERR_LAUNCH;
+      return launch_fwd_signed<D, false, false, true, false, false>(tq, tk, tv, to, p, stream);
     }
     return FA_ERR_UNSUPPORTED_D;
   }
   if (p.block_mask) {  // square case only (checked by the caller)
-    if (p.scale_log2 < 0.f) return launch_fwd_dn<D, true, false, true>(tq, tk, tv, to, p, stream);
-    return launch_fwd_dn<D, false, false, true>(tq, tk, tv, to, p, stream);
+    if (dyn) return launch_fwd_signed<D, false, true, false, false, true>(tq, tk, tv, to, p, stream);
+    return launch_fwd_signed<D, false, true, false, false, false>(tq, tk, tv, to, p, stream);
   }
   if (general) {
-    if (p.scale_log2 < 0.f) return launch_fwd_dn<D, true, true>(tq, tk, tv, to, p, stream);
-    return launch_fwd_dn<D, false, true>(tq, tk, tv, to, p, stream);
+    if (dyn) return launch_fwd_signed<D, true, false, false, false, true>(tq, tk, tv, to, p, stream);
+    return launch_fwd_signed<D, true, false, false, false, false>(tq, tk, tv, to, p, stream);
   }
   // Staged O stores (at d = 128 with the epilogue warpgroup) pay at every
-  // length; they need persistent CTAs (no mask, more items than CTAs).
+  // length; they need persistent CTAs (more items than CTAs).
   const long long items = (long long)p.BH * p.n_pairs;
   if (p.grid < items) {
-    if (p.scale_log2 < 0.f)
-      return launch_fwd_dn<D, true, false, false, false, true>(tq, tk, tv, to, p, stream);
-    return launch_fwd_dn<D, false, false, false, false, true>(tq, tk, tv, to, p, stream);
+    if (dyn) return launch_fwd_signed<D, false, false, false, true, true>(tq, tk, tv, to, p, stream);
+    return launch_fwd_signed<D, false, false, false, true, false>(tq, tk, tv, to, p, stream);
   }
-  if (p.scale_log2 < 0.f) return launch_fwd_dn<D, true, false>(tq, tk, tv, to, p, stream);
-  return launch_fwd_dn<D, false, false>(tq, tk, tv, to, p, stream);
+  if (dyn) return FA_ERR_LAUNCH;  // a work counter comes with a persistent grid
+  return launch_fwd_signed<D, false, false, false, false, false>(tq, tk, tv, to, p, stream);
 }
 
 }  // namespace

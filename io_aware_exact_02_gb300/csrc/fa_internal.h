@@ -63,7 +63,16 @@ struct FwdParams {
   int causal;
   float scale_log2;  // scale * log2(e)
   int grid;          // CTAs launched
+  // Dynamic item claiming (persistent CTAs under a causal or block mask):
+  // {items claimed, CTAs finished}, zero at launch; the last CTA to finish
+  // sets both back to zero.  Null: the static split of the list.
+  int* sched;
 };
+
+// Slots of the forward's work counters: calls on one stream share a slot
+// (they run in order), calls on different streams get different slots.
+constexpr int kFwdSchedSlots = 64;
+constexpr int kFwdSchedStride = 32;  // ints per slot: one 128-byte line each
 
 // Number of 128-key tiles, counted from key 0, that the query rows
 // [r0, min(r0 + 128, rows)) of a K/V head need: all of them without a mask,
@@ -90,10 +99,12 @@ __host__ __device__ inline int snake_cta(int idx, int ctas) {
 
 // The forward kernel's grid.  Without a mask every item costs the same and
 // min(items, SMs) persistent CTAs split the list statically.  Under a causal
-// mask item costs differ by up to N/128 and there are few items per SM, so
-// every item gets its own CTA: the hardware hands CTAs to SMs in list order
-// as SMs free up, i.e. greedy list scheduling of the longest-first list
-// (the LPT rule), which a static split cannot match.
+// mask item costs differ by up to N/128, so a static split cannot balance
+// them: the CTAs take the longest-first list greedily instead (the LPT
+// rule).  With a work counter (FwdParams::sched) min(items, SMs) persistent
+// CTAs claim the items in list order as they become ready for one; without
+// one every item gets its own CTA and the hardware hands CTAs to SMs in
+// list order as SMs free up.  This function gives the grid of the latter.
 __host__ __device__ inline int fwd_grid(int BH, int n_pairs, int causal, int sm_count) {
   const long long items = (long long)BH * n_pairs;
   if (causal) return (int)items;

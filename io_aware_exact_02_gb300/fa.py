@@ -450,7 +450,8 @@ def check_device_status(stream=None):
 
 
 def fwd_schedule(B: int, H: int, N: int, causal: bool, num_ctas: int = 152):
-    """The forward kernel's work list: (bh, pair, cost, cta) per item, in list order."""
+    """The forward kernel's work list: (bh, pair, cost, cta) per item, in list order
+    (cta -1: claimed from the work counter at run time)."""
     lib = load()
     n = lib.fa_fwd_schedule(B, H, N, int(bool(causal)), int(num_ctas), None, None, None, None, 0)
     if n < 0:

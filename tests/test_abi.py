@@ -152,16 +152,21 @@ def test_lpt_example_of_the_pages(lib):
 
 
 @pytest.mark.parametrize("B,H,N,causal", [(1, 2, 1024, 1), (2, 5, 3000, 1), (3, 4, 700, 0),
-                                          (1, 17, 4096, 1), (1, 1, 1, 0)])
+                                          (1, 17, 4096, 1), (1, 1, 1, 0), (1, 1, 1024, 1),
+                                          (1, 1, 1792, 1)])
 def test_schedule_covers_every_item_once_longest_first(lib, B, H, N, causal):
     items = fa.fwd_schedule(B, H, N, causal, num_ctas=7)
     n_pairs = -(-N // 256)
     assert sorted((bh, p) for bh, p, _, _ in items) == [(bh, p) for bh in range(B * H)
                                                        for p in range(n_pairs)]
-    ctas = len(items) if causal else min(len(items), 7)
-    assert [c for _, _, _, c in items] == fa.snake_assign(len(items), ctas)
-    if causal:
+    if causal and len(items) > 7:
+        # Claimed from the work counter at run time by 7 persistent CTAs.
+        assert all(c == -1 for _, _, _, c in items)
+    elif causal:
+        # No more items than CTAs: item t on CTA t.
         assert [c for _, _, _, c in items] == list(range(len(items)))
+    else:
+        assert [c for _, _, _, c in items] == fa.snake_assign(len(items), min(len(items), 7))
     n_kv = -(-N // 128)
     for bh, p, c, _ in items:
         expect = (min(2 * p + 1, n_kv) + min(2 * p + 2, n_kv)) if causal else 2 * n_kv

@@ -179,28 +179,65 @@ def test_fwd_full_size_sampled(name):
     sampled_check(w, o, lse, q, k, v, extra=late_items(w))
 
 
-@pytest.mark.parametrize("N,d", [(1000, 128), (1920, 128), (3000, 64), (257, 64), (100, 128),
-                                 (129, 128), (300, 128), (64, 64)])
-def test_fwd_staged_stores_ragged(N, d):
-    # Non-causal grids with more items than SMs store O through the staging
-    # ring slots with TMA (at d = 128 from the epilogue warpgroup); the tail
+@pytest.mark.parametrize("N,d,causal", [(1000, 128, 0), (1920, 128, 0), (3000, 64, 0), (257, 64, 0),
+                                        (100, 128, 0), (129, 128, 0), (300, 128, 0), (64, 64, 0),
+                                        (1000, 128, 1), (1000, 64, 1), (129, 128, 1), (300, 64, 1),
+                                        (2000, 128, 1)])
+def test_fwd_staged_stores_ragged(N, d, causal):
+    # Grids with more items than SMs store O through the staging ring slots
+    # with TMA (at d = 128 from the epilogue warpgroup): without a mask each
+    # persistent CTA takes its items in snake order, under the causal mask
+    # the CTAs claim items of unequal cost from the work counter.  The tail
     # tile of every head is partly past N (rows there must not be written),
     # and at N <= 128 every item's second Q tile has no rows at all.
     # Sampled rows of the first, last and random heads, including each
     # head's last rows.
     from io_aware_exact_02_gb300.synth import Workload
-    w = Workload("staged_N%d_d%d" % (N, d), 8, 24, N, d, False)
+    w = Workload("staged_N%d_d%d_c%d" % (N, d, causal), 8, 24, N, d, bool(causal))
     q, k, v, _ = synth.draw_workload(w, seed=N + d, with_dout=False)
     dev = torch.device("cuda")
     # A guard band after O catches a store past the end of the tensor.
     o_buf = torch.full((w.B * w.H * N * d + 4096,), 7.0, dtype=torch.bfloat16, device=dev)
     o = o_buf[: w.B * w.H * N * d].view(w.B, w.H, N, d)
     lse = torch.empty((w.B, w.H, N), dtype=torch.float32, device=dev)
-    fa.fwd(q.to(dev), k.to(dev), v.to(dev), causal=False, scale=w.softmax_scale, out=o, lse=lse)
+    fa.fwd(q.to(dev), k.to(dev), v.to(dev), causal=w.causal, scale=w.softmax_scale, out=o, lse=lse)
     fa.check_device_status()
     assert torch.all(o_buf[w.B * w.H * N * d:] == 7.0)
     assert torch.isfinite(o).all() and torch.isfinite(lse).all()
     sampled_check(w, o, lse, q, k, v, n_heads=4, n_rows=40, seed=N)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_fwd_claimed_items_repeat_bitwise(d):
+    # Under the causal mask with more items than SMs, the persistent CTAs
+    # claim items from the library's work counter for the stream, which
+    # every launch must leave at zero.  Repeated calls on one stream, calls
+    # on a second stream, a static (non-causal) call and a general-path call
+    # in between, give the same bits every time; an item is computed by one
+    # CTA whichever claims it.
+    B, H, N = 8, 24, 1000
+    q, k, v, _ = synth.draw(B, H, N, d, seed=70 + d, with_dout=False)
+    dev = torch.device("cuda")
+    q, k, v = q.to(dev), k.to(dev), v.to(dev)
+    o0, l0 = fa.fwd(q, k, v, causal=True)
+    runs = []
+    for i in range(3):
+        runs.append(fa.fwd(q, k, v, causal=True))
+        fa.fwd(q, k, v, causal=False)
+        fa.fwd_gqa(q, k, v, causal=True, num_splits=1)
+    s2 = torch.cuda.Stream()
+    s2.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s2):
+        runs.append(fa.fwd(q, k, v, causal=True))
+        runs.append(fa.fwd(q, k, v, causal=True))
+    torch.cuda.current_stream().wait_stream(s2)
+    torch.cuda.synchronize()
+    fa.check_device_status()
+    for o, l in runs:
+        assert torch.equal(o, o0) and torch.equal(l, l0)
+    w = synth.Workload("claimed_d%d" % d, B, H, N, d, True)
+    sampled_check(w, o0, l0, q.cpu(), k.cpu(), v.cpu(), n_heads=3, n_rows=32, seed=d,
+                  extra=late_items(w))
 
 
 def test_fwd_long_sequence_sampled_rows():

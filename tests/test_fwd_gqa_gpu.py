@@ -74,6 +74,10 @@ CASES = [
     # time and the split O rows eight at a time (ragged in both)
     (2, 8, 2, 1, 4700, 128, True, 37),
     (1, 4, 1, 2, 5000, 64, False, 64),
+    # causal prefill with more items than SMs: persistent CTAs claim the
+    # items (of unequal cost) from the work counter, with and without splits
+    (8, 16, 4, 300, 300, 64, True, 1),
+    (8, 16, 4, 260, 1000, 128, True, 2),
 ]
 
 
@@ -96,8 +100,11 @@ def test_fwd_gqa_auto_splits_decode():
     compare(o, lse, o_ref, lse_ref, "auto")
 
 
-def test_square_general_path_equals_fa_fwd_bitwise():
-    q, k, v, _ = synth.draw(2, 3, 700, 128, seed=8, with_dout=False)
+@pytest.mark.parametrize("B,H,N,d", [(2, 3, 700, 128), (8, 24, 1000, 128), (8, 24, 1000, 64)])
+def test_square_general_path_equals_fa_fwd_bitwise(B, H, N, d):
+    # The larger shapes have more items than SMs: persistent CTAs (claiming
+    # the items from the work counter under the causal mask) in both paths.
+    q, k, v, _ = synth.draw(B, H, N, d, seed=8, with_dout=False)
     dev = torch.device("cuda")
     q, k, v = q.to(dev), k.to(dev), v.to(dev)
     for causal in (False, True):
