@@ -91,6 +91,15 @@ struct FwdCfg {
   static constexpr int kBoxes = kFp8 ? D / 128 : D / 64;
 };
 
+// A work item: K/V head bh, pair `pair` of its packed query rows, key
+// split; idx is its index in the list (the list's length: no item).  Q
+// tile t's rows see key tiles [j0, j0 + n_t[t]) of the split.  Block-
+// sparse: Q tile t has n_t[t] active key tiles and the item takes
+// nmax = max(n_t[0], n_t[1]) steps.
+struct FwdItem {
+  int idx, bh, pair, split, row0, j0, n_t[2], nmax, hi[2];
+};
+
 template <int D, bool kFp8 = false>
 struct alignas(1024) FwdSmem {
   uint8_t q[2][FwdCfg<D, kFp8>::kTileBytes];
@@ -110,12 +119,12 @@ struct alignas(1024) FwdSmem {
   uint64_t ml_full[2];      // kEpi: softmax t has published its rows' 1 / l
   uint64_t ml_empty[2];     // kEpi: the epilogue has read them
   float inv_l[2][kTile];    // kEpi: 1 / l per row of each Q tile (0: no key seen)
-  // Dynamic item claiming: the producer writes the m-th claimed item index
-  // into slot m % kItemRing (item_full); every other role reads it and
-  // arrives on item_empty.
+  // The item ring: the producer writes the CTA's m-th item, decoded, into
+  // slot m % kItemRing (item_full); every other role reads it and arrives
+  // on item_empty.
   uint64_t item_full[kItemRing];
   uint64_t item_empty[kItemRing];
-  int item_idx[kItemRing];
+  FwdItem item_rec[kItemRing];
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
@@ -210,13 +219,12 @@ __global__ void __launch_bounds__(FwdCfg<D, kFp8>::threads(kStage), 1)
       mbar_init(&sm.ml_full[t], 128);
       mbar_init(&sm.ml_empty[t], 128);
     }
-    // Readers of a claimed index: the MMA thread, the eight softmax warps,
+    // Readers of an item record: the MMA thread, the eight softmax warps,
     // the four epilogue warps and the store thread (when the kernel has them).
-    if (kDyn)
-      for (int i = 0; i < kItemRing; ++i) {
-        mbar_init(&sm.item_full[i], 1);
-        mbar_init(&sm.item_empty[i], 1 + 8 + (kEpi ? 4 : 0) + (kStage ? 1 : 0));
-      }
+    for (int i = 0; i < kItemRing; ++i) {
+      mbar_init(&sm.item_full[i], 1);
+      mbar_init(&sm.item_empty[i], 1 + 8 + (kEpi ? 4 : 0) + (kStage ? 1 : 0));
+    }
     mbar_init(&sm.drain, 1);
     sm.abort_flag = 0;
     fence_mbar_init();
@@ -238,8 +246,10 @@ __global__ void __launch_bounds__(FwdCfg<D, kFp8>::threads(kStage), 1)
   // 4G-1-c, ... for G CTAs -- so that every CTA gets a similar mix of long
   // and short items.  With one CTA per item (G = items) each CTA takes
   // exactly item c.  With a work counter (p.sched) the producer claims the
-  // next item of the list whenever it is ready to load one, and hands the
-  // index to the other roles through the item ring.
+  // next item of the list whenever it is ready to load one.  Either way the
+  // producer decodes the item and hands the record to the other roles
+  // through the item ring, so that they spend no time on it at an item
+  // boundary.
   constexpr bool dyn = kDyn;
   const int splits = kGeneral ? p.splits : 1;
   const int num_items = p.BH * p.n_pairs * splits;
@@ -257,26 +267,29 @@ __global__ void __launch_bounds__(FwdCfg<D, kFp8>::threads(kStage), 1)
     const int base = k * G;
     return (k & 1) ? base + (G - 1 - (int)blockIdx.x) : base + (int)blockIdx.x;
   };
-  // The CTA's m-th item (num_items: none left).  Dynamic claiming: waits
-  // for the producer's m-th claim; the caller then releases the ring slot
-  // with release_item(m), once per warp (or by the single thread of a
-  // one-thread role) after all of its lanes have read the index.
-  auto item_at = [&](int m, bool& ok) -> int {
-    if (!dyn) return m * G < num_items ? item_of_round(m) : num_items;
+  // The list index of the CTA's m-th item (num_items: none left), for the
+  // producer: claimed from the work counter, or the static split's.
+  auto next_index = [&](int m) -> int {
+    if (dyn) return min(atomicAdd(p.sched, 1), num_items);
+    return m * G < num_items ? item_of_round(m) : num_items;
+  };
+  using Item = FwdItem;
+  // The CTA's m-th item as the producer published it (idx == num_items:
+  // none left).  The caller then releases the ring slot with
+  // release_item(m), once per warp (or by the single thread of a
+  // one-thread role) after all of its lanes have read the record.
+  auto take_item = [&](int m, bool& ok) -> Item {
     const int slot = m % kItemRing;
     ok = mbar_wait(&sm.item_full[slot], (m / kItemRing) & 1, p.status, abortf, kSiteItemFull);
-    return ok ? *reinterpret_cast<volatile int*>(&sm.item_idx[slot]) : num_items;
+    Item it;
+    if (ok) {
+      it = sm.item_rec[slot];
+    } else {
+      it.idx = num_items;
+    }
+    return it;
   };
-  auto release_item = [&](int m) {
-    if (dyn) mbar_arrive(&sm.item_empty[m % kItemRing]);
-  };
-  // An item: K/V head bh, pair `pair` of its packed query rows, key split.
-  // Q tile t's rows see key tiles [j0, j0 + n_t[t]) of the split.  Block-
-  // sparse: Q tile t has n_t[t] active key tiles and the item takes
-  // nmax = max(n_t[0], n_t[1]) steps.
-  struct Item {
-    int bh, pair, split, row0, j0, n_t[2], nmax, hi[2];
-  };
+  auto release_item = [&](int m) { mbar_arrive(&sm.item_empty[m % kItemRing]); };
   // Block-sparse: is key tile jj active for query tile t of the item?
   auto active = [&](const Item& it, int t, int jj) -> bool {
     if (jj >= it.hi[t]) return false;
@@ -295,6 +308,7 @@ __global__ void __launch_bounds__(FwdCfg<D, kFp8>::threads(kStage), 1)
   };
   auto decode = [&](int idx) -> Item {
     Item it;
+    it.idx = idx;
     it.split = idx % splits;
     fwd_item(idx / splits, p.BH, p.n_pairs, &it.bh, &it.pair);
     it.row0 = it.pair * kPairRows;
@@ -347,13 +361,12 @@ __global__ void __launch_bounds__(FwdCfg<D, kFp8>::threads(kStage), 1)
     int n_done = 0, cb = 0, n_staged = 0;
     bool ok = true;
     for (int m = 0; ok; ++m) {
-      const int idx = item_at(m, ok);
+      const Item item = take_item(m, ok);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
-      __syncwarp();  // every lane has read the index
+      __syncwarp();  // every lane has read the record
       if (lane_id() == 0) release_item(m);
-      if (idx >= num_items) break;
-      const Item item = decode(idx);
+      if (item.idx >= num_items) break;
       if (!warp_bound_ok(item_ok(item), p.status, abortf, kChkItem)) {
         ok = false;
         break;
@@ -434,24 +447,24 @@ __global__ void __launch_bounds__(FwdCfg<D, kFp8>::threads(kStage), 1)
       int n_staged = 0;  // items whose O staging uses were handed over
       bool ok = true;
       for (int m = 0; ok; ++m) {
-        int idx;
-        if (dyn) {
-          // Claim the next item once every role has read the index that
-          // last used this ring slot.
-          const int slot = m % kItemRing;
-          if (m >= kItemRing && !mbar_wait(&sm.item_empty[slot], (m / kItemRing - 1) & 1,
-                                           p.status, abortf, kSiteItemEmpty)) {
-            ok = false;
-            break;
-          }
-          idx = min(atomicAdd(p.sched, 1), num_items);
-          *reinterpret_cast<volatile int*>(&sm.item_idx[slot]) = idx;
-          mbar_arrive(&sm.item_full[slot]);
-        } else {
-          idx = item_at(m, ok);
+        // Publish the next item once every role has read the record that
+        // last used this ring slot.
+        const int slot = m % kItemRing;
+        if (m >= kItemRing && !mbar_wait(&sm.item_empty[slot], (m / kItemRing - 1) & 1,
+                                         p.status, abortf, kSiteItemEmpty)) {
+          ok = false;
+          break;
         }
+        const int idx = next_index(m);
+        Item it;
+        if (idx < num_items) {
+          it = decode(idx);
+        } else {
+          it.idx = num_items;
+        }
+        sm.item_rec[slot] = it;
+        mbar_arrive(&sm.item_full[slot]);
         if (idx >= num_items) break;
-        const Item it = decode(idx);
         if (!item_ok(it)) {
           ok = false;
           break;
@@ -631,11 +644,10 @@ __global__ void __launch_bounds__(FwdCfg<D, kFp8>::threads(kStage), 1)
       };
 
       for (int m = 0; ok; ++m) {
-        const int idx = item_at(m, ok);
+        const Item it = take_item(m, ok);
         if (!ok) break;
         release_item(m);
-        if (idx >= num_items) break;
-        const Item it = decode(idx);
+        if (it.idx >= num_items) break;
         if (!item_ok(it)) {
           ok = false;
           break;
@@ -785,11 +797,10 @@ __global__ void __launch_bounds__(FwdCfg<D, kFp8>::threads(kStage), 1)
       int cb = 0, n_staged = 0;
       bool ok = true;
       for (int m = 0; ok; ++m) {
-        const int idx = item_at(m, ok);
+        const Item it = take_item(m, ok);
         if (!ok) break;
         release_item(m);
-        if (idx >= num_items) break;
-        const Item it = decode(idx);
+        if (it.idx >= num_items) break;
         if (!item_ok(it)) {
           ok = false;
           break;
@@ -844,13 +855,12 @@ __global__ void __launch_bounds__(FwdCfg<D, kFp8>::threads(kStage), 1)
     bool ok = true;
 
     for (int m = 0; ok; ++m) {
-      const int idx = item_at(m, ok);
+      const Item item = take_item(m, ok);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
-      __syncwarp();  // every lane has read the index
+      __syncwarp();  // every lane has read the record
       if (lane_id() == 0) release_item(m);
-      if (idx >= num_items) break;
-      const Item item = decode(idx);
+      if (item.idx >= num_items) break;
       if (!warp_bound_ok(item_ok(item), p.status, abortf, kChkItem)) {
         ok = false;
         break;
