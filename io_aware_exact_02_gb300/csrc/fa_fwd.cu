@@ -83,6 +83,17 @@ struct FwdCfg {
   // TMEM column of S/P and of O for Q tile t.
   static __device__ __forceinline__ uint32_t col_s(int t) { return (uint32_t)t * 128u; }
   static __device__ __forceinline__ uint32_t col_o(int t) { return 256u + (uint32_t)t * D; }
+  // kSRing (d = 64, bf16): the 128 columns past the two 64-column O
+  // accumulators are a third S buffer.  An item's S products (t, j), taken in
+  // the order k = 2j + t, use buffer k % 3, so the tensor core computes
+  // S(t, j+1) while softmax t still works on S(t, j): the product that last
+  // used S(t, j+1)'s buffer is P(t, j) V's predecessor, product k - 1,
+  // whose P V has been issued by then.  Buffer b's columns:
+  static constexpr bool kSRing = D == 64 && !kFp8;
+  static __device__ __forceinline__ uint32_t col_buf(int b) {
+    return b < 2 ? (uint32_t)b * 128u : 256u + 2u * D;
+  }
+  static_assert(!kSRing || 256 + 2 * D + 128 <= (int)kTmemCols, "third S buffer past tensor memory");
   // MMA K-steps (32 bytes of each operand row per step) of S = Q K^T and
   // of O += P V.
   static constexpr int kKSteps = kFp8 ? D / 32 : D / 16;
@@ -112,6 +123,7 @@ struct alignas(1024) FwdSmem {
   uint64_t p_half[2];   // bf16: P of keys 0-63 of the tile in tensor memory
   uint64_t p_full[2];
   uint64_t o_full[2];
+  uint64_t pv_done[2];  // kSRing: O_t += P_t V complete (one phase per product)
   uint64_t o_empty[2];  // softmax t has read O_t of the item (epilogue done)
   uint64_t staged[2];   // softmax t has written O_t into its ring slot for the store
   uint64_t stored[2];   // the store warp has read softmax t's staged O_t
@@ -134,7 +146,7 @@ struct alignas(1024) FwdSmem {
 enum : int {
   kSiteQFull = 101, kSiteKvEmpty, kSiteKvFull, kSitePFull, kSiteSFull, kSiteOFull, kSiteDrain,
   kSiteQEmpty, kSiteOEmpty, kSiteStageSlot, kSiteStaged, kSiteStored, kSitePHalf, kSiteMlFull,
-  kSiteMlEmpty, kSiteItemFull, kSiteItemEmpty
+  kSiteMlEmpty, kSiteItemFull, kSiteItemEmpty, kSitePvDone
 };
 // Bounds checks of the checked build (FA_CHECKS).
 enum : int {
@@ -212,6 +224,7 @@ __global__ void __launch_bounds__(FwdCfg<D, kFp8>::threads(kStage), 1)
       mbar_init(&sm.p_half[t], 128);
       mbar_init(&sm.p_full[t], 128);
       mbar_init(&sm.o_full[t], 1);
+      mbar_init(&sm.pv_done[t], 1);
       mbar_init(&sm.o_empty[t], 128);
       mbar_init(&sm.staged[t], 128);
       mbar_init(&sm.stored[t], 1);
@@ -339,6 +352,13 @@ __global__ void __launch_bounds__(FwdCfg<D, kFp8>::threads(kStage), 1)
       it.nmax = max(it.n_t[0], it.n_t[1]);
     }
     return it;
+  };
+  // The S ring (FwdCfg::kSRing) serves the dense square kernels' items whose
+  // two Q tiles take the same key tiles (every item without a mask); the
+  // others keep one S buffer per Q tile.
+  constexpr bool kRing = Cfg::kSRing && !kGeneral && !kSparse;
+  auto ring_item = [&](const Item& it) -> bool {
+    return kRing && it.nmax > 0 && it.n_t[0] == it.nmax && it.n_t[1] == it.nmax;
   };
   // Checked build: the item's head, pair and split exist and its key tiles
   // [j0, j0 + n_t) lie inside the head's.
@@ -574,21 +594,25 @@ __global__ void __launch_bounds__(FwdCfg<D, kFp8>::threads(kStage), 1)
       int q_used = 0;   // items that loaded Q (q_full / q_empty phases)
       bool ok = true;
 
-      auto issue_s = [&](int t, int kslot) {
+      // S_t = Q_t K into the S buffer at column `col` (Q tile t's own, or
+      // the S ring's).
+      auto issue_s_at = [&](int t, int kslot, uint32_t col) {
         const uint64_t qd = desc_here(kmajor_desc(q_addr[t], 0)), kd = desc_here(kmajor_desc(smem_u32(sm.kv[kslot]), 0));
 #pragma unroll
         for (int kk = 0; kk < Cfg::kKSteps; ++kk) {
           const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
           if constexpr (kFp8)
-            mma_ss_f8(tmem + Cfg::col_s(t), desc_plus(qd, off), desc_plus(kd, off), id_s, kk > 0);
+            mma_ss_f8(tmem + col, desc_plus(qd, off), desc_plus(kd, off), id_s, kk > 0);
           else
-            mma_ss(tmem + Cfg::col_s(t), desc_plus(qd, off), desc_plus(kd, off), id_s, kk > 0);
+            mma_ss(tmem + col, desc_plus(qd, off), desc_plus(kd, off), id_s, kk > 0);
         }
         tc_commit(&sm.s_full[t]);
       };
-      // O_t += P_t V; the item's first product overwrites O_t, so it waits
-      // until softmax t has stored the previous item's O_t.
-      auto issue_pv = [&](int t, int vslot, bool accumulate) -> bool {
+      auto issue_s = [&](int t, int kslot) { issue_s_at(t, kslot, Cfg::col_s(t)); };
+      // O_t += P_t V with P_t in the S buffer at column `pcol`; the item's
+      // first product overwrites O_t, so it waits until softmax t has stored
+      // the previous item's O_t.
+      auto issue_pv_at = [&](int t, int vslot, bool accumulate, uint32_t pcol) -> bool {
         if (!accumulate && n_done > 0) {
           if (!mbar_wait(&sm.o_empty[t], (n_done - 1) & 1, p.status, abortf, kSiteOEmpty))
             return false;
@@ -607,14 +631,18 @@ __global__ void __launch_bounds__(FwdCfg<D, kFp8>::threads(kStage), 1)
           }
           // P occupies 8 TMEM columns per K-step: 16 bf16 or 32 E4M3 keys.
           if constexpr (kFp8)
-            mma_ts_f8(tmem + Cfg::col_o(t), tmem + Cfg::col_s(t) + kk * 8,
+            mma_ts_f8(tmem + Cfg::col_o(t), tmem + pcol + kk * 8,
                       desc_plus(vd, (kk >> 2) * 16384 + (kk & 3) * 32), id_pv,
                       (accumulate || kk > 0) ? 1u : 0u);
           else
-            mma_ts(tmem + Cfg::col_o(t), tmem + Cfg::col_s(t) + kk * 8, desc_plus(vd, kk * 2048),
+            mma_ts(tmem + Cfg::col_o(t), tmem + pcol + kk * 8, desc_plus(vd, kk * 2048),
                    id_pv, (accumulate || kk > 0) ? 1u : 0u);
         }
+        if constexpr (kRing) tc_commit(&sm.pv_done[t]);
         return true;
+      };
+      auto issue_pv = [&](int t, int vslot, bool accumulate) -> bool {
+        return issue_pv_at(t, vslot, accumulate, Cfg::col_s(t));
       };
       auto wait_full = [&](int cnt) -> bool {
         return mbar_wait(&sm.kv_full[cnt % S], (cnt / S) & 1, p.status, abortf, kSiteKvFull);
@@ -664,6 +692,43 @@ __global__ void __launch_bounds__(FwdCfg<D, kFp8>::threads(kStage), 1)
           }
           ok = mbar_wait(&sm.q_full, q_used & 1, p.status, abortf, kSiteQFull);
           if (ok) ok = wait_full(cb);
+          if (ok && ring_item(it)) {
+            // S ring: S(0,0), S(1,0) into buffers 0 and 1; at step j, as soon
+            // as softmax t has the first half of P(t, j) in tensor memory
+            // (so it is past its wait for S(t, j)), S(t, j+1) goes into the
+            // buffer of product 2j + t - 1, whose P V is already issued, and
+            // then O_t += P(t, j) V_j.  K_{j+1}'s last reader is S(1, j+1),
+            // V_j's is PV(1, j).
+            tc_fence_after();
+            issue_s_at(0, cb % S, Cfg::col_buf(0));
+            issue_s_at(1, cb % S, Cfg::col_buf(1));
+            tc_commit(&sm.kv_empty[cb % S]);
+            if (nmax == 1) tc_commit(&sm.q_empty);
+            for (int j = 0; j < nmax && ok; ++j) {
+              const int vc = cb + 2 * j + 1, kc = cb + 2 * j + 2;
+              ok = wait_full(vc) && (j + 1 >= nmax || wait_full(kc));
+              for (int t = 0; t < 2 && ok; ++t) {
+                ok = wait_p(t);
+                if (!ok) break;
+                tc_fence_after();
+                if (j + 1 < nmax) {
+                  issue_s_at(t, kc % S, Cfg::col_buf((2 * j + t + 2) % 3));
+                  if (t == 1) {
+                    tc_commit(&sm.kv_empty[kc % S]);
+                    if (j + 1 == nmax - 1) tc_commit(&sm.q_empty);  // last product reading Q
+                  }
+                }
+                ok = issue_pv_at(t, vc % S, j > 0, Cfg::col_buf((2 * j + t) % 3));
+                if (!ok) break;
+                if (j == nmax - 1) tc_commit(&sm.o_full[t]);
+              }
+              if (ok) tc_commit(&sm.kv_empty[vc % S]);
+            }
+            cb += 2 * nmax + ring_per_item_extra;
+            ++q_used;
+            ++n_done;
+            continue;
+          }
           if (ok) {
             tc_fence_after();
             for (int t = 0; t < 2; ++t)
@@ -852,6 +917,7 @@ __global__ void __launch_bounds__(FwdCfg<D, kFp8>::threads(kStage), 1)
     int n_done = 0;
     int cb = 0;        // ring uses before the current item (as the MMA thread counts them)
     int n_staged = 0;  // this warpgroup's O tiles handed to the store warp
+    int n_pv = 0;      // kRing: O_t += P_t V products before this step, over all items
     bool ok = true;
 
     for (int m = 0; ok; ++m) {
@@ -867,6 +933,7 @@ __global__ void __launch_bounds__(FwdCfg<D, kFp8>::threads(kStage), 1)
       }
       const int bh = item.bh;
       const int n_t = item.n_t[t];
+      const bool ring = ring_item(item);
       // This tile's O staging use of the ring, when the item has one.
       const bool staged = stage_epi && item.nmax > 0;
       const int stage_use = cb + 2 * item.nmax + t;
@@ -906,8 +973,19 @@ __global__ void __launch_bounds__(FwdCfg<D, kFp8>::threads(kStage), 1)
         s_par ^= 1;
         if (!ok) break;
         tc_fence_after();
-        softmax_tile<D, kNeg, kFp8>(colS, colO, c2, tlim, j > 0, m_ref, l,
-                                    [&] { mbar_arrive(&sm.p_half[t]); });
+        // S ring: step j's S is product 2j + t of the item, in buffer (2j + t) % 3;
+        // it may have completed before the previous P V, which a rescale of O
+        // must wait for.
+        const uint32_t colSj =
+            ring ? tmem + lane_base + Cfg::col_buf((2 * j + t) % 3) : colS;
+        softmax_tile_w<D, kNeg, kFp8>(colSj, colO, c2, tlim, j > 0, m_ref, l,
+                                      [&] { mbar_arrive(&sm.p_half[t]); },
+                                      [&] {
+                                        if constexpr (kRing)
+                                          (void)mbar_wait(&sm.pv_done[t], (n_pv - 1) & 1, p.status,
+                                                          abortf, kSitePvDone);
+                                      });
+        if constexpr (kRing) ++n_pv;
         tc_fence_before();
         mbar_arrive(&sm.p_full[t]);
       }

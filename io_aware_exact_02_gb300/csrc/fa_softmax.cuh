@@ -28,11 +28,15 @@ constexpr float kRescaleSlack = 8.0f;  // log2 units
 // probabilities of keys 0-63 are in tensor memory, half_ready() is called,
 // so that the first half of O += P V can run while keys 64-127 are
 // exponentiated.  A warp that rescales O (rarely) calls it only after the
-// rescale, at the end.  Warp-collective (TMEM loads and stores).
-template <int D, bool kNeg, bool kFp8, class HalfReady>
-__device__ __forceinline__ void softmax_tile(uint32_t colS, uint32_t colO, float c2, int tlim,
-                                             bool may_rescale, float& m_ref, float& l,
-                                             HalfReady&& half_ready) {
+// rescale, at the end.  before_rescale() is called before O is read for a
+// rescale: it must return once the previous P V product has written O (the
+// caller's S having completed implies that, unless the tensor core computed
+// S ahead of that product).  Warp-collective (TMEM loads and stores).
+template <int D, bool kNeg, bool kFp8, class HalfReady, class BeforeRescale>
+__device__ __forceinline__ void softmax_tile_w(uint32_t colS, uint32_t colO, float c2, int tlim,
+                                               bool may_rescale, float& m_ref, float& l,
+                                               HalfReady&& half_ready,
+                                               BeforeRescale&& before_rescale) {
   // A masked score is replaced by the value that loses every max (min)
   // and whose exponent c2 * s is -inf, so its probability is exactly 0.
   const float neutral = kNeg ? __int_as_float(0x7f800000) : __int_as_float(0xff800000);
@@ -129,10 +133,11 @@ __device__ __forceinline__ void softmax_tile(uint32_t colS, uint32_t colO, float
   f2_unpack(ls4[0], lsa, lsb);
   l += lsa + lsb;
   tmem_wait_st();
-  // Correct the O accumulator (S being complete means the previous P V
-  // product, which wrote O, is complete too); no product of this tile's P
-  // reads O before the warp's half_ready().
+  // Correct the O accumulator once the previous P V product has written it
+  // (before_rescale); no product of this tile's P reads O before the warp's
+  // half_ready().
   if (rescale) {
+    before_rescale();
 #pragma unroll
     for (int c = 0; c < D / 32; ++c) {
       uint32_t orow[32];
@@ -148,6 +153,13 @@ __device__ __forceinline__ void softmax_tile(uint32_t colS, uint32_t colO, float
       half_ready();
     }
   }
+}
+
+template <int D, bool kNeg, bool kFp8, class HalfReady>
+__device__ __forceinline__ void softmax_tile(uint32_t colS, uint32_t colO, float c2, int tlim,
+                                             bool may_rescale, float& m_ref, float& l,
+                                             HalfReady&& half_ready) {
+  softmax_tile_w<D, kNeg, kFp8>(colS, colO, c2, tlim, may_rescale, m_ref, l, half_ready, [] {});
 }
 
 }  // namespace fa
