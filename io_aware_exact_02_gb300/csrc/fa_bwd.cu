@@ -658,8 +658,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     // step's P phase, while the path idles during the rest of the step.  So
     // kNow of a thread's kGroups float4 groups go out as soon as dQ_i is read;
     // the rest wait in registers and go out after the next step's P phase
-    // (kAfterP of them) and after its dS phase (the others), or at the end
-    // of the item.  Measured (main kernel, TFLOP/s): d = 128, N = 8K 1115
+    // (kAfterP of them) and after its dS phase (the others) -- the next
+    // item's first step for an item's last row -- or at the end.  Measured (main kernel, TFLOP/s): d = 128, N = 8K 1115
     // with all at once, 1272 spread 4/2/2; d = 64 827 -> 887 spread 2/0/2.
     constexpr int kGroups = D / kWG / 4;
     constexpr int kNow = Cfg::kDbl ? 2 : 4;
@@ -715,7 +715,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       if (!ok) break;
       __syncwarp();
       if (lane_id() == 0) mbar_arrive(&sm.item_empty[m & 1]);
-      if (t >= total) break;
+      if (t >= total) {
+        flush_held(0, kHeld);  // the last item's held groups
+        break;
+      }
       const ItemInfo w = item_info(t);
       if (!warp_bound_ok(item_ok(w), p.status, abortf, kChkItem)) {
         ok = false;
@@ -832,7 +835,11 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       if constexpr (Cfg::kDbl) {
         if (w.n_iter > 0 && !(ok = drain_dq(gstep - 1, bh, i_prev))) break;
       }
-      flush_held(0, kHeld);  // the item's last dQ row
+      // The held groups of the item's last dQ row go out during the next
+      // item's first step, after its P and dS phases (as within an item), or
+      // at the end: at an item boundary the SM's write path is busy with the
+      // last row's other reductions and the dK, dV stores below (measured:
+      // +2.6% on the main kernel at N = 1K, +2.5% for B16 H12 N1K d64).
       // Epilogue: the first half of the warpgroups stores dV, the second half
       // scale * dK, each a D / (kWG / 2)-column slice.  The next item's first
       // dV and dK products overwrite these columns only after this warp's
