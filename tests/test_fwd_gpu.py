@@ -69,14 +69,31 @@ def test_fwd_scales(scale, causal):
     compare(o, lse, o_ref, lse_ref, "scale=%g" % scale)
 
 
-def test_fwd_heavy_rows_force_rescaling():
+@pytest.mark.parametrize("d", [64, 128])
+def test_fwd_heavy_rows_force_rescaling(d):
     # 1% of K rows x8 (the long-context recipe) at a size the oracle runs in
-    # full: the running maximum of many rows grows after the first tile.
-    q, k, v, _ = synth.draw(1, 4, 2048, 128, seed=3, heavy_frac=0.01, with_dout=False)
+    # full: the running maximum of many rows grows after the first tile, so
+    # O is rescaled in tensor memory (at d = 64 without a mask after waiting
+    # for the previous P V, which the S ring lets the next S overtake).
+    q, k, v, _ = synth.draw(1, 4, 2048, d, seed=3, heavy_frac=0.01, with_dout=False)
     for causal in (False, True):
-        o, lse = run_fwd(q, k, v, causal, 1 / math.sqrt(128))
-        o_ref, lse_ref = oracle.attn_fwd(q, k, v, causal, 1 / math.sqrt(128))
-        compare(o, lse, o_ref, lse_ref, "heavy causal=%d" % causal)
+        o, lse = run_fwd(q, k, v, causal, 1 / math.sqrt(d))
+        o_ref, lse_ref = oracle.attn_fwd(q, k, v, causal, 1 / math.sqrt(d))
+        compare(o, lse, o_ref, lse_ref, "heavy causal=%d d=%d" % (causal, d))
+
+
+def test_fwd_heavy_rows_persistent_d64():
+    # The same rescaling on persistent CTAs with O staged for TMA stores
+    # (768 items on at most 152 CTAs): scale 0.5 and 3% of K rows x8 make
+    # rescales frequent; sampled rows of the first, last and random heads.
+    from io_aware_exact_02_gb300.synth import Workload
+    w = Workload("heavy_d64", 8, 24, 1024, 64, False, heavy_frac=0.03, scale=0.5)
+    q, k, v, _ = synth.draw_workload(w, seed=17, with_dout=False)
+    dev = torch.device("cuda")
+    o, lse = fa.fwd(q.to(dev), k.to(dev), v.to(dev), causal=False, scale=w.softmax_scale)
+    fa.check_device_status()
+    assert torch.isfinite(o).all() and torch.isfinite(lse).all()
+    sampled_check(w, o, lse, q, k, v, n_heads=4, n_rows=48, seed=5, extra=late_items(w))
 
 
 def test_fwd_deterministic_bitwise():
