@@ -257,6 +257,34 @@ def test_fwd_claimed_items_repeat_bitwise(d):
                   extra=late_items(w))
 
 
+def test_fwd_claimed_items_concurrent_streams():
+    # Masked forward passes in flight at once on two streams use two counter
+    # slots and both give the serial result; so do calls on many more
+    # streams in turn (each stream its own slot, each left at zero).
+    B, H, N, d = 8, 16, 1024, 128
+    q, k, v, _ = synth.draw(B, H, N, d, seed=81, with_dout=False)
+    dev = torch.device("cuda")
+    q, k, v = q.to(dev), k.to(dev), v.to(dev)
+    o_ref, l_ref = fa.fwd(q, k, v, causal=True)
+    torch.cuda.synchronize()
+    streams = [torch.cuda.Stream() for _ in range(24)]
+    outs = []
+    for s in streams[:2]:
+        s.wait_stream(torch.cuda.current_stream())
+    for s in streams[:2]:
+        with torch.cuda.stream(s):
+            outs.append(fa.fwd(q, k, v, causal=True))
+    for s in streams[2:]:
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            outs.append(fa.fwd(q, k, v, causal=True))
+        s.synchronize()
+    torch.cuda.synchronize()
+    fa.check_device_status()
+    for o, l in outs:
+        assert torch.equal(o, o_ref) and torch.equal(l, l_ref)
+
+
 def test_fwd_long_sequence_sampled_rows():
     # N = 65536 (512 key tiles per head) causal and not: sampled rows against
     # the oracle's row-wise definition.
