@@ -1205,6 +1205,8 @@ template <int D, bool kNeg, bool kGeneral, bool kSparse, bool kFp8, bool kStage,
 int launch_fwd_dn(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                   const CUtensorMap& to, const FwdParams& p, cudaStream_t stream) {
   if (kDyn != (p.sched != nullptr)) return FA_ERR_LAUNCH;
+  static_assert(sizeof(FwdSmem<D, kFp8>) + 1024 <= 232448,
+                "forward shared memory above the 227 KB a CTA may have");
   const size_t smem = sizeof(FwdSmem<D, kFp8>) + 1024;
   if (cudaFuncSetAttribute(fa_fwd_kernel<D, kNeg, kGeneral, kSparse, kFp8, kStage, kDyn>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
