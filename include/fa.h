@@ -38,9 +38,11 @@
  *
  * Device state: the first call on a device caches, per device index, the
  * device addresses of the library's static device data (the status word,
- * the no-alloc scratch array) and the SM count.  Do not use the library on
- * a device after cudaDeviceReset() in the same process: the cached
- * addresses belong to the context that the reset destroyed.
+ * the no-alloc scratch array, the forward pass's per-stream work counters)
+ * and the SM count, and each stream that runs a masked forward pass keeps
+ * its counter slot (see fa_fwd_schedule).  Do not use the library on a
+ * device after cudaDeviceReset() in the same process: the cached addresses
+ * belong to the context that the reset destroyed.
  */
 #ifndef FA_H_
 #define FA_H_
