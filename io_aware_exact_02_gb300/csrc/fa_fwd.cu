@@ -1,23 +1,27 @@
 // fa_fwd.cu -- forward pass of exact attention on sm_103a.
 //
-// A work item is 256 query rows (two 128-row Q tiles) of one head.  Without
-// a mask the grid is persistent (one CTA per SM, each walking a share of the
-// items; CMU 11-868 FlashAttention post, slide page 26), so the next item's
-// Q and K/V loads overlap the end of the current one; under a causal mask
-// each item gets a CTA and the block scheduler dispatches the longest-first
-// list greedily (slide pages 27-46).  A CTA keeps both Q tiles in
+// A work item is 256 query rows (two 128-row Q tiles) of one head.  The grid
+// is persistent (one CTA per SM; CMU 11-868 FlashAttention post, slide page
+// 26), so the next item's Q and K/V loads overlap the end of the current
+// one: without a mask each CTA walks a static share of the items; under a
+// causal or block mask the CTAs claim the longest-first list greedily from a
+// work counter (slide pages 27-46).  The producer decodes each item and
+// hands the record to the other roles through a small ring in shared
+// memory.  A CTA keeps both Q tiles in
 // shared memory, streams the head's K and V tiles through a ring of
 // shared-memory slots filled by TMA, and never writes a score to HBM: S
 // lives in tensor memory, P replaces it there as bf16, and only O and the
 // per-row logsumexp are stored (cs2680 Lecture 9, sec. 9.2 and 9.4; CMU post,
 // slide pages 9-12).
 //
-// Warp roles (320 threads; 352 when O is staged):
+// Warp roles (320 threads; 352 when O is staged; 384 at d = 64 and 512 with
+// the epilogue warpgroup, see FwdCfg):
 //   warps 0-3  softmax for Q tile 0 (thread r owns row r of the tile)
 //   warps 4-7  softmax for Q tile 1
-//   warp 8     TMA producer: Q tiles once, then K_0, V_0, K_1, V_1, ...
-//   warp 9     MMA issuer (one thread) and TMEM owner
-//   warp 10    (kStage) O store warp: TMA stores of the staged O tiles
+//   (kEpi)     warps 8-11 the epilogue warpgroup (O out of tensor memory)
+//   then       the TMA producer (Q tiles once, then K_0, V_0, K_1, V_1, ...),
+//              the MMA issuer (one thread, TMEM owner) and, when O is staged,
+//              the O store warp (TMA stores of the staged O tiles)
 // The two softmax warpgroups ping-pong: while one exponentiates its tile
 // the tensor core computes the other tile's S and PV products (the overlap
 // the CMU post motivates on slide pages 20-22 and 51-52).
