@@ -2,9 +2,11 @@
 
 The library keeps no host-side state between calls that a replay would
 repeat wrongly: the backward's work-item counter lives in the caller's
-workspace and is reset by its own prep kernel on every replay, and the
-forward's staged stores need no host state.  Shapes with more work items
-than SMs, so the persistent paths (and the forward's staged O stores) run.
+workspace and is reset by its own prep kernel on every replay; under the
+causal mask the forward's CTAs claim items from the capturing stream's
+counter slot, which every launch (and so every replay) leaves at zero; the
+staged O stores need no host state.  Shapes with more work items than SMs,
+so the persistent paths (and the forward's staged O stores) run.
 """
 import math
 
