@@ -34,7 +34,7 @@ struct DeviceState {
   int sm_count = 0;
   int pair_max = 0;       // forward CTA pairs resident at once (0: not yet known)
   int* fwd_sched = nullptr;                  // device address of g_fwd_sched
-  cudaStream_t sched_stream[kFwdSchedSlots];  // the stream each slot serves
+  unsigned long long sched_stream[kFwdSchedSlots];  // the stream each slot serves (its id)
   int sched_used = 0;
 };
 
@@ -99,13 +99,21 @@ void set_fwd_grid(FwdParams* p, DeviceState* ds, long long items, bool uneven, b
   p->sched = nullptr;
   p->grid = fwd_grid(1, (int)items, uneven ? 1 : 0, ds->sm_count);
   if (!uneven || !claim || items <= ds->sm_count) return;
+  // Streams are told apart by the runtime's stream id, which also tells
+  // apart the per-thread default streams of different threads (they share
+  // one handle value); the handle stands in if the id cannot be had.
+  unsigned long long key = 0;
+  if (cudaStreamGetId(stream, &key) != cudaSuccess) {
+    cudaGetLastError();
+    key = ~reinterpret_cast<uintptr_t>(stream);
+  }
   std::lock_guard<std::mutex> lk(g_mu);
   int slot = -1;
   for (int i = 0; i < ds->sched_used; ++i)
-    if (ds->sched_stream[i] == stream) slot = i;
+    if (ds->sched_stream[i] == key) slot = i;
   if (slot < 0 && ds->sched_used < kFwdSchedSlots) {
     slot = ds->sched_used++;
-    ds->sched_stream[slot] = stream;
+    ds->sched_stream[slot] = key;
   }
   if (slot < 0) return;
   p->sched = ds->fwd_sched + slot * kFwdSchedStride;

@@ -285,6 +285,47 @@ def test_fwd_claimed_items_concurrent_streams():
         assert torch.equal(o, o_ref) and torch.equal(l, l_ref)
 
 
+def test_fwd_claimed_items_per_thread_default_streams():
+    # Two host threads launch masked forward passes on their own per-thread
+    # default streams (one handle value, cudaStreamPerThread, for both): the
+    # library tells the streams apart by their ids, so each gets its own
+    # work-counter slot and both results equal the serial one bitwise.
+    import ctypes
+    import threading
+    B, H, N, d = 8, 16, 1024, 128
+    q, k, v, _ = synth.draw(B, H, N, d, seed=83, with_dout=False)
+    dev = torch.device("cuda")
+    q, k, v = q.to(dev), k.to(dev), v.to(dev)
+    o_ref, l_ref = fa.fwd(q, k, v, causal=True)
+    torch.cuda.synchronize()
+    outs = [(torch.empty_like(q), torch.empty((B, H, N), dtype=torch.float32, device=dev))
+            for _ in range(2)]
+    rcs = [None, None]
+    per_thread = ctypes.c_void_p(2)  # cudaStreamPerThread
+    lib = fa.load()
+
+    def run(i):
+        torch.cuda.set_device(q.device)
+        o, l = outs[i]
+        rc = 0
+        for _ in range(4):
+            rc = rc or lib.fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                  l.data_ptr(), B, H, N, d, 1, ctypes.c_float(1 / math.sqrt(d)),
+                                  per_thread)
+        rcs[i] = rc
+
+    threads = [threading.Thread(target=run, args=(i,)) for i in range(2)]
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join()
+    torch.cuda.synchronize()
+    fa.check_device_status()
+    assert rcs == [0, 0]
+    for o, l in outs:
+        assert torch.equal(o, o_ref) and torch.equal(l, l_ref)
+
+
 def test_fwd_long_sequence_sampled_rows():
     # N = 65536 (512 key tiles per head) causal and not: sampled rows against
     # the oracle's row-wise definition.
