@@ -324,10 +324,10 @@ const char* fa_status_string(int status);
  * num_ctas persistent CTAs claim them from a device work counter as each
  * becomes ready for another, so item_cta is -1 (decided at run time);
  * otherwise item t gets CTA t.  The counter is the library's: one slot per
- * stream (told apart by the runtime's stream id, so the per-thread default
- * streams of different threads get different slots), so launches on one
- * stream (which run in order) share it and launches on different streams do
- * not; a launch leaves its slot as it found it.  A CUDA graph that holds a masked forward pass uses the slot of
+ * stream (streams told apart by handle; cudaStreamPerThread by host thread,
+ * since it names a different stream in each), so launches on one stream
+ * (which run in order) share it and launches on different streams do not; a
+ * launch leaves its slot as it found it.  A CUDA graph that holds a masked forward pass uses the slot of
  * the stream it was captured on: it must not run at the same time as
  * another masked forward pass on that stream, nor twice at once.  After
  * 64 streams on a device have run masked forward passes, calls on further

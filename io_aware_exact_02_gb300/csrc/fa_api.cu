@@ -4,6 +4,7 @@
 // caller's workspace.
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <cmath>
 #include <cstddef>
 #include <cstdint>
@@ -99,14 +100,15 @@ void set_fwd_grid(FwdParams* p, DeviceState* ds, long long items, bool uneven, b
   p->sched = nullptr;
   p->grid = fwd_grid(1, (int)items, uneven ? 1 : 0, ds->sm_count);
   if (!uneven || !claim || items <= ds->sm_count) return;
-  // Streams are told apart by the runtime's stream id, which also tells
-  // apart the per-thread default streams of different threads (they share
-  // one handle value); the handle stands in if the id cannot be had.
-  unsigned long long key = 0;
-  if (cudaStreamGetId(stream, &key) != cudaSuccess) {
-    cudaGetLastError();
-    key = ~reinterpret_cast<uintptr_t>(stream);
-  }
+  // Streams are told apart by their handle, except the per-thread default
+  // stream, whose one handle value names a different stream in every host
+  // thread: it gets a key of the calling thread's own.  (No CUDA call here,
+  // so the lookup is safe while the stream is being captured into a graph.)
+  static std::atomic<unsigned long long> next_thread_key{1};
+  thread_local const unsigned long long thread_key = next_thread_key++;
+  const unsigned long long key =
+      stream == cudaStreamPerThread ? (thread_key | (1ull << 63))
+                                    : (unsigned long long)reinterpret_cast<uintptr_t>(stream);
   std::lock_guard<std::mutex> lk(g_mu);
   int slot = -1;
   for (int i = 0; i < ds->sched_used; ++i)
