@@ -667,6 +667,29 @@ def run_gpu(args, w, rank, world, local_rank):
                             "frac_of_peak": bf / bwd_total / 1e12 / peak}
     if "nominal_at_clock" in tp:
         kernels["bwd_total"]["frac_nominal"] = bf / bwd_total / 1e12 / tp["nominal_at_clock"]
+    # The backward pass as one fa_bwd call, after the timed region (as the N
+    # sweep measures it): its three kernels back to back, each launched with
+    # programmatic dependent launch.  The per-kernel events of the timed step
+    # keep each launch from overlapping the end of the kernel before it,
+    # which at short lengths costs a few microseconds per call.
+    call_s = []
+    for it in range(7):
+        if flush is not None:
+            flush.zero_()
+        c0 = torch.cuda.Event(enable_timing=True)
+        c1 = torch.cuda.Event(enable_timing=True)
+        c0.record(stream)
+        fa.bwd(q, k, v, o, do, lse, causal=causal, scale=scale, dq=dq, dk=dk, dv=dv, workspace=ws)
+        c1.record(stream)
+        torch.cuda.synchronize(dev)
+        if it >= 2:
+            call_s.append(c0.elapsed_time(c1) / 1e3)
+    fa.check_device_status()
+    bwd_call = sum(call_s) / len(call_s)
+    kernels["bwd_call"] = {"ms_per_call": bwd_call * 1e3, "tflops": bf / bwd_call / 1e12,
+                           "frac_of_peak": bf / bwd_call / 1e12 / peak,
+                           "note": "one fa_bwd call, L2 flushed before it when the inputs fit "
+                                   "in L2, after the timed region"}
     hbm_bytes = 8.0 * B * H * N * d + 4.0 * B * H * N  # fwd: Q, K, V read, O written, lse
     kernels["fwd"]["algorithmic_hbm_gbs"] = hbm_bytes / fwd_avg / 1e9
 
