@@ -208,3 +208,26 @@ def test_blocksparse_causal_large_sampled_head():
     refs = oracle.attn_bwd_blockmask(sel(q), sel(k), sel(v), sel(do), True, 1 / math.sqrt(d),
                                      mask.numpy())
     check_bwd((sel(dq), sel(dk), sel(dv)), refs, "causal N4096", mask, True)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_blocksparse_claimed_items_d64_sampled_heads(causal):
+    # d = 64 with more work items (B*H*N/256 = 512) than SMs: the forward's
+    # persistent CTAs claim the items, of uneven cost under the mask, from the
+    # work counter.  Two sampled heads (one of them the last) against the
+    # oracle's block-sparse form, forward and backward.
+    B, H, N, d = 4, 16, 2048, 64
+    q, k, v, do = synth.draw(B, H, N, d, seed=91 + causal)
+    mask = synth.draw_block_mask(16, 0.3, seed=13 + causal)
+    o, lse, dq, dk, dv = run(q, k, v, do, mask, causal, 1 / math.sqrt(d))
+    for head in (5, B * H - 1):
+
+        def sel(t):
+            return t.reshape(B * H, *t.shape[2:])[head][None, None]
+
+        o_ref, lse_ref = oracle.attn_fwd_blockmask(sel(q), sel(k), sel(v), causal,
+                                                   1 / math.sqrt(d), mask.numpy())
+        check_fwd(sel(o), sel(lse), o_ref, lse_ref, "d64 head %d" % head)
+        refs = oracle.attn_bwd_blockmask(sel(q), sel(k), sel(v), sel(do), causal, 1 / math.sqrt(d),
+                                         mask.numpy())
+        check_bwd((sel(dq), sel(dk), sel(dv)), refs, "d64 head %d" % head, mask, causal)
