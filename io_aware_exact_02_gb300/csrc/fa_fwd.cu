@@ -358,11 +358,14 @@ __global__ void __launch_bounds__(FwdCfg<D, kFp8>::threads(kStage), 1)
     return it;
   };
   // The S ring (FwdCfg::kSRing) serves the dense square kernels' items whose
-  // two Q tiles take the same key tiles (every item without a mask); the
-  // others keep one S buffer per Q tile.
+  // Q tile 1 takes all the item's key tiles and Q tile 0 the same or all but
+  // the last (every item without a mask, and under the causal mask, whose
+  // tile 0 ends one key tile earlier); the others keep one S buffer per Q
+  // tile.
   constexpr bool kRing = Cfg::kSRing && !kGeneral && !kSparse;
   auto ring_item = [&](const Item& it) -> bool {
-    return kRing && it.nmax > 0 && it.n_t[0] == it.nmax && it.n_t[1] == it.nmax;
+    return kRing && it.nmax > 0 && it.n_t[1] == it.nmax && it.n_t[0] >= 1 &&
+           it.n_t[0] >= it.nmax - 1;
   };
   // Checked build: the item's head, pair and split exist and its key tiles
   // [j0, j0 + n_t) lie inside the head's.
@@ -712,10 +715,11 @@ __global__ void __launch_bounds__(FwdCfg<D, kFp8>::threads(kStage), 1)
               const int vc = cb + 2 * j + 1, kc = cb + 2 * j + 2;
               ok = wait_full(vc) && (j + 1 >= nmax || wait_full(kc));
               for (int t = 0; t < 2 && ok; ++t) {
+                if (j >= it.n_t[t]) continue;  // Q tile 0 of a causal item: no last step
                 ok = wait_p(t);
                 if (!ok) break;
                 tc_fence_after();
-                if (j + 1 < nmax) {
+                if (j + 1 < it.n_t[t]) {
                   issue_s_at(t, kc % S, Cfg::col_buf((2 * j + t + 2) % 3));
                   if (t == 1) {
                     tc_commit(&sm.kv_empty[kc % S]);
@@ -724,7 +728,7 @@ __global__ void __launch_bounds__(FwdCfg<D, kFp8>::threads(kStage), 1)
                 }
                 ok = issue_pv_at(t, vc % S, j > 0, Cfg::col_buf((2 * j + t) % 3));
                 if (!ok) break;
-                if (j == nmax - 1) tc_commit(&sm.o_full[t]);
+                if (j == it.n_t[t] - 1) tc_commit(&sm.o_full[t]);
               }
               if (ok) tc_commit(&sm.kv_empty[vc % S]);
             }
